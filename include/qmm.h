@@ -1,0 +1,167 @@
+/*
+ * qmm.h — skinny-batch product of a 4-bit k-quant (Q4K) weight matrix with bf16 activations,
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  The pages describe a speculative-decoding verify pass: anchor + k draft
+ * rows go through the target model in one batch, and the quantized matrix products take
+ * 83-92% of the GPU time ("sixi-asi 0.9", section "What I got wrong in 0.8").  Each such
+ * product multiplies a weight matrix stored in 4-bit k-quant form with a skinny batch of
+ * M = 1..32 activation rows.  This library computes exactly that product:
+ *
+ *     Y[i][n] = sum_k  w[n][k] * x[i][k]        0 <= i < M,  0 <= n < N,  0 <= k < K
+ *
+ * with x the bf16 activations, w the dequantized weights (below) and Y in fp32.  On the pages
+ * the matrix-vector kernel decodes the 4-bit weights once per activation row ("sixi-asi 0.9",
+ * same section); every kernel behind this header reads and decodes each weight byte once for
+ * all M rows.
+ *
+ * ------------------------------------------------------------------------------------------
+ * Q4K byte format.  The pages name the format (Q4_K_M GGUF weights, "sixi-asi 0.9" section
+ * "Numbers") but print no byte layout; the fields are 256-weight super-blocks with fp16 d and
+ * dmin, eight 32-weight sub-blocks with a 6-bit scale and a 6-bit min, and 4-bit quants, so
+ * that w = d*sc*q - dmin*m.  This is the byte layout of this library:
+ *
+ *   A row of K weights (K a multiple of 256) is K/256 super-blocks of 256 consecutive weights,
+ *   stored in order of k.  Rows are stored one after another, so super-block b of row n starts
+ *   at byte  (n * (K/256) + b) * 144.  Every super-block is 144 bytes (4.5 bits per weight):
+ *
+ *     bytes [0, 2)    d     IEEE-754 binary16, little-endian   (scale of the scales)
+ *     bytes [2, 4)    dmin  IEEE-754 binary16, little-endian   (scale of the mins)
+ *     bytes [4, 16)   the 96-bit little-endian integer F.  Sub-block j (j = 0..7) owns
+ *                     sc_j = bits [12j, 12j+6) of F and m_j = bits [12j+6, 12j+12) of F,
+ *                     both unsigned 6-bit integers.
+ *     bytes [16, 144) the 1024-bit little-endian integer Q.  Weight t of the super-block
+ *                     (t = 0..255) has the unsigned 4-bit quant q_t = bits [4t, 4t+4) of Q:
+ *                     byte 16 + t/2, low nibble for even t, high nibble for odd t.
+ *                     Weight t belongs to sub-block j = t / 32.
+ *
+ *   Dequantization: with D = fp32(d) and Dm = fp32(dmin), weight t is the single
+ *   round-to-nearest-even fp32 rounding of the exact real number D*sc_j*q_t - Dm*m_j.  (Both
+ *   products are exact in fp32; the difference is rounded once.)  A zero weight is -0 exactly
+ *   when D*sc_j*q_t is -0 and Dm*m_j is +0 (the IEEE-754 sign rule for a difference of
+ *   zeros), otherwise +0.  qmm_dequant returns these values bit for bit.
+ *
+ * Quantizer used by qmm_pack (the pages give none; this is the plain asymmetric min/max rule):
+ *   for each super-block and each sub-block j of 32 weights w_t:
+ *     lo_j = min(0, min_t w_t),  hi_j = max_t w_t,  scale_j = (hi_j - lo_j)/15,  off_j = 0 - lo_j
+ *   d = fp16(max(0, max_j scale_j) / 63), dmin = fp16(max(0, max_j off_j) / 63)
+ *       (binary16 round to nearest even; the maxima start from +0, so no -0 is stored)
+ *   sc_j = D > 0  ? clamp(rint(scale_j / D), 0, 63)  : 0
+ *   m_j  = Dm > 0 ? clamp(rint(off_j / Dm), 0, 63)   : 0
+ *   q_t  = D*sc_j > 0 ? clamp(rint((w_t + Dm*m_j) / (D*sc_j)), 0, 15) : 0
+ *   All arithmetic is IEEE fp32, round to nearest even, each operation rounded separately.
+ *
+ * ------------------------------------------------------------------------------------------
+ * Conventions for every call below.
+ *   - Pointers named *_dev are CUDA device pointers, *_host are host pointers.  All buffers
+ *     are owned by the caller; the library keeps no pointer after a call returns.
+ *   - X is M x K row-major bf16 (raw bit patterns in uint16_t), Y is M x N row-major fp32.
+ *     Wq and X must be 16-byte aligned; Y must be 4-byte aligned.  Y is overwritten, never
+ *     accumulated, and must not overlap Wq or X.
+ *   - 1 <= M <= 32, 1 <= N < 2^31, 256 <= K < 2^31, K % 256 == 0.
+ *   - GPU calls are asynchronous: they validate their arguments on the host, enqueue work on
+ *     `stream` (0 = the legacy default stream) and return.  Argument errors are returned
+ *     before anything is enqueued.  A launch failure returns QMM_ERR_CUDA (the CUDA error
+ *     text is available from qmm_last_cuda_error).  Faults that happen while a kernel runs
+ *     surface at the caller's next synchronization, as for any CUDA kernel.
+ *   - The library allocates no device memory on any call.  Calls on different streams may
+ *     run concurrently; the only mutable global state is a per-device cache of launch
+ *     attributes, written once under a lock.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMM_QK          256   /* weights per super-block                         */
+#define QMM_BLOCK_BYTES 144   /* bytes per super-block                           */
+#define QMM_MAX_M       32    /* largest activation batch (rows of X)            */
+#define QMM_MAX_BATCH   512   /* largest entry count of one qmm_run_batched call */
+
+typedef enum {
+  QMM_OK = 0,
+  QMM_ERR_NULL = 1,       /* a required pointer is NULL                                   */
+  QMM_ERR_SHAPE = 2,      /* N or K out of range, or K % 256 != 0                          */
+  QMM_ERR_M_RANGE = 3,    /* M outside [1, 32]                                             */
+  QMM_ERR_ALIGN = 4,      /* Wq or X not 16-byte aligned, or Y not 4-byte aligned          */
+  QMM_ERR_BUFSIZE = 5,    /* caller buffer smaller than required                          */
+  QMM_ERR_NONFINITE = 6,  /* qmm_pack: a weight is Inf/NaN or a scale overflows fp16      */
+  QMM_ERR_CUDA = 7,       /* a CUDA runtime call or kernel launch failed                   */
+  QMM_ERR_COUNT = 8,      /* qmm_run_batched: count outside [1, QMM_MAX_BATCH]              */
+  QMM_ERR_VARIANT = 9     /* an explicitly requested kernel variant cannot run this shape  */
+} qmm_status;
+
+/* Bytes of the packed form of an N x K weight matrix: N * (K/256) * 144.
+ * Returns 0 when the shape is invalid (see QMM_ERR_SHAPE). */
+size_t qmm_packed_bytes(int64_t N, int64_t K);
+
+/* Pack W_host (N x K row-major fp32, host memory) into the Q4K format above, written to the
+ * caller's host buffer out_host of out_bytes >= qmm_packed_bytes(N, K) bytes.  Runs on the
+ * host CPU (the cold path: weights are packed once), on up to `threads` threads (<= 0: all
+ * hardware threads).  Errors: QMM_ERR_NULL, QMM_ERR_SHAPE, QMM_ERR_BUFSIZE,
+ * QMM_ERR_NONFINITE; out_host is unspecified after an error. */
+qmm_status qmm_pack(const float* W_host, int64_t N, int64_t K, void* out_host, size_t out_bytes,
+                    int threads);
+
+/* Y_dev[M x N] = X_dev[M x K] * dequant(Wq_dev)^T, enqueued on `stream`.
+ * Wq_dev: packed weights on the device (qmm_packed_bytes(N, K) bytes, 16-byte aligned).
+ * X_dev: bf16 activations; Y_dev: fp32 result (overwritten).  The kernel variant is chosen
+ * from (M, N, K) by the library's measured dispatch table (qmm_select_variant). */
+qmm_status qmm_run(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
+                   float* Y_dev, int M, cudaStream_t stream);
+
+/* One entry of a batched call: an independent product Y = X * dequant(Wq)^T. */
+typedef struct {
+  const void* Wq;      /* device, packed N x K */
+  const uint16_t* X;   /* device, M x K bf16   */
+  float* Y;            /* device, M x N fp32   */
+  int64_t N;
+  int64_t K;
+} qmm_entry;
+
+/* Run `count` independent products that share one M, in ONE kernel launch on `stream`.
+ * This is one pass over a model's layer matrices when every stream shares the pass
+ * ("sixi-asi 0.11", section "Why sixteen streams were the ceiling"): many matrices, each
+ * weight read once.  Entries may share X; the Y buffers must not overlap each other, any X
+ * or any Wq.  entries_host is read during the call only (the work list travels in the
+ * kernel's parameters; nothing is allocated).  Every entry is validated as in qmm_run; the
+ * first invalid entry's error is returned and nothing is launched. */
+qmm_status qmm_run_batched(const qmm_entry* entries_host, int count, int M, cudaStream_t stream);
+
+/* Test hook: out_dev[N x K] (fp32, row-major) = the dequantized weights, computed on the
+ * device with the same decode steps the product kernels use.  Bit-exact to the definition. */
+qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
+                       cudaStream_t stream);
+
+/* Kernel variants.  qmm_run picks one from the dispatch table; qmm_run_variant forces one
+ * (tests and benchmarks use it to measure the switch point between them). */
+typedef enum {
+  QMM_VARIANT_AUTO = 0,
+  QMM_VARIANT_FMA = 1,   /* CUDA cores: in-register dequant, fp32 FMA, warp-shuffle K reduce */
+  QMM_VARIANT_TC = 2     /* tcgen05 tensor cores, fp32 accumulators in tensor memory        */
+} qmm_variant;
+
+/* As qmm_run with a forced variant; QMM_ERR_VARIANT if that variant cannot run the shape. */
+qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
+                           float* Y_dev, int M, int variant, cudaStream_t stream);
+
+/* The variant qmm_run uses for this shape (never QMM_VARIANT_AUTO). */
+int qmm_select_variant(int M, int64_t N, int64_t K);
+
+/* Human-readable text of a status code (static storage). */
+const char* qmm_strerror(qmm_status status);
+
+/* Text of the CUDA error behind the last QMM_ERR_CUDA returned on this thread. */
+const char* qmm_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */
