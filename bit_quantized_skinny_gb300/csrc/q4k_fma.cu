@@ -1,0 +1,386 @@
+// q4k_fma.cu — the CUDA-core variant of the skinny Q4K x bf16 product (sm_103a).
+//
+// The pages' verify-pass profile ("sixi-asi 0.9", section "What I got wrong in 0.8") spends its
+// time in a matrix-vector kernel that decodes the 4-bit weights again for every activation row,
+// and in a matrix kernel that is latency-bound because too few bytes are in flight (section
+// "The patch": one 256-thread block per SM, 29% of DRAM bandwidth).  This kernel reads and
+// decodes every weight once for all rows of X and keeps tens of kilobytes per SM in flight:
+//
+//   * Work: a product is cut into row ranges (tasks); one CTA of 8 warps owns a task.  Within a
+//     task the K axis is cut into chunks of 4 super-blocks (1024 weights, 576 bytes per row) and
+//     the (chunk, 4-row box) units are dealt to the 8 warps in equal contiguous slices.
+//   * Streaming: each warp has its own 4-stage ring in shared memory.  One bulk copy
+//     (cp.async.bulk, completion on an mbarrier) per row brings a box of 4 rows x 576 bytes; the
+//     copy for box u+4 is issued as soon as box u is consumed.
+//   * Decode: lane l owns sub-block l%8 of super-block l/8 of the chunk: 32 weights, 16 bytes of
+//     quants.  Its 32 activations per row of X live in registers as fp32 pairs, loaded once per
+//     chunk.  Nibbles become exact fp32 values (exponent trick + one add.f32x2 per pair), the
+//     dot product runs on fma.f32x2, and the scales are applied once per sub-block:
+//     part = (D*sc_j) * sum_t q_t x_t - (Dm*m_j) * sum_t x_t.
+//   * K-reduction: a warp-shuffle butterfly sums the 32 lanes (one chunk) for the 4 rows x MT
+//     activation rows of a box; chunk partials go to shared memory and are summed over the
+//     chunks in increasing order at the end of the task.  The order of every addition depends
+//     only on K, so an M-row product is bitwise equal to M one-row products.
+#include <cmath>
+#include <cstdio>
+#include <algorithm>
+#include <vector>
+#include <mutex>
+
+#include "q4k_device.cuh"
+#include "q4k_internal.h"
+
+namespace q4k {
+
+__device__ unsigned g_status;
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRB = 4;        // rows per box
+constexpr int kStages = 4;    // ring depth per warp
+constexpr int kBoxBytes = kRB * kChunkBytes;               // 2304
+constexpr int kRingBytes = kWarps * kStages * kBoxBytes;   // 73728
+constexpr int kBarBytes = kWarps * kStages * 8;            // 256
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kMinBlocksPerSM = 2;
+
+struct FmaEntry {
+  const uint8_t* W;
+  const uint16_t* X;
+  float* Y;
+  int N;
+  int K;
+  int ranges;          // row ranges of this product (per pass)
+  int rows_per_range;  // ceil(N / ranges)
+  int task_begin;      // first task index of this entry
+  int pad_;
+};
+
+template <int MAXE>
+struct FmaParams {
+  int count;
+  int M;
+  int passes;
+  int tasks_total;
+  int partial_cap;  // max over entries of rows_per_range * chunks (partial-buffer floats / MT)
+  int pad_[3];
+  FmaEntry e[MAXE];
+};
+
+template <int MT, int MAXE>
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSM)
+q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t ring = smem_addr(smem) + warp * kStages * kBoxBytes;
+  const uint32_t bars = smem_addr(smem + kRingBytes) + warp * kStages * 8;
+  float* partial = reinterpret_cast<float*>(smem + kRingBytes + kBarBytes);
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(bars + 8 * s, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const uint64_t pol = policy_evict_first();
+  uint32_t boxes_done = 0;    // boxes consumed by this warp so far (ring position)
+  uint32_t boxes_issued = 0;  // boxes issued by this warp so far
+  bool failed = false;
+
+  for (int t = blockIdx.x; t < P.tasks_total; t += gridDim.x) {
+    // ---- locate the task: entry, pass, row range
+    int e = 0;
+    if (MAXE > 1) {
+      int lo = 0, hi = P.count - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.e[mid].task_begin <= t) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
+    }
+    const FmaEntry& E = P.e[e];
+    const int local = t - E.task_begin;
+    const int pass = local / E.ranges;
+    const int range = local - pass * E.ranges;
+    const int r0 = range * E.rows_per_range;
+    const int r1 = min(E.N, r0 + E.rows_per_range);
+    const int i0 = pass * MT;
+    const int nb = E.K >> 8;
+    const int nch = (nb + kChunkBlocks - 1) / kChunkBlocks;
+    const int rows = r1 - r0;
+    const int nrb = (rows + kRB - 1) / kRB;
+    const int T = nch * nrb;
+    const int u_begin = (int)((int64_t)warp * T / kWarps);
+    const int u_end = (int)((int64_t)(warp + 1) * T / kWarps);
+    const int64_t rowbytes = (int64_t)nb * kBlockBytes;
+    const uint8_t* W = E.W;
+
+    auto issue = [&](int u) {
+      const int c = u / nrb;
+      const int rb = u - c * nrb;
+      const int row0 = r0 + rb * kRB;
+      const int nval = min(kRB, r1 - row0);
+      const uint32_t cb = (uint32_t)min(kChunkBlocks, nb - c * kChunkBlocks) * kBlockBytes;
+      const uint32_t stage = boxes_issued % kStages;
+      const uint32_t bar = bars + 8 * stage;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(bar, nval * cb);
+      __syncwarp();
+      if (lane < nval)
+        bulk_g2s(ring + stage * kBoxBytes + lane * kChunkBytes,
+                 W + (int64_t)(row0 + lane) * rowbytes + (int64_t)c * kChunkBytes, cb, bar, pol);
+      ++boxes_issued;
+    };
+
+    if (!failed)
+      for (int u = u_begin; u < min(u_end, u_begin + kStages); ++u) issue(u);
+
+    uint64_t xp[MT][16];
+    float negxs[MT];
+    int cur_c = -1;
+    bool lane_valid = false;
+
+    for (int u = u_begin; u < u_end && !failed; ++u) {
+      const int c = u / nrb;
+      const int rb = u - c * nrb;
+      if (c != cur_c) {
+        // activations of this lane's sub-block for rows i0..i0+MT-1, as fp32 pairs
+        cur_c = c;
+        const int kb = c * kChunkBlocks + (lane >> 3);
+        lane_valid = kb < nb;
+        const int64_t k0 = (int64_t)c * kChunkWeights + lane * 32;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          uint4 v[4];
+          if (lane_valid && i0 + i < P.M) {
+            const uint16_t* xr = E.X + (int64_t)(i0 + i) * E.K + k0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) v[g] = ldg_nc_v4(xr + 8 * g);
+          } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) v[g] = make_uint4(0, 0, 0, 0);
+          }
+          float s = 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t w4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float lo = __uint_as_float(w4[h] << 16);
+              const float hi = __uint_as_float(w4[h] & 0xFFFF0000u);
+              xp[i][4 * g + h] = f2pack(lo, hi);
+              s += lo;
+              s += hi;
+            }
+          }
+          negxs[i] = -s;
+        }
+      }
+
+      const uint32_t stage = boxes_done % kStages;
+      const uint32_t parity = (boxes_done / kStages) & 1u;
+      if (!mbar_wait(bars + 8 * stage, parity, kWaitLimit)) {
+        atomicOr(&g_status, kErrWaitTimeout);
+        failed = true;
+        break;
+      }
+
+      constexpr int V = kRB * (MT == 1 ? 1 : (MT == 2 ? 2 : 4));
+      float vals[V];
+#pragma unroll
+      for (int k = 0; k < V; ++k) vals[k] = 0.f;
+
+      const int row0 = r0 + rb * kRB;
+      const uint32_t sb = ring + stage * kBoxBytes + (lane >> 3) * kBlockBytes;
+#pragma unroll
+      for (int s = 0; s < kRB; ++s) {
+        if (row0 + s < r1) {
+          const uint4 h = lds128(sb + s * kChunkBytes);
+          const uint4 q = lds128(sb + s * kChunkBytes + 16 + 16 * (lane & 7));
+          const SubScale sc = decode_scales(h, lane & 7);
+          const Quads w0 = nibbles_to_f32(q.x);
+          const Quads w1 = nibbles_to_f32(q.y);
+          const Quads w2 = nibbles_to_f32(q.z);
+          const Quads w3 = nibbles_to_f32(q.w);
+#pragma unroll
+          for (int i = 0; i < MT; ++i) {
+            uint64_t a = fma2(w0.p01, xp[i][0], 0ull);
+            a = fma2(w0.p23, xp[i][1], a);
+            a = fma2(w0.p45, xp[i][2], a);
+            a = fma2(w0.p67, xp[i][3], a);
+            a = fma2(w1.p01, xp[i][4], a);
+            a = fma2(w1.p23, xp[i][5], a);
+            a = fma2(w1.p45, xp[i][6], a);
+            a = fma2(w1.p67, xp[i][7], a);
+            uint64_t b = fma2(w2.p01, xp[i][8], 0ull);
+            b = fma2(w2.p23, xp[i][9], b);
+            b = fma2(w2.p45, xp[i][10], b);
+            b = fma2(w2.p67, xp[i][11], b);
+            b = fma2(w3.p01, xp[i][12], b);
+            b = fma2(w3.p23, xp[i][13], b);
+            b = fma2(w3.p45, xp[i][14], b);
+            b = fma2(w3.p67, xp[i][15], b);
+            const float2 fa = f2unpack(a), fb = f2unpack(b);
+            const float dot = (fa.x + fa.y) + (fb.x + fb.y);
+            const float part = fmaf(sc.dmm, negxs[i], sc.dsc * dot);
+            vals[s * (V / kRB) + i] = lane_valid ? part : 0.f;
+          }
+        }
+      }
+      __syncwarp();
+      ++boxes_done;
+      if (u + kStages < u_end) issue(u + kStages);
+
+      butterfly_reduce<V>(vals, lane);
+      constexpr int span = 32 / V;
+      if ((lane & (span - 1)) == 0) {
+        const int idx = lane / span;
+        const int s = idx / (V / kRB);
+        const int i = idx - s * (V / kRB);
+        if (i < MT && row0 + s < r1)
+          partial[((row0 - r0 + s) * nch + c) * MT + i] = vals[0];
+      }
+    }
+    __syncthreads();
+
+    // ---- sum the chunk partials in increasing chunk order and write Y
+    for (int idx = threadIdx.x; idx < rows * MT; idx += kThreads) {
+      const int i = idx / rows;
+      const int rl = idx - i * rows;
+      if (i0 + i < P.M) {
+        float y = 0.f;
+        for (int c = 0; c < nch; ++c) y += partial[(rl * nch + c) * MT + i];
+        E.Y[(int64_t)(i0 + i) * E.N + r0 + rl] = y;
+      }
+    }
+    __syncthreads();
+  }
+
+  // After a timed-out wait, give the copies still in flight a bounded time to land.
+  if (failed) {
+    while (boxes_done < boxes_issued) {
+      const uint32_t stage = boxes_done % kStages;
+      const uint32_t parity = (boxes_done / kStages) & 1u;
+      if (!mbar_wait(bars + 8 * stage, parity, kWaitLimit)) break;
+      ++boxes_done;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Host side: task planning and launch.
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+DeviceInfo device_info() {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DeviceInfo{};
+  std::lock_guard<std::mutex> g(mu);
+  if (!cache[dev].ok) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DeviceInfo{};
+    cache[dev].sms = sms;
+    cache[dev].ok = true;
+  }
+  return cache[dev];
+}
+
+constexpr int kMaxSmem = 113 * 1024;  // two CTAs per SM
+
+template <int MT, int MAXE>
+cudaError_t launch_fma_t(const Job* jobs, int count, int M, cudaStream_t stream) {
+  static_assert(sizeof(FmaParams<MAXE>) < 32000, "kernel parameters too large");
+  const DeviceInfo dev = device_info();
+  if (!dev.ok) return cudaErrorInvalidDevice;
+  const int passes = (M + MT - 1) / MT;
+  const int slots = dev.sms * kMinBlocksPerSM;
+
+  FmaParams<MAXE> P;
+  P.count = count;
+  P.M = M;
+  P.passes = passes;
+  double total_bytes = 0;
+  for (int k = 0; k < count; ++k) total_bytes += (double)jobs[k].N * (double)(jobs[k].K / 256) * 144.0;
+  const double per_slot = total_bytes / slots;
+
+  // Rows per range: a fair share of the weight bytes, at least one 4-row box, and a partial
+  // buffer that keeps two CTAs per SM.
+  int tasks = 0, partial_cap = 1;
+  for (int k = 0; k < count; ++k) {
+    const int64_t N = jobs[k].N, K = jobs[k].K;
+    const int nb = (int)(K / 256);
+    const int nch = (nb + kChunkBlocks - 1) / kChunkBlocks;
+    const double bytes = (double)N * nb * 144.0;
+    int64_t ranges = (int64_t)std::max(1.0, std::floor(bytes / per_slot + 0.5));
+    ranges = std::min<int64_t>(ranges, (N + kRB - 1) / kRB);
+    int64_t rpr = (N + ranges - 1) / ranges;
+    const int64_t max_rows = (kMaxSmem - kRingBytes - kBarBytes) / ((int64_t)nch * MT * 4);
+    if (rpr > max_rows) rpr = std::max<int64_t>(kRB, (max_rows / kRB) * kRB);
+    ranges = (N + rpr - 1) / rpr;
+    FmaEntry& E = P.e[k];
+    E.W = static_cast<const uint8_t*>(jobs[k].W);
+    E.X = jobs[k].X;
+    E.Y = jobs[k].Y;
+    E.N = (int)N;
+    E.K = (int)K;
+    E.ranges = (int)ranges;
+    E.rows_per_range = (int)rpr;
+    E.task_begin = tasks;
+    E.pad_ = 0;
+    tasks += (int)ranges * passes;
+    partial_cap = std::max<int>(partial_cap, (int)(rpr * nch));
+  }
+  P.tasks_total = tasks;
+  P.partial_cap = partial_cap;
+  const size_t smem = kRingBytes + kBarBytes + (size_t)partial_cap * MT * sizeof(float);
+  if (smem > (size_t)kMaxSmem) return cudaErrorInvalidConfiguration;
+
+  auto kern = q4k_fma_kernel<MT, MAXE>;
+  static std::mutex attr_mu;
+  static bool attr_set[64] = {};
+  int devno = 0;
+  cudaError_t err = cudaGetDevice(&devno);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> g(attr_mu);
+    if (devno >= 64 || !attr_set[devno]) {
+      err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+      if (err != cudaSuccess) return err;
+      if (devno < 64) attr_set[devno] = true;
+    }
+  }
+  const int grid = std::min(tasks, slots);
+  kern<<<grid, kThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fma(const Job* jobs, int count, int M, cudaStream_t stream) {
+  if (count == 1) {
+    return (M == 1) ? launch_fma_t<1, 1>(jobs, count, M, stream)
+                    : launch_fma_t<2, 1>(jobs, count, M, stream);
+  }
+  return (M == 1) ? launch_fma_t<1, 512>(jobs, count, M, stream)
+                  : launch_fma_t<2, 512>(jobs, count, M, stream);
+}
+
+cudaError_t read_and_clear_device_status(unsigned* out) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+  *out = v;
+  return e;
+}
+
+}  // namespace q4k

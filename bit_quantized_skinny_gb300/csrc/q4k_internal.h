@@ -1,0 +1,34 @@
+// q4k_internal.h — launch interface between the C-ABI layer (qmm_api.cpp) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace q4k {
+
+// One product handed to a kernel: Y[M x N] = X[M x K] * dequant(W)^T.
+struct Job {
+  const void* W;
+  const uint16_t* X;
+  float* Y;
+  int64_t N;
+  int64_t K;
+};
+
+// Launch the CUDA-core (fma) kernel over `count` jobs sharing M, in one launch.
+// Returns a cudaError_t (cudaSuccess when enqueued).
+cudaError_t launch_fma(const Job* jobs, int count, int M, cudaStream_t stream);
+
+// Launch the tensor-core (tcgen05) kernel; cudaErrorNotSupported when it cannot run the shape.
+cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream);
+bool tc_supports(int M, int64_t N, int64_t K);
+
+// Device dequantization test hook.
+cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
+
+// Device status word: read and clear (synchronous; 0 = no error).
+cudaError_t read_and_clear_device_status(unsigned* out);
+
+// Host packer (qmm_pack.cpp).  Returns 0, or 6 on non-finite input / fp16 overflow.
+int pack_q4k(const float* W, int64_t N, int64_t K, uint8_t* out, int threads);
+
+}  // namespace q4k

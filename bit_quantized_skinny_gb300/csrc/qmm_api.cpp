@@ -1,0 +1,152 @@
+// qmm_api.cpp — the C ABI (include/qmm.h): argument validation, variant dispatch, launches.
+//
+// Dispatch follows the pages' "switch point" idea ("sixi-asi 0.9", section "The patch": the
+// row count at which the skinny product moves from one kernel family to another, tuned per
+// GPU).  Here the families are the CUDA-core kernel (q4k_fma.cu) and the tensor-core kernel;
+// the switch point below is the measured one for GB300.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <cuda_runtime_api.h>
+
+#include "../../include/qmm.h"
+#include "q4k_internal.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "no error";
+
+qmm_status cuda_fail(cudaError_t e) {
+  const char* s = cudaGetErrorString(e);
+  std::strncpy(g_last_cuda_error, s ? s : "unknown CUDA error", sizeof(g_last_cuda_error) - 1);
+  g_last_cuda_error[sizeof(g_last_cuda_error) - 1] = 0;
+  return QMM_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qmm_status check_shape(int64_t N, int64_t K) {
+  if (N < 1 || N >= (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+  if (K < 256 || K > (int64_t(1) << 20) || K % 256 != 0) return QMM_ERR_SHAPE;
+  return QMM_OK;
+}
+
+qmm_status check_job(const void* W, int64_t N, int64_t K, const uint16_t* X, const float* Y) {
+  if (!W || !X || !Y) return QMM_ERR_NULL;
+  qmm_status s = check_shape(N, K);
+  if (s != QMM_OK) return s;
+  if (!aligned(W, 16) || !aligned(X, 16) || !aligned(Y, 4)) return QMM_ERR_ALIGN;
+  return QMM_OK;
+}
+
+// Largest M that the CUDA-core kernel serves when the caller lets the library choose.
+// (Measured switch point on GB300; see the bench's sweep.)
+constexpr int kFmaMaxM = 32;
+
+int select_variant(int M, int64_t N, int64_t K) {
+  if (M <= kFmaMaxM || !q4k::tc_supports(M, N, K)) return QMM_VARIANT_FMA;
+  return QMM_VARIANT_TC;
+}
+
+qmm_status run_jobs(const q4k::Job* jobs, int count, int M, int variant, cudaStream_t stream) {
+  if (variant == QMM_VARIANT_AUTO) {
+    variant = QMM_VARIANT_TC;
+    for (int k = 0; k < count; ++k)
+      if (select_variant(M, jobs[k].N, jobs[k].K) == QMM_VARIANT_FMA) variant = QMM_VARIANT_FMA;
+  }
+  cudaError_t e;
+  if (variant == QMM_VARIANT_FMA) {
+    e = q4k::launch_fma(jobs, count, M, stream);
+  } else if (variant == QMM_VARIANT_TC) {
+    for (int k = 0; k < count; ++k)
+      if (!q4k::tc_supports(M, jobs[k].N, jobs[k].K)) return QMM_ERR_VARIANT;
+    e = q4k::launch_tc(jobs, count, M, stream);
+  } else {
+    return QMM_ERR_VARIANT;
+  }
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qmm_packed_bytes(int64_t N, int64_t K) {
+  if (check_shape(N, K) != QMM_OK) return 0;
+  return (size_t)N * (size_t)(K / 256) * QMM_BLOCK_BYTES;
+}
+
+qmm_status qmm_pack(const float* W_host, int64_t N, int64_t K, void* out_host, size_t out_bytes,
+                    int threads) {
+  if (!W_host || !out_host) return QMM_ERR_NULL;
+  qmm_status s = check_shape(N, K);
+  if (s != QMM_OK) return s;
+  if (out_bytes < qmm_packed_bytes(N, K)) return QMM_ERR_BUFSIZE;
+  const int rc = q4k::pack_q4k(W_host, N, K, static_cast<uint8_t*>(out_host), threads);
+  return rc == 0 ? QMM_OK : QMM_ERR_NONFINITE;
+}
+
+qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
+                           float* Y_dev, int M, int variant, cudaStream_t stream) {
+  qmm_status s = check_job(Wq_dev, N, K, X_dev, Y_dev);
+  if (s != QMM_OK) return s;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  const q4k::Job job{Wq_dev, X_dev, Y_dev, N, K};
+  return run_jobs(&job, 1, M, variant, stream);
+}
+
+qmm_status qmm_run(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev, float* Y_dev,
+                   int M, cudaStream_t stream) {
+  return qmm_run_variant(Wq_dev, N, K, X_dev, Y_dev, M, QMM_VARIANT_AUTO, stream);
+}
+
+qmm_status qmm_run_batched(const qmm_entry* entries_host, int count, int M, cudaStream_t stream) {
+  if (!entries_host) return QMM_ERR_NULL;
+  if (count < 1 || count > QMM_MAX_BATCH) return QMM_ERR_COUNT;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  q4k::Job jobs[QMM_MAX_BATCH];
+  for (int k = 0; k < count; ++k) {
+    const qmm_entry& e = entries_host[k];
+    qmm_status s = check_job(e.Wq, e.N, e.K, e.X, e.Y);
+    if (s != QMM_OK) return s;
+    jobs[k] = q4k::Job{e.Wq, e.X, e.Y, e.N, e.K};
+  }
+  return run_jobs(jobs, count, M, QMM_VARIANT_AUTO, stream);
+}
+
+qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev, cudaStream_t stream) {
+  if (!Wq_dev || !out_dev) return QMM_ERR_NULL;
+  qmm_status s = check_shape(N, K);
+  if (s != QMM_OK) return s;
+  if (!aligned(Wq_dev, 16) || !aligned(out_dev, 16)) return QMM_ERR_ALIGN;
+  cudaError_t e = q4k::launch_dequant(Wq_dev, N, K, out_dev, stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
+int qmm_select_variant(int M, int64_t N, int64_t K) { return select_variant(M, N, K); }
+
+qmm_status qmm_device_status(unsigned* status_out) {
+  if (!status_out) return QMM_ERR_NULL;
+  cudaError_t e = q4k::read_and_clear_device_status(status_out);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
+const char* qmm_strerror(qmm_status status) {
+  switch (status) {
+    case QMM_OK: return "ok";
+    case QMM_ERR_NULL: return "a required pointer is NULL";
+    case QMM_ERR_SHAPE: return "invalid shape: need 1 <= N < 2^31, 256 <= K <= 2^20, K % 256 == 0";
+    case QMM_ERR_M_RANGE: return "M must be in [1, 32]";
+    case QMM_ERR_ALIGN: return "Wq and X must be 16-byte aligned, Y 4-byte aligned";
+    case QMM_ERR_BUFSIZE: return "output buffer too small";
+    case QMM_ERR_NONFINITE: return "non-finite weight or fp16 overflow of a super-block scale";
+    case QMM_ERR_CUDA: return "CUDA error (see qmm_last_cuda_error)";
+    case QMM_ERR_COUNT: return "batched entry count must be in [1, QMM_MAX_BATCH]";
+    case QMM_ERR_VARIANT: return "the requested kernel variant cannot run this shape";
+  }
+  return "unknown status";
+}
+
+const char* qmm_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

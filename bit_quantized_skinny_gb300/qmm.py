@@ -1,0 +1,161 @@
+"""ctypes binding of libqmm.so (include/qmm.h): argument marshalling only.
+
+Every step of the product runs in the library's CUDA kernels; this module passes device
+pointers (``tensor.data_ptr()``), sizes and the caller's current CUDA stream.  There is no
+fallback: if the library is missing or cannot load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmm.so")
+
+QMM_QK = 256
+QMM_BLOCK_BYTES = 144
+QMM_MAX_M = 32
+QMM_MAX_BATCH = 512
+
+VARIANT_AUTO, VARIANT_FMA, VARIANT_TC = 0, 1, 2
+VARIANT_NAMES = {VARIANT_FMA: "fma", VARIANT_TC: "tc"}
+
+STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANGE",
+          4: "QMM_ERR_ALIGN", 5: "QMM_ERR_BUFSIZE", 6: "QMM_ERR_NONFINITE", 7: "QMM_ERR_CUDA",
+          8: "QMM_ERR_COUNT", 9: "QMM_ERR_VARIANT"}
+
+# Every symbol include/qmm.h declares.
+EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",
+           "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
+           "qmm_last_cuda_error"]
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        lib = _lib
+        text = lib.qmm_strerror(status).decode() if lib is not None else STATUS.get(status, "?")
+        if status == 7 and lib is not None:
+            text += ": " + lib.qmm_last_cuda_error().decode()
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({text})")
+
+
+class _Entry(ctypes.Structure):
+    _fields_ = [("Wq", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libqmm.so (raises if it is missing: build it with build_lib.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libqmm.so not found at {p}: run bit_quantized_skinny_gb300.build_lib.build()")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
+    lib.qmm_packed_bytes.argtypes = [i64, i64]
+    lib.qmm_packed_bytes.restype = ctypes.c_size_t
+    lib.qmm_pack.argtypes = [vp, i64, i64, vp, ctypes.c_size_t, i32]
+    lib.qmm_pack.restype = i32
+    lib.qmm_run.argtypes = [vp, i64, i64, vp, vp, i32, vp]
+    lib.qmm_run.restype = i32
+    lib.qmm_run_variant.argtypes = [vp, i64, i64, vp, vp, i32, i32, vp]
+    lib.qmm_run_variant.restype = i32
+    lib.qmm_run_batched.argtypes = [ctypes.POINTER(_Entry), i32, i32, vp]
+    lib.qmm_run_batched.restype = i32
+    lib.qmm_dequant.argtypes = [vp, i64, i64, vp, vp]
+    lib.qmm_dequant.restype = i32
+    lib.qmm_select_variant.argtypes = [i32, i64, i64]
+    lib.qmm_select_variant.restype = i32
+    lib.qmm_device_status.argtypes = [ctypes.POINTER(u32)]
+    lib.qmm_device_status.restype = i32
+    lib.qmm_strerror.argtypes = [i32]
+    lib.qmm_strerror.restype = ctypes.c_char_p
+    lib.qmm_last_cuda_error.argtypes = []
+    lib.qmm_last_cuda_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise QmmError(status, what)
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def packed_bytes(N: int, K: int) -> int:
+    return load().qmm_packed_bytes(N, K)
+
+
+def pack(W: np.ndarray, threads: int = 0, out: np.ndarray | None = None) -> np.ndarray:
+    """Pack an N x K fp32 host array into Q4K bytes (host, multi-threaded)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    nbytes = packed_bytes(N, K)
+    if nbytes == 0:
+        raise QmmError(2, "qmm_pack")
+    if out is None:
+        out = np.empty(nbytes, dtype=np.uint8)
+    _check(load().qmm_pack(W.ctypes.data_as(ctypes.c_void_p), N, K, out.ctypes.data_as(ctypes.c_void_p),
+                           out.nbytes, threads), "qmm_pack")
+    return out
+
+
+def run(Wq, N: int, K: int, X, Y, M: int | None = None, variant: int = VARIANT_AUTO, stream=None):
+    """Y[M x N] = X[M x K] * dequant(Wq)^T on the GPU (torch CUDA tensors: uint8/any Wq,
+    bf16 or int16 X, fp32 Y).  Asynchronous on `stream` (default: torch's current stream)."""
+    if M is None:
+        M = X.shape[0]
+    st = load().qmm_run_variant(ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()),
+                                ctypes.c_void_p(Y.data_ptr()), M, variant, _stream_handle(stream))
+    _check(st, "qmm_run")
+
+
+def run_raw(wq_ptr: int, N: int, K: int, x_ptr: int, y_ptr: int, M: int, variant: int = VARIANT_AUTO,
+            stream_handle: int = 0) -> int:
+    """Unchecked call on raw device pointers; returns the status code."""
+    return load().qmm_run_variant(ctypes.c_void_p(wq_ptr), N, K, ctypes.c_void_p(x_ptr),
+                                  ctypes.c_void_p(y_ptr), M, variant, ctypes.c_void_p(stream_handle))
+
+
+def make_entries(items):
+    """items: sequence of (Wq, X, Y, N, K) with torch tensors or raw int pointers."""
+    arr = (_Entry * len(items))()
+    for k, (Wq, X, Y, N, K) in enumerate(items):
+        ptr = lambda t: t if isinstance(t, int) else t.data_ptr()
+        arr[k] = _Entry(ptr(Wq), ptr(X), ptr(Y), N, K)
+    return arr
+
+
+def run_batched(entries, M: int, stream=None):
+    """One launch over independent products sharing M.  `entries` from make_entries()."""
+    st = load().qmm_run_batched(entries, len(entries), M, _stream_handle(stream))
+    _check(st, "qmm_run_batched")
+
+
+def dequant(Wq, N: int, K: int, out, stream=None):
+    _check(load().qmm_dequant(ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(out.data_ptr()),
+                              _stream_handle(stream)), "qmm_dequant")
+
+
+def select_variant(M: int, N: int, K: int) -> int:
+    return load().qmm_select_variant(M, N, K)
+
+
+def device_status() -> int:
+    v = ctypes.c_uint(0)
+    _check(load().qmm_device_status(ctypes.byref(v)), "qmm_device_status")
+    return v.value

@@ -1,0 +1,49 @@
+"""Synthetic workloads: the matrix shapes of the benchmark configurations and a streaming
+generate -> pack -> upload helper that keeps host memory bounded for the 248320-row
+vocabulary projection.  Weights follow inputs.weight_chunks (W ~ N(0, 0.02^2)), packed with
+the library's host packer.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import inputs
+
+# One transformer layer's Q4K matrices of the 27B hybrid model the pages run
+# (attention projections and the FFN), as (name, N, K).
+LAYER_SHAPES = [
+    ("q", 5120, 5120),
+    ("k", 1024, 5120),
+    ("v", 1024, 5120),
+    ("o", 5120, 5120),
+    ("gate_up", 34816, 5120),
+    ("down", 5120, 17408),
+]
+LM_HEAD = ("lm_head", 248320, 5120)
+TINY = ("tiny", 256, 512)
+
+
+def packed_weights(N: int, K: int, seed: int, device=None, keep_host: bool = False, threads: int = 0):
+    """Pack W(N, K, seed) chunk by chunk.  Returns (device_tensor or None, host_bytes or None)."""
+    import torch
+    from . import qmm
+
+    rowbytes = (K // 256) * 144
+    dev = torch.empty(N * rowbytes, dtype=torch.uint8, device=device) if device is not None else None
+    host = np.empty(N * rowbytes, dtype=np.uint8) if (keep_host or device is None) else None
+    for row0, w in inputs.weight_chunks(N, K, seed):
+        rows = w.shape[0]
+        buf = qmm.pack(w, threads=threads)
+        if host is not None:
+            host[row0 * rowbytes:(row0 + rows) * rowbytes] = buf
+        if dev is not None:
+            dev[row0 * rowbytes:(row0 + rows) * rowbytes].copy_(torch.from_numpy(buf), non_blocking=False)
+    return dev, host
+
+
+def activations(M: int, K: int, seed: int, device=None):
+    """(torch bf16 tensor on `device`, host uint16 bits) of M x K activations."""
+    import torch
+    bits = inputs.activations_bf16_bits(M, K, seed)
+    t = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    return (t.to(device) if device is not None else t), bits

@@ -58,7 +58,7 @@
  *   - X is M x K row-major bf16 (raw bit patterns in uint16_t), Y is M x N row-major fp32.
  *     Wq and X must be 16-byte aligned; Y must be 4-byte aligned.  Y is overwritten, never
  *     accumulated, and must not overlap Wq or X.
- *   - 1 <= M <= 32, 1 <= N < 2^31, 256 <= K < 2^31, K % 256 == 0.
+ *   - 1 <= M <= 32, 1 <= N < 2^31, 256 <= K <= 2^20, K % 256 == 0.
  *   - GPU calls are asynchronous: they validate their arguments on the host, enqueue work on
  *     `stream` (0 = the legacy default stream) and return.  Argument errors are returned
  *     before anything is enqueued.  A launch failure returns QMM_ERR_CUDA (the CUDA error
@@ -153,6 +153,12 @@ qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint1
 
 /* The variant qmm_run uses for this shape (never QMM_VARIANT_AUTO). */
 int qmm_select_variant(int M, int64_t N, int64_t K);
+
+/* Read and clear the status word that the kernels of this library keep on the current device
+ * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the
+ * last read.  Bit 0: a kernel stopped waiting for its own weight copies after a bounded number
+ * of polls; the outputs of the calls since the last read are then invalid. */
+qmm_status qmm_device_status(unsigned* status_out);
 
 /* Human-readable text of a status code (static storage). */
 const char* qmm_strerror(qmm_status status);

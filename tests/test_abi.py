@@ -1,0 +1,97 @@
+"""CPU tests of the C-ABI library: it loads, exports every symbol of include/qmm.h, validates
+arguments before touching the GPU, and its host packer equals the oracle's packer byte for byte."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from bit_quantized_skinny_gb300 import build_lib, inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    build_lib.build()
+    from bit_quantized_skinny_gb300 import qmm as q
+    q.load()
+    return q
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(qmm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(qmm):
+    declared = header_functions()
+    assert "qmm_run" in declared and "qmm_pack" in declared and "qmm_run_batched" in declared
+    lib = qmm.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(declared) == sorted(qmm.EXPORTS)
+
+
+def test_packed_bytes(qmm):
+    assert qmm.packed_bytes(34816, 5120) == 100_270_080
+    assert qmm.packed_bytes(248320, 5120) == 715_161_600
+    assert qmm.packed_bytes(5120, 17408) == 50_135_040
+    assert qmm.packed_bytes(1, 255) == 0
+    assert qmm.packed_bytes(0, 256) == 0
+
+
+def test_argument_errors_need_no_gpu(qmm):
+    lib = qmm.load()
+    p = ctypes.c_void_p(16)   # never dereferenced: every call below fails validation first
+    assert lib.qmm_run(None, 4, 256, p, p, 1, None) == 1
+    assert lib.qmm_run(p, 4, 255, p, p, 1, None) == 2
+    assert lib.qmm_run(p, 0, 256, p, p, 1, None) == 2
+    assert lib.qmm_run(p, 4, 256, p, p, 0, None) == 3
+    assert lib.qmm_run(p, 4, 256, p, p, 33, None) == 3
+    assert lib.qmm_run(ctypes.c_void_p(24), 4, 256, p, p, 1, None) == 4
+    assert lib.qmm_run(p, 4, 256, ctypes.c_void_p(8), p, 1, None) == 4
+    assert lib.qmm_run(p, 4, 256, p, ctypes.c_void_p(18), 1, None) == 4
+    assert lib.qmm_run_batched(None, 1, 1, None) == 1
+    ents = qmm.make_entries([(16, 16, 16, 4, 256)])
+    assert lib.qmm_run_batched(ents, 0, 1, None) == 8
+    assert lib.qmm_run_batched(ents, 513, 1, None) == 8
+    assert lib.qmm_dequant(p, 4, 100, p, None) == 2
+    assert lib.qmm_strerror(3) == b"M must be in [1, 32]"
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (37, 2304), (5, 256), (64, 5120)])
+def test_pack_equals_oracle_pack(qmm, oracle_lib, shape):
+    N, K = shape
+    W = inputs.weights_f32(N, K, 100 + N)
+    assert np.array_equal(qmm.pack(W), oracle_lib.pack(W))
+    assert np.array_equal(qmm.pack(W, threads=3), oracle_lib.pack(W))
+
+
+def test_pack_equals_oracle_on_awkward_values(qmm, oracle_lib):
+    rng = np.random.default_rng(9)
+    W = (rng.standard_normal((48, 768)) * np.exp(rng.uniform(-12, 6, (48, 1)))).astype(np.float32)
+    W[0, :256] = 0.0
+    W[1, :256] = -0.0
+    W[2, :256] = 3.0
+    W[3, :256] = -3.0
+    W[4, 0:32] = np.linspace(-1, 1, 32, dtype=np.float32)
+    W[5, :] = np.float32(1e-30)
+    W[6, :] = np.float32(-7e-6)
+    assert np.array_equal(qmm.pack(W), oracle_lib.pack(W))
+
+
+def test_pack_errors(qmm):
+    W = np.zeros((2, 256), np.float32)
+    W[1, 3] = np.nan
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.pack(W)
+    assert e.value.status == 6
+    W[1, 3] = 1e9
+    with pytest.raises(qmm.QmmError):
+        qmm.pack(W)
+    lib = qmm.load()
+    small = np.zeros(10, np.uint8)
+    assert lib.qmm_pack(W.ctypes.data_as(ctypes.c_void_p), 2, 256,
+                        small.ctypes.data_as(ctypes.c_void_p), small.nbytes, 1) == 5
