@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the skinny Q4K x bf16 product on GB300: weight-read GB/s, % of the HBM
+roofline and ms per 15.8 GB weight pass, per M.
+
+Workload of a step (default): one full 64-layer weight pass of the 27B hybrid model's Q4K
+matrices (per layer q 5120x5120, k and v 1024x5120, o 5120x5120, gate_up 34816x5120,
+down 5120x17408: 384 matrices, 11.89 GB of packed weights) through ONE qmm_run_batched launch
+with M activation rows (M = 8 by default: the pages' 8-row verify pass).  The weights are far
+larger than L2 (129 MB), so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--M 8] [--impl ours|reference]
+
+Under torchrun each rank runs its own full pass on its own GPU (independent problems, no
+collective on the data path); the timing is the max over ranks and `value` sums all ranks'
+weight bytes.  `--impl reference` times the oracle (plain fp64 C on the host cores) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "weight-read GB/s and % of HBM roofline vs M (1..32); ms per 15.8 GB pass"
+UNIT = "GB/s"
+PASS_BYTES = 15.8e9          # the pages' weight pass ("sixi-asi 0.9", section "The patch")
+SPEC_HBM_GBS = 8000.0        # GB300 HBM3e, nominal
+LAYERS = 64
+
+
+# ----------------------------------------------------------------------------- metric ----
+
+def weight_gbps(weight_bytes: float, ms: float) -> float:
+    """Weight-only effective bandwidth: packed weight bytes read / kernel time (GB/s)."""
+    return weight_bytes / (ms * 1e-3) / 1e9
+
+
+def ms_per_pass(gbps: float) -> float:
+    return PASS_BYTES / (gbps * 1e9) * 1e3
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except OSError:
+        return None
+
+
+def hbm_peak():
+    mp = measured_peaks()
+    if mp and mp.get("hbm_gbs"):
+        return float(mp["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_skinny_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, M: int):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    key = f"{kernel}|{workload}|M={M}"
+    ent = rec.get(key)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (ctypes) during a region."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks"}
+
+    def __init__(self, cuda_device: int, interval_s: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.interval = interval_s
+        self._stop = threading.Event()
+        try:
+            import torch
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(cuda_device).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self._reason_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _poll(self):
+        clk = ctypes.c_uint(0)
+        rs = ctypes.c_ulonglong(0)
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
+                    self._reason_fn(self.handle, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
+                    "samples": 0, "source": "nvml unavailable" if not self.ok else "no samples"}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml"}
+
+
+# ----------------------------------------------------------------------------- workload --
+
+def layer_pass_setup(M: int, device: str):
+    """Device buffers for the 64-layer pass: each distinct matrix is packed once and copied
+    into 64 distinct device buffers (content does not change the speed; every buffer is
+    read from HBM).  Returns (entries, info) with info holding the host-side copies."""
+    import torch
+    from bit_quantized_skinny_gb300 import inputs, qmm, workloads
+
+    bases, hosts = [], []
+    for idx, (name, N, K) in enumerate(workloads.LAYER_SHAPES):
+        Wd, Wh = workloads.packed_weights(N, K, inputs.seed_for(4, idx), device=device, keep_host=True)
+        bases.append(Wd)
+        hosts.append(Wh)
+    xs = {}
+    for K in sorted({K for _, _, K in workloads.LAYER_SHAPES}):
+        xs[K] = workloads.activations(M, K, inputs.seed_for(4, 100 + K % 97), device=device)
+    items, ys, ws = [], [], []
+    for layer in range(LAYERS):
+        for idx, (name, N, K) in enumerate(workloads.LAYER_SHAPES):
+            w = bases[idx] if layer == 0 else bases[idx].clone()
+            y = torch.empty((M, N), dtype=torch.float32, device=device)
+            ws.append(w)
+            ys.append(y)
+            items.append((w, xs[K][0], y, N, K))
+    entries = qmm.make_entries(items)
+    weight_bytes = sum(w.numel() for w in ws)
+    algo_bytes = weight_bytes + sum(M * K * 2 + M * N * 4 for _, _, _, N, K in items)
+    return entries, dict(items=items, ws=ws, ys=ys, xs=xs, hosts=hosts, weight_bytes=weight_bytes,
+                         algo_bytes=algo_bytes)
+
+
+def time_steps(fn, steps: int, warmup: int, stream, sync_ranks):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    sync_ranks()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sync_ranks()
+    return e0.elapsed_time(e1) / steps
+
+
+def cpu_baseline(info, M: int, budget_s: float = 12.0):
+    """The oracle as it stands, timed on the host cores over a bounded sample of the pass:
+    evenly spaced rows of each of the six distinct matrices, M activation rows."""
+    import numpy as np
+    import oracle
+    from bit_quantized_skinny_gb300 import inputs, workloads
+
+    oracle.build()
+    cores = oracle.max_threads()
+    shapes = workloads.LAYER_SHAPES
+    xs = {K: inputs.activations_bf16_bits(M, K, 9) for K in {K for _, _, K in shapes}}
+    # calibrate: time 2*cores rows of the down matrix
+    t0 = time.perf_counter()
+    N, K = shapes[5][1], shapes[5][2]
+    oracle.matmul(info["hosts"][5], N, K, xs[K], rows=np.arange(2 * cores) % N)
+    per_weight = (time.perf_counter() - t0) / (2 * cores * K)
+    total_w = sum(N * K for _, N, K in shapes)
+    frac = min(1.0, budget_s / (per_weight * total_w))
+    done_bytes, t_total, sampled_rows = 0, 0.0, 0
+    for idx, (name, N, K) in enumerate(shapes):
+        nrows = max(cores, int(N * frac))
+        rows = np.linspace(0, N - 1, nrows).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.matmul(info["hosts"][idx], N, K, xs[K], rows=rows)
+        t_total += time.perf_counter() - t0
+        done_bytes += nrows * (K // 256) * 144
+        sampled_rows += nrows
+    return {"value": round(weight_gbps(done_bytes, t_total * 1e3), 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{sampled_rows} evenly spaced weight rows of the six distinct layer matrices "
+                      f"({done_bytes / 1e6:.1f} MB of packed weights, {frac * 100:.2f}% of one layer), "
+                      f"M={M}, fp64, OpenMP over rows; {t_total:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- arms ------
+
+def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
+    import numpy as np
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, qmm
+
+    torch.cuda.set_device(local_rank)
+    device = f"cuda:{local_rank}"
+    if rank == 0:
+        build_lib.build()
+    sync = (lambda: torch.distributed.barrier()) if dist_ok else (lambda: None)
+    sync()
+    qmm.load()
+    stream = torch.cuda.current_stream()
+    M = args.M
+    entries, info = layer_pass_setup(M, device)
+
+    step = lambda: qmm.run_batched(entries, M)
+    step()
+    torch.cuda.synchronize()
+    if qmm.device_status() != 0:
+        raise RuntimeError("kernel reported a device-side error")
+
+    with ClockSampler(local_rank) as clocks:
+        ms = time_steps(step, args.steps, args.warmup, stream, sync)
+    if qmm.device_status() != 0:
+        raise RuntimeError("kernel reported a device-side error")
+    ms_t = torch.tensor([ms], dtype=torch.float64)
+    if dist_ok:
+        ms_t = ms_t.to(device)
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    wb = info["weight_bytes"]
+    per_gpu_gbps = weight_gbps(wb, ms)
+    if per_gpu_gbps > SPEC_HBM_GBS:
+        raise SystemExit(f"roofline guard: {per_gpu_gbps:.0f} GB/s exceeds the {SPEC_HBM_GBS:.0f} GB/s HBM "
+                         f"peak; a benchmark that beats the roofline is a bug report")
+    value = weight_gbps(wb * world, ms_max)
+
+    # ---- end to end through the C ABI with host buffers: H2D of X, the pass, D2H of Y
+    pin_x = {K: x[0].cpu().pin_memory() for K, x in info["xs"].items()}
+    pin_y = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in info["ys"]]
+    h2d = sum(x.numel() * 2 for x in pin_x.values())
+    d2h = sum(y.numel() * 4 for y in pin_y)
+
+    def e2e_step():
+        for K, x in info["xs"].items():
+            x[0].copy_(pin_x[K], non_blocking=True)
+        qmm.run_batched(entries, M)
+        for y_dev, y_host in zip(info["ys"], pin_y):
+            y_host.copy_(y_dev, non_blocking=True)
+
+    ms_e2e = time_steps(e2e_step, args.steps, args.warmup, stream, sync)
+
+    # ---- per-M sweep on the same pass (context for the switch point; same timing rules)
+    per_m = {}
+    if args.sweep and rank == 0:
+        for m in args.sweep:
+            ents_m, info_m = (entries, info) if m == M else layer_pass_setup(m, device)
+            f = (lambda e=ents_m, mm=m: qmm.run_batched(e, mm))
+            msm = time_steps(f, max(3, args.steps // 2), 3, stream, lambda: None)
+            g = weight_gbps(info_m["weight_bytes"], msm)
+            per_m[str(m)] = {"gbps": round(g, 1), "ms_per_15.8GB_pass": round(ms_per_pass(g), 4),
+                             "frac_of_measured_hbm": round(g / hbm_peak()[0], 4),
+                             "ms_per_row": round(msm / m, 4)}
+            if m != M:
+                del ents_m, info_m
+                torch.cuda.empty_cache()
+
+    peak, peak_kind = hbm_peak()
+    achieved = info["algo_bytes"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: W ~ N(0, 0.02^2) packed to Q4K by qmm_pack, X ~ N(0,1) in bf16, seeded",
+        "config": {
+            "workload": "64-layer Q4K weight pass: per layer q 5120x5120, k 1024x5120, v 1024x5120, "
+                        "o 5120x5120, gate_up 34816x5120, down 5120x17408 (384 matrices), "
+                        f"M={M} bf16 rows, one qmm_run_batched launch per pass",
+            "M": M, "matrices": len(info["items"]), "weight_bytes_per_step": wb,
+            "ms_per_15.8GB_pass": round(ms_per_pass(per_gpu_gbps), 4),
+            "frac_of_spec_8TBps": round(per_gpu_gbps / SPEC_HBM_GBS, 4),
+            "l2": "inputs larger than L2: 11.9 GB of weights per step vs 129 MB L2, no flush",
+            "parallelism": f"{world} independent replica(s), one per GPU" if world > 1 else "1 GPU",
+        },
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("q4k_fma_kernel", "pass64", M),
+                     "kernel": "q4k_fma_kernel",
+                     "algorithmic_bytes_per_launch": info["algo_bytes"]},
+        "e2e": {"value": round(weight_gbps(wb * world, ms_e2e), 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(ms_e2e, 5),
+                "note": "qmm_run_batched with the step's X copied from pinned host memory and every "
+                        "Y copied back to pinned host memory inside the timed region; the weights "
+                        "are resident model parameters"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "per_M": per_m,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(info, M)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank: int):
+    """The oracle (plain fp64 C, host cores) on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from bit_quantized_skinny_gb300 import inputs, qmm, build_lib, workloads
+
+    build_lib.build()
+    oracle.build()
+    cores = oracle.max_threads()
+    M = args.M
+    shapes = workloads.LAYER_SHAPES
+    hosts = []
+    for idx, (name, N, K) in enumerate(shapes):
+        _, Wh = workloads.packed_weights(N, K, inputs.seed_for(4, idx), device=None, keep_host=True)
+        hosts.append(Wh)
+    xs = {K: inputs.activations_bf16_bits(M, K, 9) for K in {K for _, _, K in shapes}}
+    # one step: a fixed, evenly spaced sample of rows from each distinct matrix (~1.5 s of work)
+    N5, K5 = shapes[5][1], shapes[5][2]
+    t0 = time.perf_counter()
+    oracle.matmul(hosts[5], N5, K5, xs[K5], rows=np.arange(16 * cores) % N5)
+    per_weight = (time.perf_counter() - t0) / (16 * cores * K5)
+    total_w = sum(N * K for _, N, K in shapes)
+    frac = min(1.0, 1.5 / (per_weight * total_w))
+    samples = [np.linspace(0, N - 1, max(cores, int(N * frac))).astype(np.int64) for _, N, _ in shapes]
+    step_bytes = sum(len(r) * (K // 256) * 144 for r, (_, _, K) in zip(samples, shapes))
+
+    def step():
+        for idx, (name, N, K) in enumerate(shapes):
+            oracle.matmul(hosts[idx], N, K, xs[K], rows=samples[idx])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = weight_gbps(step_bytes, dt * 1e3)
+    sample = (f"{sum(len(r) for r in samples)} evenly spaced weight rows of the six distinct layer "
+              f"matrices per step ({step_bytes / 1e6:.1f} MB packed), M={M}, fp64, OpenMP over rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: W ~ N(0, 0.02^2) packed to Q4K, X ~ N(0,1) in bf16, seeded",
+        "config": {"workload": "64-layer Q4K weight pass (bounded row sample per step), "
+                               f"M={M}, the oracle on the host cores", "M": M},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--M", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 4, 8, 16, 32])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    dist_ok = False
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist_ok = True
+    try:
+        run_ours(args, rank, world, local_rank, dist_ok)
+    finally:
+        if dist_ok:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -23,15 +23,11 @@ __global__ void __launch_bounds__(256) q4k_dequant_kernel(const uint8_t* __restr
   float4* o = reinterpret_cast<float4*>(out + s * 32);
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const Quads qq = nibbles_to_f32(words[w]);
-    const uint64_t pr[4] = {qq.p01, qq.p23, qq.p45, qq.p67};
+    float q8[8];
+    nibbles_to_f32(words[w], q8);
     float v[8];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const float2 f = f2unpack(pr[p]);
-      v[2 * p] = fmaf(sc.dsc, f.x, -sc.dmm);
-      v[2 * p + 1] = fmaf(sc.dsc, f.y, -sc.dmm);
-    }
+    for (int p = 0; p < 8; ++p) v[p] = fmaf(sc.dsc, q8[p], -sc.dmm);
     o[2 * w] = make_float4(v[0], v[1], v[2], v[3]);
     o[2 * w + 1] = make_float4(v[4], v[5], v[6], v[7]);
   }

@@ -63,41 +63,37 @@ __device__ __forceinline__ SubScale decode_scales(uint4 h, int j) {
   const uint32_t hi = (j < 3) ? h.z : h.w;
   const uint32_t v = __funnelshift_r(lo, hi, (12 * j) & 31);
   // Small integers to fp32 exactly: OR the value into the mantissa of 2^23, subtract 2^23.
-  const uint64_t sm = add2(f2pack(__uint_as_float((v & 63u) | 0x4B000000u),
-                                  __uint_as_float((v & 0xFC0u) | 0x4B000000u)),
-                           pair_bits(0xCB000000u, 0xCB000000u));
-  const float2 s = f2unpack(sm);  // (sc_j, 64*m_j)
+  const float sc = __uint_as_float((v & 63u) | 0x4B000000u) - 8388608.0f;
+  const float m64 = __uint_as_float((v & 0xFC0u) | 0x4B000000u) - 8388608.0f;  // 64 * m_j
   SubScale r;
-  r.dsc = dd.x * s.x;
-  r.dmm = (dd.y * 0.015625f) * s.y;  // Dm * 2^-6 * 64 m = Dm * m, exact
+  r.dsc = dd.x * sc;
+  r.dmm = (dd.y * 0.015625f) * m64;  // Dm * 2^-6 * 64 m = Dm * m, exact
   return r;
 }
 
 // ---------------------------------------------------------------- nibble -> fp32 ---------
-// The 8 quants of one 32-bit word (nibble p = weight 8w+p) as exact fp32 pairs
-// (q0,q1) (q2,q3) (q4,q5) (q6,q7).  A nibble at bits [4p, 4p+4) with p <= 4 is ORed into a
-// float whose exponent makes one unit of the nibble worth 1.0: the float is 2^(23-4p) + q.
-// Nibbles 5..7 are first shifted down by 12 bits.  One add.f32x2 per pair removes the offsets.
-struct Quads {
-  uint64_t p01, p23, p45, p67;
-};
+// The 8 quants of one 32-bit word (nibble p = weight 8w+p) as exact fp32 values.  A nibble at
+// bits [4p, 4p+4) with p <= 4 is ORed into a float whose exponent makes one unit of the nibble
+// worth 1.0: the float is 2^(23-4p) + q; nibbles 5..7 are first shifted down by 12 bits.  One
+// fp32 subtraction per weight removes the offset (exact).  Written as scalar code so that the
+// compiler can pair the subtractions into packed fp32x2 instructions itself.
+// (a & mask) | magic in one 3-input logic instruction.
+__device__ __forceinline__ float and_or_f32(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
+  return __uint_as_float(r);
+}
 
-__device__ __forceinline__ Quads nibbles_to_f32(uint32_t a) {
+__device__ __forceinline__ void nibbles_to_f32(uint32_t a, float (&q)[8]) {
   const uint32_t b = a >> 12;
-  Quads r;
-  r.p01 = add2(f2pack(__uint_as_float((a & 0x0000Fu) | 0x4B000000u),    // 2^23 + q0
-                      __uint_as_float((a & 0x000F0u) | 0x49000000u)),   // 2^19 + q1
-               pair_bits(0xCB000000u, 0xC9000000u));
-  r.p23 = add2(f2pack(__uint_as_float((a & 0x00F00u) | 0x47000000u),    // 2^15 + q2
-                      __uint_as_float((a & 0x0F000u) | 0x45000000u)),   // 2^11 + q3
-               pair_bits(0xC7000000u, 0xC5000000u));
-  r.p45 = add2(f2pack(__uint_as_float((a & 0xF0000u) | 0x43000000u),    // 2^7  + q4
-                      __uint_as_float((b & 0x00F00u) | 0x47000000u)),   // 2^15 + q5
-               pair_bits(0xC3000000u, 0xC7000000u));
-  r.p67 = add2(f2pack(__uint_as_float((b & 0x0F000u) | 0x45000000u),    // 2^11 + q6
-                      __uint_as_float((b & 0xF0000u) | 0x43000000u)),   // 2^7  + q7
-               pair_bits(0xC5000000u, 0xC3000000u));
-  return r;
+  q[0] = and_or_f32(a, 0x0000Fu, 0x4B000000u) - 8388608.0f;  // 2^23 + q0
+  q[1] = and_or_f32(a, 0x000F0u, 0x49000000u) - 524288.0f;   // 2^19 + q1
+  q[2] = and_or_f32(a, 0x00F00u, 0x47000000u) - 32768.0f;    // 2^15 + q2
+  q[3] = and_or_f32(a, 0x0F000u, 0x45000000u) - 2048.0f;     // 2^11 + q3
+  q[4] = and_or_f32(a, 0xF0000u, 0x43000000u) - 128.0f;      // 2^7  + q4
+  q[5] = and_or_f32(b, 0x00F00u, 0x47000000u) - 32768.0f;
+  q[6] = and_or_f32(b, 0x0F000u, 0x45000000u) - 2048.0f;
+  q[7] = and_or_f32(b, 0xF0000u, 0x43000000u) - 128.0f;
 }
 
 // ---------------------------------------------------------------- shared memory / TMA ----
@@ -131,15 +127,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
 
-// One bounded wait for phase `parity` of the mbarrier.  Returns false after `limit` polls.
+// One bounded wait for phase `parity` of the mbarrier.  Each poll parks the thread until the
+// phase completes or `kSuspendNs` pass (so a waiting warp takes no issue slots from the warps
+// that compute); after `limit` polls the wait gives up and returns false.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
   for (uint32_t it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
     if (done) return true;
   }
   return false;

@@ -43,7 +43,7 @@ constexpr int kStages = 4;    // ring depth per warp
 constexpr int kBoxBytes = kRB * kChunkBytes;               // 2304
 constexpr int kRingBytes = kWarps * kStages * kBoxBytes;   // 73728
 constexpr int kBarBytes = kWarps * kStages * 8;            // 256
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimit = 1u << 17;   // polls of up to 20 us each: ~2.6 s
 constexpr int kMinBlocksPerSM = 2;
 
 struct FmaEntry {
@@ -139,7 +139,7 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
     if (!failed)
       for (int u = u_begin; u < min(u_end, u_begin + kStages); ++u) issue(u);
 
-    uint64_t xp[MT][16];
+    float xf[MT][32];
     float negxs[MT];
     int cur_c = -1;
     bool lane_valid = false;
@@ -170,11 +170,10 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
             const uint32_t w4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const float lo = __uint_as_float(w4[h] << 16);
-              const float hi = __uint_as_float(w4[h] & 0xFFFF0000u);
-              xp[i][4 * g + h] = f2pack(lo, hi);
-              s += lo;
-              s += hi;
+              xf[i][8 * g + 2 * h] = __uint_as_float(w4[h] << 16);
+              xf[i][8 * g + 2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+              s += xf[i][8 * g + 2 * h];
+              s += xf[i][8 * g + 2 * h + 1];
             }
           }
           negxs[i] = -s;
@@ -202,30 +201,23 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
           const uint4 h = lds128(sb + s * kChunkBytes);
           const uint4 q = lds128(sb + s * kChunkBytes + 16 + 16 * (lane & 7));
           const SubScale sc = decode_scales(h, lane & 7);
-          const Quads w0 = nibbles_to_f32(q.x);
-          const Quads w1 = nibbles_to_f32(q.y);
-          const Quads w2 = nibbles_to_f32(q.z);
-          const Quads w3 = nibbles_to_f32(q.w);
+          float qf[32];
+          nibbles_to_f32(q.x, *reinterpret_cast<float(*)[8]>(&qf[0]));
+          nibbles_to_f32(q.y, *reinterpret_cast<float(*)[8]>(&qf[8]));
+          nibbles_to_f32(q.z, *reinterpret_cast<float(*)[8]>(&qf[16]));
+          nibbles_to_f32(q.w, *reinterpret_cast<float(*)[8]>(&qf[24]));
 #pragma unroll
           for (int i = 0; i < MT; ++i) {
-            uint64_t a = fma2(w0.p01, xp[i][0], 0ull);
-            a = fma2(w0.p23, xp[i][1], a);
-            a = fma2(w0.p45, xp[i][2], a);
-            a = fma2(w0.p67, xp[i][3], a);
-            a = fma2(w1.p01, xp[i][4], a);
-            a = fma2(w1.p23, xp[i][5], a);
-            a = fma2(w1.p45, xp[i][6], a);
-            a = fma2(w1.p67, xp[i][7], a);
-            uint64_t b = fma2(w2.p01, xp[i][8], 0ull);
-            b = fma2(w2.p23, xp[i][9], b);
-            b = fma2(w2.p45, xp[i][10], b);
-            b = fma2(w2.p67, xp[i][11], b);
-            b = fma2(w3.p01, xp[i][12], b);
-            b = fma2(w3.p23, xp[i][13], b);
-            b = fma2(w3.p45, xp[i][14], b);
-            b = fma2(w3.p67, xp[i][15], b);
-            const float2 fa = f2unpack(a), fb = f2unpack(b);
-            const float dot = (fa.x + fa.y) + (fb.x + fb.y);
+            // four accumulators (weights t = 4k, 4k+1, 4k+2, 4k+3), summed in a fixed order
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+              a0 = fmaf(qf[t], xf[i][t], a0);
+              a1 = fmaf(qf[t + 1], xf[i][t + 1], a1);
+              a2 = fmaf(qf[t + 2], xf[i][t + 2], a2);
+              a3 = fmaf(qf[t + 3], xf[i][t + 3], a3);
+            }
+            const float dot = (a0 + a1) + (a2 + a3);
             const float part = fmaf(sc.dmm, negxs[i], sc.dsc * dot);
             vals[s * (V / kRB) + i] = lane_valid ? part : 0.f;
           }
