@@ -31,10 +31,9 @@
 #include "q4k_internal.h"
 
 namespace q4k {
-
-__device__ unsigned g_status;
-
 namespace {
+
+__device__ unsigned g_status;   // this file's kernels' status word
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
@@ -366,7 +365,7 @@ cudaError_t launch_fma(const Job* jobs, int count, int M, cudaStream_t stream) {
                   : launch_fma_t<2, 512>(jobs, count, M, stream);
 }
 
-cudaError_t read_and_clear_device_status(unsigned* out) {
+cudaError_t read_and_clear_fma_status(unsigned* out) {
   unsigned v = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
   if (e != cudaSuccess) return e;

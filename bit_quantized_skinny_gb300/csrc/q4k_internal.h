@@ -25,8 +25,9 @@ bool tc_supports(int M, int64_t N, int64_t K);
 // Device dequantization test hook.
 cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 
-// Device status word: read and clear (synchronous; 0 = no error).
-cudaError_t read_and_clear_device_status(unsigned* out);
+// Device status words of the kernel files: read and clear (synchronous; 0 = no error).
+cudaError_t read_and_clear_fma_status(unsigned* out);
+cudaError_t read_and_clear_tc_status(unsigned* out);
 
 // Host packer (qmm_pack.cpp).  Returns 0, or 6 on non-finite input / fp16 overflow.
 int pack_q4k(const float* W, int64_t N, int64_t K, uint8_t* out, int threads);

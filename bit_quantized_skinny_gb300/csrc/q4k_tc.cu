@@ -1,11 +1,668 @@
-// q4k_tc.cu — tensor-core (tcgen05) variant of the skinny Q4K x bf16 product.
-// Not built yet: every shape is reported unsupported, so dispatch keeps the CUDA-core kernel.
+// q4k_tc.cu — tensor-core (tcgen05) variant of the skinny Q4K x bf16 product (sm_103a).
+//
+// The skinny product of the pages' verify pass ("sixi-asi 0.9", section "What I got wrong in
+// 0.8") is a weight stream: every weight is read once and used by M <= 32 activation rows.  On
+// CUDA cores each weight costs one logic op, one subtraction and M fused multiply-adds; here the
+// M multiplies go to the tensor cores and the per-weight CUDA-core work drops to about one
+// instruction per pair of weights, the same for every M.  That is the M-dependent tiling of the
+// pages (a matrix kernel from a few rows on, section "The patch") done with GB300's units.
+//
+// Operands ("swap AB": the 128-row MMA dimension runs over weight rows):
+//   A[128 rows x 16 k] fp16 in tensor memory (TMEM): A = sc_j * q_t, an integer <= 945, exact.
+//     Written by the dequant warps with tcgen05.st, one thread per weight row (lane).
+//   B[16 k x Mpad] fp16 in shared memory: the activations of one super-block, x * 2^-s with one
+//     power-of-two s per super-block so that every bf16 value is exact in fp16 (see below).
+//   D[128 x Mpad] fp32 in TMEM, one accumulator per 256-weight super-block.
+//   One more K=16 MMA per super-block multiplies A_ext = (m_0..m_7, m_0..m_7) with
+//   B_ext = (hi_0..hi_7, lo_0..lo_7), the fp16 halves of the sub-block sums of x, so the
+//   dmin term also comes from the tensor cores.  The epilogue forms, per super-block,
+//     y += (D*2^s) * acc - (Dm*2^s*64) * acc_ext
+//   in fp32 registers.  Products in the MMAs are exact; only fp32 accumulation rounds.
+//
+// K order inside a super-block: the nibble trick below yields the quants of one 32-bit word as
+// fp16 pairs (q0,q4) (q1,q5) (q2,q6) (q3,q7); TMEM column 4w+c holds k = 8w+c (low half) and
+// 8w+c+4 (high half), and the activations are laid out in B with the same permutation.
+//
+// Pipeline (one CTA per SM, persistent over 128-row tiles of every product in the launch):
+//   warp 8      producer: per-row bulk copies of two super-blocks per row into a 3-stage ring
+//               (row stride 304 bytes: bank-conflict-free 16-byte reads), and one bulk copy per
+//               super-block of the prepared B block into a 4-slot ring
+//   warps 0..7  dequant: warp w owns TMEM lanes 32*(w%4).. and K half w/4 of each super-block;
+//               then the epilogue of the previous super-block (token half w/4)
+//   warp 9      allocates TMEM; one thread issues 17 MMAs per super-block and commits them to
+//               the accumulator / A-slot / B-slot barriers
+// Every wait is bounded; on timeout the kernel records an error in the status word and drains.
+//
+// Activation preparation (q4k_xprep_kernel, one CTA per super-block of each distinct X): picks
+// s so that the largest |x| of the super-block lands in [2^14, 2^15); a bf16 value is then exact
+// in fp16 unless it is below 2^-32 of that largest value (such values are rounded to fp16's
+// 2^-24 step of the scaled range), and writes B, B_ext and 2^s into a per-stream workspace.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+#include <cuda_fp16.h>
+
+#include "q4k_device.cuh"
 #include "q4k_internal.h"
+#include "q4k_tcgen05.cuh"
 
 namespace q4k {
 
-bool tc_supports(int, int64_t, int64_t) { return false; }
 
-cudaError_t launch_tc(const Job*, int, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+__device__ unsigned g_status;   // this file's kernels' status word
+
+constexpr int kTileRows = 128;
+constexpr int kDqWarps = 8;        // warps 0..7: dequant (0..3 even K halves, 4..7 odd K halves)
+constexpr int kProdWarp = 8;       // bulk copies of the prepared activations
+constexpr int kMmaWarp = 9;        // warps 9, 10: MMA issue (super-blocks alternate); 9 owns TMEM
+constexpr int kMmaWarps = 2;
+constexpr int kWProdWarp0 = 11;    // warps 11..14: weight copies, 32 rows each
+constexpr int kWProdWarps = 4;
+constexpr int kEpiWarp0 = 15;      // warps 15..18: epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // 608
+constexpr int kWGroupSB = 4;                         // super-blocks per W stage (576-byte row copies)
+constexpr int kWStages = 2;
+constexpr int kWRowStride = kWGroupSB * kBlockBytes + 16;   // 592: conflict-free 16-byte reads
+constexpr int kWStageBytes = kTileRows * kWRowStride;      // 38912
+constexpr int kASlots = 5;         // half-super-block A units in TMEM
+constexpr int kAccSlots = 2;
+constexpr int kScaleSlots = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kWaitLimit = 1u << 17;
+constexpr int kMaxE = 512;
+
+__host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
+// activation-block ring depth: as deep as shared memory allows next to the weight stages
+__host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 8 : 4; }
+// A unit slot: 64 columns of sc*q pairs (128 k) + 8 columns of (m_j) pairs for the dmin MMA
+__host__ __device__ constexpr uint32_t a_col(int slot) { return 72u * slot; }        // 0..359
+__host__ __device__ constexpr uint32_t acc1_col(int slot) { return 384u + 64u * slot; }
+__host__ __device__ constexpr uint32_t acc2_col(int slot) { return 416u + 64u * slot; }
+
+// barrier indices inside the barrier block
+constexpr int kMaxBSlots = 8;
+enum : int {
+  kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages,
+  kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
+  kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kASlots,
+  kBarAccFull = kBarAEmpty + kASlots, kBarAccEmpty = kBarAccFull + kAccSlots,
+  kBarScFull = kBarAccEmpty + kAccSlots, kBarScEmpty = kBarScFull + kScaleSlots,
+  kNumBars = kBarScEmpty + kScaleSlots
+};
+
+template <int MPAD>
+struct TcSmem {
+  static constexpr int kW = 0;
+  static constexpr int kB = kW + kWStages * kWStageBytes;
+  static constexpr int kScale = kB + b_slots(MPAD) * bblock_bytes(MPAD);   // [slot][row] float2
+  static constexpr int kBars = kScale + kScaleSlots * kTileRows * 8;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 16;
+};
+
+struct TcEntry {
+  const uint8_t* W;
+  float* Y;
+  const uint8_t* B;    // prepared activation blocks of this entry's X
+  int N;
+  int K;
+  int tiles;
+  int task_begin;
+};
+
+struct TcParams {
+  int count;
+  int M;
+  int tasks_total;
+  int pad_;
+  TcEntry e[kMaxE];
+};
+
+struct PrepEntry {
+  const uint16_t* X;
+  uint8_t* out;
+  int K;
+  int block_begin;   // first CTA index of this X
+};
+
+struct PrepParams {
+  int count;
+  int M;
+  int blocks_total;
+  int pad_;
+  PrepEntry e[kMaxE];
+};
+
+__device__ __forceinline__ uint32_t h2bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 bits2h(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+// ------------------------------------------------------------------------------------------
+// Activation preparation.  Block = 8*MPAD threads; thread (i = t/8, j = t%8) handles token i,
+// sub-block j (32 activations) of one super-block.
+template <int MPAD>
+__global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_constant__ PrepParams P) {
+  __shared__ unsigned s_max[8];
+  const int b = blockIdx.x;
+  int e = 0;
+  {
+    int lo = 0, hi = P.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (P.e[mid].block_begin <= b) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+  }
+  const PrepEntry& E = P.e[e];
+  const int sb = b - E.block_begin;
+  const int t = threadIdx.x;
+  const int i = t >> 3, j = t & 7;
+  const bool valid = i < P.M;
+  uint4 v[4];
+  if (valid) {
+    const uint16_t* xr = E.X + (int64_t)i * E.K + (int64_t)sb * 256 + 32 * j;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) v[g] = ldg_nc_v4(xr + 8 * g);
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) v[g] = make_uint4(0, 0, 0, 0);
+  }
+  unsigned mx = 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t w4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      mx = max(mx, w4[h] & 0x7FFFu);
+      mx = max(mx, (w4[h] >> 16) & 0x7FFFu);
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if ((t & 31) == 0) s_max[t >> 5] = mx;
+  __syncthreads();
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < (8 * MPAD) / 32; ++w) mx = max(mx, s_max[w]);
+  // largest |x| in [2^(e-127), 2^(e-126)); scale it into [2^14, 2^15)
+  int s = 0;
+  if (mx != 0) s = min(120, max(-120, (int)(mx >> 7) - 141));
+  const float f = __uint_as_float((uint32_t)(127 - s) << 23);   // 2^-s
+
+  uint8_t* out = E.out + (int64_t)sb * bblock_bytes(MPAD);
+  float xsum = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < 4; ++ww) {
+    const int w = 4 * j + ww;  // word (8 activations) index within the super-block
+    const uint32_t w4[4] = {v[ww].x, v[ww].y, v[ww].z, v[ww].w};
+    float xv[8];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      xv[2 * h] = __uint_as_float(w4[h] << 16) * f;
+      xv[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) * f;
+    }
+    uint32_t packed[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) packed[c] = h2bits(__floats2half2_rn(xv[c], xv[c + 4]));
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const __half2 hh = bits2h(packed[p & 3]);
+      xsum += (p < 4) ? __low2float(hh) : __high2float(hh);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + ((i >> 3) * 32 + w) * 128 + (i & 7) * 16);
+    *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+  const float xs = xsum * 0.015625f;  // 2^-6: a sum of 32 values below 2^15 stays below 2^14
+  const __half hi = __float2half_rn(xs);
+  const __half lo = __float2half_rn(xs - __half2float(hi));
+  __half* ext = reinterpret_cast<__half*>(out + MPAD * 512);
+  ext[(((i >> 3) * 2 + 0) * 128 + (i & 7) * 16) / 2 + j] = hi;
+  ext[(((i >> 3) * 2 + 1) * 128 + (i & 7) * 16) / 2 + j] = lo;
+  if (t == 0) {
+    float* sig = reinterpret_cast<float*>(out + MPAD * 544);
+    sig[0] = __uint_as_float((uint32_t)(127 + s) << 23);  // 2^s
+    sig[1] = 0.f;
+    sig[2] = 0.f;
+    sig[3] = 0.f;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+template <int MPAD>
+__global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_constant__ TcParams P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  using L = TcSmem<MPAD>;
+  constexpr int kBB = bblock_bytes(MPAD);
+  constexpr int kBSlots = b_slots(MPAD);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sW = smem_addr(smem + L::kW);
+  const uint32_t sB = smem_addr(smem + L::kB);
+  float2* scale_ring = reinterpret_cast<float2*>(smem + L::kScale);
+  const uint32_t bars = smem_addr(smem + L::kBars);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  auto bar = [&](int k) { return bars + 8u * k; };
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kWStages; ++k) { mbar_init(bar(kBarWFull + k), kWProdWarps); mbar_init(bar(kBarWEmpty + k), kDqWarps); }
+    for (int k = 0; k < kBSlots; ++k) { mbar_init(bar(kBarBFull + k), 1); mbar_init(bar(kBarBEmpty + k), 1); }
+    for (int k = 0; k < kASlots; ++k) { mbar_init(bar(kBarAFull + k), 4); mbar_init(bar(kBarAEmpty + k), 1); }
+    for (int k = 0; k < kAccSlots; ++k) { mbar_init(bar(kBarAccFull + k), 1); mbar_init(bar(kBarAccEmpty + k), kEpiWarps); }
+    for (int k = 0; k < kScaleSlots; ++k) { mbar_init(bar(kBarScFull + k), 4); mbar_init(bar(kBarScEmpty + k), kEpiWarps); }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(smem_addr(tmem_holder), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  auto wait = [&](int k, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar(k), parity, kWaitLimit)) return true;
+    atomicOr(&g_status, kErrWaitTimeout);
+    *abort_flag = 1;
+    return false;
+  };
+  auto locate = [&](int t) {
+    int lo = 0, hi = P.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (P.e[mid].task_begin <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------------ activation blocks
+    uint32_t bq = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+      const TcEntry& E = P.e[locate(t)];
+      const int nb = E.K >> 8;
+      for (int sb = 0; sb < nb; ++sb) {
+        const uint32_t bs = bq % kBSlots;
+        if (!wait(kBarBEmpty + bs, ((bq / kBSlots) & 1u) ^ 1u)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kBarBFull + bs), kBB);
+          bulk_g2s(sB + bs * kBB, E.B + (int64_t)sb * kBB, kBB, bar(kBarBFull + bs), 0ull);
+        }
+        __syncwarp();
+        ++bq;
+      }
+    }
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
+    // ------------------------------------------------------------------ MMA issue
+    // Two warps issue alternate super-blocks: a single thread spends ~45 cycles per MMA issue,
+    // two threads keep the tensor pipe busy about twice as long.
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
+      const uint32_t mine = warp - kMmaWarp;
+      uint32_t su = 0;   // super-blocks (A units 2su, 2su+1; B slot su%4; accumulator su%2)
+      uint32_t em = 0;   // accumulator uses by this warp
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+        const int nb = P.e[locate(t)].K >> 8;
+        for (int sb = 0; sb < nb; ++sb, ++su) {
+          if ((su & 1u) != mine) continue;
+          const uint32_t u0 = 2 * su, u1 = 2 * su + 1;
+          const uint32_t a0 = u0 % kASlots, a1 = u1 % kASlots;
+          const uint32_t bm = su, bs = bm % kBSlots, es = mine;
+          if (!wait(kBarAccEmpty + es, (em & 1u) ^ 1u) ||
+              !wait(kBarBFull + bs, (bm / kBSlots) & 1u) ||
+              !wait(kBarAFull + a0, (u0 / kASlots) & 1u)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t d1 = tmem + acc1_col(es);
+          const uint32_t d2 = tmem + acc2_col(es);
+          const uint32_t bslot = sB + bs * kBB;
+          const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
+          tc::mma_f16_ts_x8(d1, tmem + a_col(a0), bdesc, 16, idesc, 0);
+          tc::commit(bar(kBarAEmpty + a0));
+          if (!wait(kBarAFull + a1, (u1 / kASlots) & 1u)) { ok = false; break; }
+          tc::fence_after_sync();
+          tc::mma_f16_ts_x8(d1, tmem + a_col(a1), bdesc + 8 * 16, 16, idesc, 1);
+          tc::mma_f16_ts(d2, tmem + a_col(a1) + 64, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
+          tc::commit(bar(kBarAccFull + es));
+          tc::commit(bar(kBarAEmpty + a1));
+          tc::commit(bar(kBarBEmpty + bs));
+          ++em;
+        }
+      }
+      if (!ok && em > 0)   // let issued MMAs finish before TMEM is released
+        mbar_wait(bar(kBarAccFull + mine), (em - 1) & 1u, kWaitLimit);
+    }
+  } else if (warp >= kWProdWarp0 && warp < kWProdWarp0 + kWProdWarps) {
+    // ------------------------------------------------------------------ weight copies
+    // Warp p copies rows 32p .. 32p+31 of every stage, one row (576 bytes) per lane: bulk copies
+    // from one warp are processed one after another, so four warps issue in parallel.
+    const int p = warp - kWProdWarp0;
+    const uint64_t pol = policy_evict_first();
+    uint32_t G = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+      const TcEntry& E = P.e[locate(t)];
+      const int nb = E.K >> 8;
+      const int row0 = (t - E.task_begin) * kTileRows;
+      const int nrows = min(kTileRows, E.N - row0);
+      const int64_t rowbytes = (int64_t)nb * kBlockBytes;
+      const int rr = 32 * p + lane;
+      const int mine = max(0, min(32, nrows - 32 * p));
+      for (int g = 0; g < (nb + kWGroupSB - 1) / kWGroupSB; ++g, ++G) {
+        const uint32_t st = G % kWStages;
+        if (!wait(kBarWEmpty + st, ((G / kWStages) & 1u) ^ 1u)) { ok = false; break; }
+        fence_proxy_async_smem();
+        const int nsb = min(kWGroupSB, nb - g * kWGroupSB);
+        const uint32_t bytes_row = nsb * kBlockBytes;
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarWFull + st), mine * bytes_row);
+        __syncwarp();
+        if (rr < nrows)
+          bulk_g2s(sW + st * kWStageBytes + rr * kWRowStride,
+                   E.W + (int64_t)(row0 + rr) * rowbytes + (int64_t)g * (kWGroupSB * kBlockBytes),
+                   bytes_row, bar(kBarWFull + st), pol);
+      }
+    }
+  } else if (warp < kDqWarps) {
+    // ------------------------------------------------------------------ dequant
+    const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
+    const int h = warp >> 2;         // K half of each super-block (A unit parity)
+    const int r = 32 * q + lane;     // row inside the tile
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t su = 0, bc = 0, sc_cnt = 0;
+    const __half2 k1024 = bits2h(0x64006400u);
+    const __half2 kn1024 = __float2half2_rn(-1024.f);
+    const __half2 k1o16 = __float2half2_rn(0.0625f);
+    const __half2 kn64 = __float2half2_rn(-64.f);
+    bool ok = true;
+    uint32_t G = 0;   // weight stages consumed
+    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+      const TcEntry& E = P.e[locate(t)];
+      const int nb = E.K >> 8;
+      for (int sb = 0; sb < nb && ok; ++sb, ++su) {
+        const uint32_t st = G % kWStages;
+        if ((sb % kWGroupSB) == 0 && !wait(kBarWFull + st, (G / kWStages) & 1u)) { ok = false; break; }
+        float sigma = 1.f;
+        if (h == 0) {
+          const uint32_t bs = bc % kBSlots;
+          if (!wait(kBarBFull + bs, (bc / kBSlots) & 1u)) { ok = false; break; }
+          sigma = *reinterpret_cast<const float*>(smem + L::kB + bs * kBB + MPAD * 544);
+          ++bc;
+        }
+        const uint32_t u = 2 * su + h;
+        const uint32_t as = u % kASlots;
+        if (!wait(kBarAEmpty + as, ((u / kASlots) & 1u) ^ 1u)) { ok = false; break; }
+        tc::fence_after_sync();
+
+        // ---- this row's half super-block from shared memory
+        const uint32_t rb = sW + st * kWStageBytes + r * kWRowStride + (sb % kWGroupSB) * kBlockBytes;
+        const uint4 hd = lds128(rb);
+        uint4 qv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
+        if ((sb % kWGroupSB) == kWGroupSB - 1 || sb == nb - 1) {
+          // stage consumed by this warp (the producers refill it once all eight are done)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarWEmpty + st));
+          ++G;
+        }
+
+        // ---- scales of this super-block for the epilogue (even-half warps)
+        if (h == 0) {
+          const float2 dd = __half22float2(bits2h(hd.x));
+          const uint32_t ss = sc_cnt % kScaleSlots;
+          if (!wait(kBarScEmpty + ss, ((sc_cnt / kScaleSlots) & 1u) ^ 1u)) { ok = false; break; }
+          scale_ring[ss * kTileRows + r] = make_float2(dd.x * sigma, dd.y * sigma * 64.f);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarScFull + ss));
+          ++sc_cnt;
+        }
+
+        // ---- the 12-bit (sc, m) groups of this half's sub-blocks 4h .. 4h+3
+        const uint64_t F = h ? ((uint64_t)hd.w << 32 | hd.z) : ((uint64_t)hd.z << 32 | hd.y);
+        const int fbase = h ? 16 : 0;
+        __half2 sc2[4], scm[4], sc16[4], sc64[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint32_t g = (uint32_t)(F >> (fbase + 12 * jj)) & 0xFFFu;
+          const uint32_t scb = ((g & 63u) | 0x6400u) * 0x10001u;       // (1024+sc, 1024+sc)
+          sc2[jj] = __hsub2(bits2h(scb), k1024);                       // (sc, sc) exact
+          scm[jj] = __hmul2(sc2[jj], kn1024);                           // -1024 sc
+          sc16[jj] = __hmul2(sc2[jj], k1o16);                           // sc / 16
+          sc64[jj] = __hmul2(sc2[jj], kn64);                            // -64 sc
+        }
+
+        // ---- A = sc*q as fp16 pairs, 16 columns per sub-block, into TMEM
+        const uint32_t aaddr = tl + a_col(as);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t words[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+          uint32_t cols[16];
+#pragma unroll
+          for (int ww = 0; ww < 4; ++ww) {
+            const uint32_t wv = words[ww];
+            const uint32_t b8 = wv >> 8;
+            uint32_t p0, p1, p2, p3;
+            asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p0) : "r"(wv));
+            asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p1) : "r"(wv));
+            asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p2) : "r"(b8));
+            asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p3) : "r"(b8));
+            cols[4 * ww + 0] = h2bits(__hfma2(bits2h(p0), sc2[k], scm[k]));   // (q0, q4) * sc
+            cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p1), sc16[k], sc64[k]));  // (q1, q5) * sc
+            cols[4 * ww + 2] = h2bits(__hfma2(bits2h(p2), sc2[k], scm[k]));   // (q2, q6) * sc
+            cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p3), sc16[k], sc64[k]));  // (q3, q7) * sc
+          }
+          tc::st_x16(aaddr + 16 * k, cols);
+        }
+        if (h == 1) {
+          // A_ext (odd unit): (m_0..m_7) at k = 0..7 and again at k = 8..15
+          const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 (bits 0..47)
+          const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 (bits 16..63)
+          uint32_t mm[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            mm[jj] = (uint32_t)((jj < 4 ? (G >> (12 * jj)) : (H >> (16 + 12 * (jj - 4)))) >> 6) & 63u;
+          uint32_t ext[8];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            ext[c] = ext[c + 4] =
+                h2bits(__hsub2(bits2h((mm[2 * c] | 0x6400u) | ((mm[2 * c + 1] | 0x6400u) << 16)), k1024));
+          tc::st_x8(aaddr + 64, ext);
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarAFull + as));
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t ec = 0, scc = 0;
+    bool ok = true;
+    float y[MPAD];
+    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+      const TcEntry& E = P.e[locate(t)];
+      const int nb = E.K >> 8;
+      const int row0 = (t - E.task_begin) * kTileRows;
+#pragma unroll
+      for (int c = 0; c < MPAD; ++c) y[c] = 0.f;
+      for (int sb = 0; sb < nb; ++sb) {
+        const uint32_t es = ec % kAccSlots, ss = scc % kScaleSlots;
+        if (!wait(kBarScFull + ss, (scc / kScaleSlots) & 1u) ||
+            !wait(kBarAccFull + es, (ec / kAccSlots) & 1u)) { ok = false; break; }
+        tc::fence_after_sync();
+        const float2 sc = scale_ring[ss * kTileRows + r];
+        // read the accumulators 16 tokens at a time (keeps the register footprint small)
+#pragma unroll
+        for (int c0 = 0; c0 < MPAD; c0 += 16) {
+          float a1[16], a2[16];
+          tc::ld_x16(tl + acc1_col(es) + c0, a1);
+          tc::ld_x16(tl + acc2_col(es) + c0, a2);
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            y[c0 + c] = fmaf(sc.x, a1[c], y[c0 + c]);
+            y[c0 + c] = fmaf(-sc.y, a2[c], y[c0 + c]);
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kBarAccEmpty + es));
+          mbar_arrive(bar(kBarScEmpty + ss));
+        }
+        ++ec;
+        ++scc;
+      }
+      if (!ok) break;
+      if (row0 + r < E.N) {
+#pragma unroll
+        for (int c = 0; c < MPAD; ++c)
+          if (c < P.M) E.Y[(int64_t)c * E.N + row0 + r] = y[c];
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------------------------------
+// Per-(device, stream) workspace for the prepared activations.  Grown on demand with
+// cudaMalloc (the first call on a stream, or a call needing more room, allocates; cudaFree of a
+// smaller old buffer synchronizes the device, so no launch can still be using it).
+class Workspace {
+ public:
+  static cudaError_t get(cudaStream_t stream, size_t bytes, void** out) {
+    static std::mutex mu;
+    static std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> pool;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> g(mu);
+    auto& slot = pool[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (slot.second < bytes) {
+      if (slot.first) {
+        err = cudaFree(slot.first);
+        if (err != cudaSuccess) return err;
+        slot = {nullptr, 0};
+      }
+      const size_t want = std::max(bytes, (size_t)1 << 20);
+      void* p = nullptr;
+      err = cudaMalloc(&p, want);
+      if (err != cudaSuccess) return err;
+      slot = {p, want};
+    }
+    *out = slot.first;
+    return cudaSuccess;
+  }
+};
+
+int num_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+template <int MPAD>
+cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) {
+  static_assert(sizeof(TcParams) < 32000 && sizeof(PrepParams) < 32000, "kernel parameters too large");
+  constexpr int kBB = bblock_bytes(MPAD);
+  // distinct activations (an X pointer with its K) get one prepared block run each
+  std::vector<std::pair<const uint16_t*, int64_t>> xs;
+  std::vector<int> xidx(count);
+  for (int k = 0; k < count; ++k) {
+    int found = -1;
+    for (size_t u = 0; u < xs.size(); ++u)
+      if (xs[u].first == jobs[k].X && xs[u].second == jobs[k].K) { found = (int)u; break; }
+    if (found < 0) { found = (int)xs.size(); xs.push_back({jobs[k].X, jobs[k].K}); }
+    xidx[k] = found;
+  }
+  std::vector<size_t> xoff(xs.size());
+  size_t bytes = 0;
+  int blocks = 0;
+  for (size_t u = 0; u < xs.size(); ++u) {
+    xoff[u] = bytes;
+    bytes += (size_t)(xs[u].second / 256) * kBB;
+  }
+  void* wsp = nullptr;
+  cudaError_t err = Workspace::get(stream, bytes, &wsp);
+  if (err != cudaSuccess) return err;
+  uint8_t* ws = static_cast<uint8_t*>(wsp);
+
+  static PrepParams prep;   // large: built on the host, passed by value at launch
+  static TcParams par;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> g(mu);
+  prep.count = (int)xs.size();
+  prep.M = M;
+  for (size_t u = 0; u < xs.size(); ++u) {
+    prep.e[u] = PrepEntry{xs[u].first, ws + xoff[u], (int)xs[u].second, blocks};
+    blocks += (int)(xs[u].second / 256);
+  }
+  prep.blocks_total = blocks;
+  q4k_xprep_kernel<MPAD><<<blocks, 8 * MPAD, 0, stream>>>(prep);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+
+  par.count = count;
+  par.M = M;
+  int tasks = 0;
+  for (int k = 0; k < count; ++k) {
+    const int tiles = (int)((jobs[k].N + kTileRows - 1) / kTileRows);
+    par.e[k] = TcEntry{static_cast<const uint8_t*>(jobs[k].W), jobs[k].Y, ws + xoff[xidx[k]],
+                       (int)jobs[k].N, (int)jobs[k].K, tiles, tasks};
+    tasks += tiles;
+  }
+  par.tasks_total = tasks;
+  const int smem = TcSmem<MPAD>::kTotal;
+  auto kern = q4k_tc_kernel<MPAD>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_set[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  const int grid = std::min(tasks, num_sms());
+  kern<<<grid, kThreads, smem, stream>>>(par);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t read_and_clear_tc_status(unsigned* out) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+  *out = v;
+  return e;
+}
+
+bool tc_supports(int M, int64_t N, int64_t K) {
+  return M >= 1 && M <= 32 && N >= 1 && K >= 256 && K % 256 == 0;
+}
+
+cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream) {
+  if (count < 1 || count > kMaxE) return cudaErrorInvalidValue;
+  return (M <= 16) ? launch_tc_t<16>(jobs, count, M, stream) : launch_tc_t<32>(jobs, count, M, stream);
+}
 
 }  // namespace q4k

@@ -139,8 +139,12 @@ qmm_status qmm_run_batched(const qmm_entry* entries_host, int count, int M, cuda
 qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
                        cudaStream_t stream);
 
-/* Kernel variants.  qmm_run picks one from the dispatch table; qmm_run_variant forces one
- * (tests and benchmarks use it to measure the switch point between them). */
+/* Kernel variants.  qmm_run picks the one a cost model fitted to GB300 measurements predicts
+ * faster (CUDA cores for one activation row and for small matrices, tensor cores otherwise);
+ * qmm_run_variant forces one (tests and benchmarks use it to measure the switch point).
+ * The tensor-core variant keeps a workspace for the prepared activations per (device, stream):
+ * the first call on a stream, and any call that needs a larger one, allocates it with cudaMalloc
+ * (make such a call before capturing the stream into a CUDA graph). */
 typedef enum {
   QMM_VARIANT_AUTO = 0,
   QMM_VARIANT_FMA = 1,   /* CUDA cores: in-register dequant, fp32 FMA, warp-shuffle K reduce */

@@ -11,6 +11,8 @@ from bit_quantized_skinny_gb300 import build_lib, inputs, workloads
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
+FMA, TC = 1, 2
+VARIANTS = [pytest.param(FMA, id="fma"), pytest.param(TC, id="tc")]
 
 
 @pytest.fixture(scope="module")
@@ -85,7 +87,8 @@ def test_dequant_extreme_fields_bit_exact(qmm, oracle_lib):
 
 # ------------------------------------------------------------------ the product ------------
 
-def test_tiny_config(qmm, oracle_lib):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_tiny_config(qmm, oracle_lib, variant):
     """256 x 512 weights from W ~ N(0, 0.02^2), seed 0; M = 1 and 4."""
     N, K = 256, 512
     Wq = oracle_lib.pack(inputs.weights_f32(N, K, inputs.seed_for(1)))
@@ -93,18 +96,19 @@ def test_tiny_config(qmm, oracle_lib):
     for M in (1, 4):
         X = inputs.activations_bf16_bits(M, K, inputs.seed_for(1))
         Yref, S = oracle_lib.matmul(Wq, N, K, X)
-        Y = gpu_run(qmm, Wd, N, K, dev_x(X), M)
+        Y = gpu_run(qmm, Wd, N, K, dev_x(X), M, variant=variant)
         assert_within(Y, Yref, S, f"tiny M={M}")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("M", list(range(1, 33)))
-def test_every_M_ragged_shape(qmm, oracle_lib, M):
+def test_every_M_ragged_shape(qmm, oracle_lib, M, variant):
     """N not a multiple of the 4-row box, K = 9 super-blocks (a partial 4-block chunk)."""
     N, K = 1001, 2304
     Wq = _cached_pack(oracle_lib, N, K, 41)
     X = inputs.activations_bf16_bits(M, K, 1000 + M)
     Yref, S = oracle_lib.matmul(Wq, N, K, X)
-    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M)
+    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M, variant=variant)
     assert_within(Y, Yref, S, f"M={M}")
 
 
@@ -120,16 +124,18 @@ def _cached_pack(oracle_lib, N, K, seed):
 
 @pytest.mark.parametrize("shape", [(1, 256), (3, 256), (5, 512), (4, 1024), (7, 1280), (130, 4352)])
 @pytest.mark.parametrize("M", [1, 2, 3, 32])
-def test_small_and_degenerate_shapes(qmm, oracle_lib, shape, M):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_small_and_degenerate_shapes(qmm, oracle_lib, shape, M, variant):
     N, K = shape
     Wq = _cached_pack(oracle_lib, N, K, 5)
     X = inputs.activations_bf16_bits(M, K, 77)
     Yref, S = oracle_lib.matmul(Wq, N, K, X)
-    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M)
+    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M, variant=variant)
     assert_within(Y, Yref, S, f"{shape} M={M}")
 
 
-def test_integer_activations_are_exact(qmm, oracle_lib):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_integer_activations_are_exact(qmm, oracle_lib, variant):
     """Constant blocks (w = 0.25*3*5 - 0.125*7 = 2.875) and small integer x: every partial sum
     is exact in fp32, so the GPU must equal the closed form w0 * sum_k x bit for bit."""
     from test_oracle_pins import make_block
@@ -138,47 +144,50 @@ def test_integer_activations_are_exact(qmm, oracle_lib):
     Wq = np.frombuffer(blk * (N * K // 256), dtype=np.uint8)
     xi = np.random.default_rng(2).integers(-20, 21, size=(M, K)).astype(np.float32)
     X = inputs.bf16_bits_from_f32(xi)
-    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M)
+    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M, variant=variant)
     expect = (2.875 * xi.astype(np.float64).sum(axis=1))[:, None] * np.ones((1, N))
     assert np.array_equal(Y.astype(np.float64), expect)
 
 
-def test_zero_weights_give_exact_zero(qmm):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_zero_weights_give_exact_zero(qmm, variant):
     N, K, M = 40, 1024, 3
     Wq = np.zeros(N * K // 256 * 144, np.uint8)
     X = inputs.activations_bf16_bits(M, K, 3)
-    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M)
+    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(X), M, variant=variant)
     assert np.all(Y == 0.0)
 
 
-def test_one_hot_activations_reproduce_dequant(qmm, oracle_lib):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_one_hot_activations_reproduce_dequant(qmm, oracle_lib, variant):
     N, K = 96, 2048
     Wq = _cached_pack(oracle_lib, N, K, 13)
     ks = [0, 1, 255, 256, 1023, 1024, 2047, 517]
     eye = np.zeros((len(ks), K), np.float32)
     for r, k in enumerate(ks):
         eye[r, k] = 1.0
-    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(inputs.bf16_bits_from_f32(eye)), len(ks))
+    Y = gpu_run(qmm, dev_bytes(Wq), N, K, dev_x(inputs.bf16_bits_from_f32(eye)), len(ks), variant=variant)
     w = oracle_lib.dequant(Wq, N, K)
     for r, k in enumerate(ks):
         assert np.array_equal(Y[r], w[:, k])
 
 
-def test_row_independence_bitwise(qmm, oracle_lib):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_row_independence_bitwise(qmm, oracle_lib, variant):
     """For a fixed variant, an M-row product equals M one-row products bit for bit."""
     N, K, M = 777, 5120, 9
     Wq = _cached_pack(oracle_lib, N, K, 17)
     Wd = dev_bytes(Wq)
     X = inputs.activations_bf16_bits(M, K, 18)
-    Yall = gpu_run(qmm, Wd, N, K, dev_x(X), M, variant=1)
+    Yall = gpu_run(qmm, Wd, N, K, dev_x(X), M, variant=variant)
     for i in range(M):
-        Yi = gpu_run(qmm, Wd, N, K, dev_x(X[i:i + 1]), 1, variant=1)
+        Yi = gpu_run(qmm, Wd, N, K, dev_x(X[i:i + 1]), 1, variant=variant)
         assert np.array_equal(Yi[0].view(np.uint32), Yall[i].view(np.uint32)), i
 
 
-def test_batched_equals_single_calls(qmm, oracle_lib):
+@pytest.mark.parametrize("M", [4, 24])
+def test_batched_equals_single_calls(qmm, oracle_lib, M):
     shapes = [(512, 5120), (128, 5120), (96, 17408), (1001, 2304), (3, 256), (2048, 512)]
-    M = 4
     items, singles, refs = [], [], []
     for k, (N, K) in enumerate(shapes):
         Wq = _cached_pack(oracle_lib, N, K, 300 + k)
@@ -243,6 +252,7 @@ FULL = [
 
 @pytest.mark.parametrize("name,N,K,Ms", FULL, ids=[f[0] for f in FULL])
 def test_full_size_sampled_rows(qmm, oracle_lib, name, N, K, Ms):
+    """Both variants and the automatic choice, on the configurations' full shapes."""
     """The configurations' full shapes, in the launch the benchmark times: every output is
     computed on the GPU; sampled rows (first, last, random) are checked against the oracle.
     The sampled rows' packed bytes are also checked against the oracle's packer."""
@@ -256,8 +266,9 @@ def test_full_size_sampled_rows(qmm, oracle_lib, name, N, K, Ms):
     assert np.array_equal(oracle_lib.pack(W[first]), Wh.reshape(N, rowbytes)[first].reshape(-1))
     for M in Ms:
         X = inputs.activations_bf16_bits(M, K, seed + M)
-        Y = gpu_run(qmm, Wd, N, K, dev_x(X), M)
         Yref, S = oracle_lib.matmul(Wh, N, K, X, rows=rows)
-        assert_within(Y[:, rows], Yref, S, f"{name} M={M}")
+        for variant in (0, FMA, TC):
+            Y = gpu_run(qmm, Wd, N, K, dev_x(X), M, variant=variant)
+            assert_within(Y[:, rows], Yref, S, f"{name} M={M} variant={variant}")
     del Wd
     torch.cuda.empty_cache()
