@@ -22,6 +22,12 @@ cudaError_t launch_fma(const Job* jobs, int count, int M, cudaStream_t stream);
 cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream);
 bool tc_supports(int M, int64_t N, int64_t K);
 
+// Tensor-core product with the prepared activations in the library's fixed device buffer
+// (no allocation).  noalloc_scratch_needed(M, K) must not exceed noalloc_scratch_bytes().
+cudaError_t launch_tc_noalloc(const Job& job, int M, cudaStream_t stream);
+size_t noalloc_scratch_bytes();
+size_t noalloc_scratch_needed(int M, int64_t K);
+
 // Device dequantization test hook.
 cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 

@@ -645,6 +645,48 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------------
+// Allocation-free entry (qmm_run_noalloc): the same two kernels, with the prepared activations
+// in a fixed buffer that is part of this library's device image instead of the per-stream
+// workspace.  Every GPU that loads the library holds the buffer until the process exits.
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+template <int MPAD>
+cudaError_t launch_tc_noalloc_t(const Job& job, int M, cudaStream_t stream, uint8_t* scratch) {
+  constexpr int kBB = bblock_bytes(MPAD);
+  static PrepParams prep;   // separate from the workspace path: built here, passed by value
+  static TcParams par;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  std::lock_guard<std::mutex> g(mu);
+  const int nb = (int)(job.K / 256);
+  prep.count = 1;
+  prep.M = M;
+  prep.e[0] = PrepEntry{job.X, scratch, (int)job.K, 0};
+  prep.blocks_total = nb;
+  q4k_xprep_kernel<MPAD><<<nb, 8 * MPAD, 0, stream>>>(prep);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int tiles = (int)((job.N + kTileRows - 1) / kTileRows);
+  par.count = 1;
+  par.M = M;
+  par.e[0] = TcEntry{static_cast<const uint8_t*>(job.W), job.Y, scratch, (int)job.N, (int)job.K, tiles, 0};
+  par.tasks_total = tiles;
+  const int smem = TcSmem<MPAD>::kTotal;
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !attr_set[dev]) {
+    err = cudaFuncSetAttribute(q4k_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  (void)kBB;
+  q4k_tc_kernel<MPAD><<<std::min(tiles, num_sms()), kThreads, smem, stream>>>(par);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t read_and_clear_tc_status(unsigned* out) {
@@ -658,6 +700,36 @@ cudaError_t read_and_clear_tc_status(unsigned* out) {
 
 bool tc_supports(int M, int64_t N, int64_t K) {
   return M >= 1 && M <= 32 && N >= 1 && K >= 256 && K % 256 == 0;
+}
+
+size_t noalloc_scratch_bytes() { return kNoallocScratchBytes; }
+
+size_t noalloc_scratch_needed(int M, int64_t K) {
+  return (size_t)(K / 256) * (size_t)bblock_bytes(M <= 16 ? 16 : 32);
+}
+
+cudaError_t launch_tc_noalloc(const Job& job, int M, cudaStream_t stream) {
+  // The host only knows a stand-in for the device array; its device address is looked up once
+  // per device, with that device current.
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+      void* p = nullptr;
+      err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (err != cudaSuccess) return err;
+      addr[dev] = p;
+    }
+    scratch = addr[dev];
+  }
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  return (M <= 16) ? launch_tc_noalloc_t<16>(job, M, stream, ws) : launch_tc_noalloc_t<32>(job, M, stream, ws);
 }
 
 cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream) {

@@ -158,6 +158,17 @@ qmm_status qmm_run_batched(const qmm_entry* entries_host, int count, int M, cuda
   return run_jobs(jobs, count, M, QMM_VARIANT_AUTO, stream);
 }
 
+qmm_status qmm_run_noalloc(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev, float* Y_dev,
+                           int M, cudaStream_t stream) {
+  qmm_status s = check_job(Wq_dev, N, K, X_dev, Y_dev);
+  if (s != QMM_OK) return s;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  if (q4k::noalloc_scratch_needed(M, K) > q4k::noalloc_scratch_bytes()) return QMM_ERR_SCRATCH;
+  const q4k::Job job{Wq_dev, X_dev, Y_dev, N, K};
+  cudaError_t e = q4k::launch_tc_noalloc(job, M, stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
 qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev, cudaStream_t stream) {
   if (!Wq_dev || !out_dev) return QMM_ERR_NULL;
   qmm_status s = check_shape(N, K);
@@ -190,6 +201,7 @@ const char* qmm_strerror(qmm_status status) {
     case QMM_ERR_CUDA: return "CUDA error (see qmm_last_cuda_error)";
     case QMM_ERR_COUNT: return "batched entry count must be in [1, QMM_MAX_BATCH]";
     case QMM_ERR_VARIANT: return "the requested kernel variant cannot run this shape";
+    case QMM_ERR_SCRATCH: return "qmm_run_noalloc: the problem needs more than QMM_NOALLOC_SCRATCH_BYTES of scratch";
   }
   return "unknown status";
 }

@@ -24,12 +24,13 @@ VARIANT_NAMES = {VARIANT_FMA: "fma", VARIANT_TC: "tc"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANGE",
           4: "QMM_ERR_ALIGN", 5: "QMM_ERR_BUFSIZE", 6: "QMM_ERR_NONFINITE", 7: "QMM_ERR_CUDA",
-          8: "QMM_ERR_COUNT", 9: "QMM_ERR_VARIANT"}
+          8: "QMM_ERR_COUNT", 9: "QMM_ERR_VARIANT", 10: "QMM_ERR_SCRATCH"}
 
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
-           "qmm_last_cuda_error"]
+           "qmm_last_cuda_error", "qmm_run_noalloc"]
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class QmmError(RuntimeError):
@@ -68,6 +69,8 @@ def load(path: str | None = None):
     lib.qmm_run.restype = i32
     lib.qmm_run_variant.argtypes = [vp, i64, i64, vp, vp, i32, i32, vp]
     lib.qmm_run_variant.restype = i32
+    lib.qmm_run_noalloc.argtypes = [vp, i64, i64, vp, vp, i32, vp]
+    lib.qmm_run_noalloc.restype = i32
     lib.qmm_run_batched.argtypes = [ctypes.POINTER(_Entry), i32, i32, vp]
     lib.qmm_run_batched.restype = i32
     lib.qmm_dequant.argtypes = [vp, i64, i64, vp, vp]
@@ -122,6 +125,16 @@ def run(Wq, N: int, K: int, X, Y, M: int | None = None, variant: int = VARIANT_A
     st = load().qmm_run_variant(ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()),
                                 ctypes.c_void_p(Y.data_ptr()), M, variant, _stream_handle(stream))
     _check(st, "qmm_run")
+
+
+def run_noalloc(Wq, N: int, K: int, X, Y, M: int | None = None, stream=None):
+    """qmm_run_noalloc: the tensor-core product without any device allocation (fixed 4 MiB
+    library buffer for the prepared activations; see include/qmm.h for its limits)."""
+    if M is None:
+        M = X.shape[0]
+    st = load().qmm_run_noalloc(ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()),
+                                ctypes.c_void_p(Y.data_ptr()), M, _stream_handle(stream))
+    _check(st, "qmm_run_noalloc")
 
 
 def run_raw(wq_ptr: int, N: int, K: int, x_ptr: int, y_ptr: int, M: int, variant: int = VARIANT_AUTO,

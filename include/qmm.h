@@ -94,7 +94,8 @@ typedef enum {
   QMM_ERR_NONFINITE = 6,  /* qmm_pack: a weight is Inf/NaN or a scale overflows fp16      */
   QMM_ERR_CUDA = 7,       /* a CUDA runtime call or kernel launch failed                   */
   QMM_ERR_COUNT = 8,      /* qmm_run_batched: count outside [1, QMM_MAX_BATCH]              */
-  QMM_ERR_VARIANT = 9     /* an explicitly requested kernel variant cannot run this shape  */
+  QMM_ERR_VARIANT = 9,    /* an explicitly requested kernel variant cannot run this shape  */
+  QMM_ERR_SCRATCH = 10    /* qmm_run_noalloc: problem larger than its fixed device buffer  */
 } qmm_status;
 
 /* Bytes of the packed form of an N x K weight matrix: N * (K/256) * 144.
@@ -157,6 +158,29 @@ qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint1
 
 /* The variant qmm_run uses for this shape (never QMM_VARIANT_AUTO). */
 int qmm_select_variant(int M, int64_t N, int64_t K);
+
+/* Allocation-free variant of qmm_run (the paper has no counterpart; it exists for callers of
+ * this library).  Some callers cannot allocate device memory when they call in: code that runs
+ * while a stream is being captured into a CUDA graph (allocation is not a stream operation and
+ * breaks or is barred from the capture), latency-critical decode loops that must never touch the
+ * device allocator, and hosts that own a fixed device-memory budget or their own memory pool.
+ * qmm_run may allocate on first use (the tensor-core kernel's per-stream workspace); this call
+ * never does: it computes the same product with the tensor-core kernel and keeps the prepared
+ * activations in a fixed buffer of QMM_NOALLOC_SCRATCH_BYTES (4 MiB) that is part of the
+ * library's device image, held by every GPU that loads the library until the process exits.
+ *   - Limit: (K/256) * (Mpad*544 + 16) bytes must fit, Mpad = 16 for M <= 16 and 32 above:
+ *     K <= 61440 for M > 16, K <= 122880 for M <= 16.  Larger problems return QMM_ERR_SCRATCH
+ *     before anything is enqueued.
+ *   - The first call on each device looks up the buffer's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call shares the one buffer and leaves its contents behind; each call writes every
+ *     byte it reads before reading it, so nothing has to start zeroed.  Calls that overlap on the
+ *     GPU (concurrent streams, or host threads whose calls are not ordered) race on the buffer:
+ *     order them on one stream or serialize them.
+ * Arguments, layouts and the other errors are those of qmm_run. */
+#define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
+qmm_status qmm_run_noalloc(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
+                           float* Y_dev, int M, cudaStream_t stream);
 
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the
