@@ -9,6 +9,11 @@ with M activation rows (M = 8 by default: the pages' 8-row verify pass).  The we
 larger than L2 (129 MB), so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--M 8] [--impl ours|reference]
+  python bench.py --single gate_up|down|q|k|lm_head|all [--Ms 1,2,...] [--variant fma|tc|auto|both]
+
+`--single` times one matrix product per launch instead (weights cycled over copies totalling
+more than 4x the L2 size), for the switch-point sweep between the two kernel families and as
+the small case that profiling runs on.
 
 Under torchrun each rank runs its own full pass on its own GPU (independent problems, no
 collective on the data path); the timing is the max over ranks and `value` sums all ranks'
@@ -203,7 +208,8 @@ def time_steps(fn, steps: int, warmup: int, stream, sync_ranks):
 
 def cpu_baseline(info, M: int, budget_s: float = 12.0):
     """The oracle as it stands, timed on the host cores over a bounded sample of the pass:
-    evenly spaced rows of each of the six distinct matrices, M activation rows."""
+    evenly spaced rows of each of the six distinct matrices, M activation rows, repeated until
+    at least ~10 s of CPU work has run."""
     import numpy as np
     import oracle
     from bit_quantized_skinny_gb300 import inputs, workloads
@@ -219,20 +225,22 @@ def cpu_baseline(info, M: int, budget_s: float = 12.0):
     per_weight = (time.perf_counter() - t0) / (2 * cores * K)
     total_w = sum(N * K for _, N, K in shapes)
     frac = min(1.0, budget_s / (per_weight * total_w))
-    done_bytes, t_total, sampled_rows = 0, 0.0, 0
-    for idx, (name, N, K) in enumerate(shapes):
-        nrows = max(cores, int(N * frac))
-        rows = np.linspace(0, N - 1, nrows).astype(np.int64)
-        t0 = time.perf_counter()
-        oracle.matmul(info["hosts"][idx], N, K, xs[K], rows=rows)
-        t_total += time.perf_counter() - t0
-        done_bytes += nrows * (K // 256) * 144
-        sampled_rows += nrows
+    done_bytes, t_total, sampled_rows, rounds = 0, 0.0, 0, 0
+    while t_total < 0.8 * budget_s and rounds < 1000:
+        for idx, (name, N, K) in enumerate(shapes):
+            nrows = max(cores, int(N * frac))
+            rows = np.linspace(0, N - 1, nrows).astype(np.int64)
+            t0 = time.perf_counter()
+            oracle.matmul(info["hosts"][idx], N, K, xs[K], rows=rows)
+            t_total += time.perf_counter() - t0
+            done_bytes += nrows * (K // 256) * 144
+            sampled_rows += nrows
+        rounds += 1
     return {"value": round(weight_gbps(done_bytes, t_total * 1e3), 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": f"{sampled_rows} evenly spaced weight rows of the six distinct layer matrices "
-                      f"({done_bytes / 1e6:.1f} MB of packed weights, {frac * 100:.2f}% of one layer), "
-                      f"M={M}, fp64, OpenMP over rows; {t_total:.1f} s"}
+            "sample": f"{rounds} round(s) over {sampled_rows // rounds} evenly spaced weight rows of the six "
+                      f"distinct layer matrices ({done_bytes / 1e6:.1f} MB of packed weights in total, "
+                      f"{frac * 100:.2f}% of one layer per round), M={M}, fp64, OpenMP over rows; {t_total:.1f} s"}
 
 
 # ----------------------------------------------------------------------------- arms ------
@@ -253,6 +261,9 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
     M = args.M
     entries, info = layer_pass_setup(M, device)
 
+    variant = qmm.select_variant_batched(entries, M)
+    kernel = "q4k_tc_kernel" if variant == qmm.VARIANT_TC else "q4k_fma_kernel"
+    launches_per_step = 2 if variant == qmm.VARIANT_TC else 1   # activation prep + product
     step = lambda: qmm.run_batched(entries, M)
     step()
     torch.cuda.synchronize()
@@ -324,8 +335,11 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
         },
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": recorded_traffic("q4k_fma_kernel", "pass64", M),
-                     "kernel": "q4k_fma_kernel",
+                     "traffic": recorded_traffic(kernel, "pass64", M),
+                     "kernel": kernel,
+                     "timed": "whole step on the launching stream (the product kernel plus the "
+                              "activation-prep kernel, <0.2% of the step by ncu)" if launches_per_step == 2
+                              else "whole step on the launching stream (one kernel)",
                      "algorithmic_bytes_per_launch": info["algo_bytes"]},
         "e2e": {"value": round(weight_gbps(wb * world, ms_e2e), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -333,7 +347,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
                 "note": "qmm_run_batched with the step's X copied from pinned host memory and every "
                         "Y copied back to pinned host memory inside the timed region; the weights "
                         "are resident model parameters"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
+        "variant": qmm.VARIANT_NAMES.get(variant, str(variant)),
         "clocks": clocks.summary(),
         "per_M": per_m,
     }
@@ -341,6 +356,50 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
         line["cpu_baseline"] = cpu_baseline(info, M)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+SINGLE_SHAPES = {"gate_up": (34816, 5120), "down": (5120, 17408), "q": (5120, 5120), "k": (1024, 5120),
+                 "lm_head": (248320, 5120), "tiny": (256, 512)}
+
+
+def run_single(args):
+    """One product per launch, per shape x M x variant, weights cycled over copies totalling
+    more than 4x L2 so every launch reads HBM.  Prints one JSON line."""
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, inputs, qmm, workloads
+
+    build_lib.build()
+    qmm.load()
+    torch.cuda.set_device(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    names = list(SINGLE_SHAPES)[:5] if args.single == "all" else [args.single]
+    variants = {"fma": [qmm.VARIANT_FMA], "tc": [qmm.VARIANT_TC], "auto": [qmm.VARIANT_AUTO],
+                "both": [qmm.VARIANT_FMA, qmm.VARIANT_TC]}[args.variant]
+    stream = torch.cuda.current_stream()
+    results = {}
+    for name in names:
+        N, K = SINGLE_SHAPES[name]
+        Wd, _ = workloads.packed_weights(N, K, inputs.seed_for(3, list(SINGLE_SHAPES).index(name)), device="cuda")
+        copies = max(1, -(-4 * l2 // Wd.numel()))
+        ws = [Wd] + [Wd.clone() for _ in range(copies - 1)]
+        res = {}
+        for M in args.Ms:
+            X, _ = workloads.activations(M, K, inputs.seed_for(3, 50 + M), device="cuda")
+            Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            row = {"auto_picks": qmm.VARIANT_NAMES[qmm.select_variant(M, N, K)]}
+            for v in variants:
+                fn = lambda: [qmm.run(w, N, K, X, Y, M=M, variant=v) for w in ws]
+                ms = time_steps(fn, max(2, args.steps // 5), 3, stream, lambda: None) / len(ws)
+                row[qmm.VARIANT_NAMES.get(v, "auto")] = {"us": round(ms * 1e3, 2),
+                                                         "gbps": round(weight_gbps(Wd.numel(), ms), 1)}
+            res[str(M)] = row
+            if qmm.device_status() != 0:
+                raise RuntimeError("kernel reported a device-side error")
+        results[name] = {"N": N, "K": K, "weight_bytes": Wd.numel(), "copies": copies, "per_M": res}
+        del ws, Wd
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "weight-read GB/s per single product (one launch each)", "unit": UNIT,
+                      "l2": f"weights cycled over copies >= 4x L2 ({l2 >> 20} MB)", "shapes": results}), flush=True)
 
 
 def run_reference(args, rank: int):
@@ -408,6 +467,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 4, 8, 16, 32])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", choices=list(SINGLE_SHAPES) + ["all"], default=None)
+    ap.add_argument("--Ms", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 3, 4, 7, 8, 9, 12, 16])
+    ap.add_argument("--variant", choices=["fma", "tc", "auto", "both"], default="both")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -417,6 +479,10 @@ def main(argv=None):
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.single:
+        if rank == 0:
+            run_single(args)
         return
     dist_ok = False
     if world > 1:

@@ -180,6 +180,17 @@ qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
 
 int qmm_select_variant(int M, int64_t N, int64_t K) { return select_variant(M, N, K); }
 
+int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M) {
+  if (!entries_host || count < 1 || count > QMM_MAX_BATCH || M < 1 || M > QMM_MAX_M) return -1;
+  q4k::Job jobs[QMM_MAX_BATCH];
+  for (int k = 0; k < count; ++k) {
+    const qmm_entry& e = entries_host[k];
+    if (check_shape(e.N, e.K) != QMM_OK) return -1;
+    jobs[k] = q4k::Job{e.Wq, e.X, e.Y, e.N, e.K};
+  }
+  return select_variant_jobs(jobs, count, M);
+}
+
 qmm_status qmm_device_status(unsigned* status_out) {
   if (!status_out) return QMM_ERR_NULL;
   unsigned a = 0, b = 0;

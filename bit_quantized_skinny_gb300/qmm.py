@@ -29,7 +29,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANG
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
-           "qmm_last_cuda_error", "qmm_run_noalloc"]
+           "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -77,6 +77,8 @@ def load(path: str | None = None):
     lib.qmm_dequant.restype = i32
     lib.qmm_select_variant.argtypes = [i32, i64, i64]
     lib.qmm_select_variant.restype = i32
+    lib.qmm_select_variant_batched.argtypes = [ctypes.POINTER(_Entry), i32, i32]
+    lib.qmm_select_variant_batched.restype = i32
     lib.qmm_device_status.argtypes = [ctypes.POINTER(u32)]
     lib.qmm_device_status.restype = i32
     lib.qmm_strerror.argtypes = [i32]
@@ -166,6 +168,10 @@ def dequant(Wq, N: int, K: int, out, stream=None):
 
 def select_variant(M: int, N: int, K: int) -> int:
     return load().qmm_select_variant(M, N, K)
+
+
+def select_variant_batched(entries, M: int) -> int:
+    return load().qmm_select_variant_batched(entries, len(entries), M)
 
 
 def device_status() -> int:

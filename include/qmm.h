@@ -159,6 +159,10 @@ qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint1
 /* The variant qmm_run uses for this shape (never QMM_VARIANT_AUTO). */
 int qmm_select_variant(int M, int64_t N, int64_t K);
 
+/* The variant qmm_run_batched uses for these entries (one family runs the whole batch);
+ * -1 if the arguments are invalid. */
+int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M);
+
 /* Allocation-free variant of qmm_run (the paper has no counterpart; it exists for callers of
  * this library).  Some callers cannot allocate device memory when they call in: code that runs
  * while a stream is being captured into a CUDA graph (allocation is not a stream operation and
