@@ -71,8 +71,8 @@ constexpr int kWGroupSB = 4;                         // super-blocks per W stage
 constexpr int kWStages = 2;
 constexpr int kWRowStride = kWGroupSB * kBlockBytes + 16;   // 592: conflict-free 16-byte reads
 constexpr int kWStageBytes = kTileRows * kWRowStride;      // 38912
-constexpr int kASlots = 5;         // half-super-block A units in TMEM
-constexpr int kAccSlots = 2;
+constexpr int kMaxASlots = 5;      // half-super-block A units in TMEM
+constexpr int kMaxAccSlots = 4;
 constexpr int kScaleSlots = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
@@ -81,19 +81,28 @@ constexpr int kMaxE = 512;
 __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
 // activation-block ring depth: as deep as shared memory allows next to the weight stages
 __host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 8 : 4; }
-// A unit slot: 64 columns of sc*q pairs (128 k) + 8 columns of (m_j) pairs for the dmin MMA
-__host__ __device__ constexpr uint32_t a_col(int slot) { return 72u * slot; }        // 0..359
-__host__ __device__ constexpr uint32_t acc1_col(int slot) { return 384u + 64u * slot; }
-__host__ __device__ constexpr uint32_t acc2_col(int slot) { return 416u + 64u * slot; }
+// TMEM columns.  A unit slot: 64 columns of sc*q pairs (128 k) + 8 columns of (m_j) pairs for
+// the dmin MMA.  Accumulator slot: Mpad columns of the product, Mpad columns of the dmin term.
+// Mpad = 16: 5 A slots (0..359) + 4 accumulator slots (384..511); Mpad = 32: 5 + 2 (384..511).
+// Each MMA warp cycles through its own accumulator slots (super-block su uses su % slots), so
+// with four it can issue the next super-block while the epilogue still reads the last one.
+__host__ __device__ constexpr int a_slots(int) { return 5; }
+__host__ __device__ constexpr int acc_slots(int mpad) { return mpad <= 16 ? 4 : 2; }
+__host__ __device__ constexpr uint32_t a_col(int slot) { return 72u * slot; }
+__host__ __device__ constexpr uint32_t acc1_col(int mpad, int slot) {
+  return 512u - 2u * mpad * acc_slots(mpad) + 2u * mpad * slot;
+}
+__host__ __device__ constexpr uint32_t acc2_col(int mpad, int slot) { return acc1_col(mpad, slot) + mpad; }
+static_assert(72 * 5 <= 512 - 2 * 16 * 4 && 72 * 5 <= 512 - 2 * 32 * 2, "TMEM column plan overlaps");
 
 // barrier indices inside the barrier block
 constexpr int kMaxBSlots = 8;
 enum : int {
   kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages,
   kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
-  kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kASlots,
-  kBarAccFull = kBarAEmpty + kASlots, kBarAccEmpty = kBarAccFull + kAccSlots,
-  kBarScFull = kBarAccEmpty + kAccSlots, kBarScEmpty = kBarScFull + kScaleSlots,
+  kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kMaxASlots,
+  kBarAccFull = kBarAEmpty + kMaxASlots, kBarAccEmpty = kBarAccFull + kMaxAccSlots,
+  kBarScFull = kBarAccEmpty + kMaxAccSlots, kBarScEmpty = kBarScFull + kScaleSlots,
   kNumBars = kBarScEmpty + kScaleSlots
 };
 
@@ -239,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   using L = TcSmem<MPAD>;
   constexpr int kBB = bblock_bytes(MPAD);
   constexpr int kBSlots = b_slots(MPAD);
+  constexpr int kASlots = a_slots(MPAD);
+  constexpr int kAccSlots = acc_slots(MPAD);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t sW = smem_addr(smem + L::kW);
@@ -268,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_holder;
 
   auto wait = [&](int k, uint32_t parity) -> bool {
+    if (mbar_try(bar(k), parity)) return true;
     if (*abort_flag) return false;
     if (mbar_wait(bar(k), parity, kWaitLimit)) return true;
     atomicOr(&g_status, kErrWaitTimeout);
@@ -308,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
       const uint32_t mine = warp - kMmaWarp;
-      uint32_t su = 0;   // super-blocks (A units 2su, 2su+1; B slot su%4; accumulator su%2)
-      uint32_t em = 0;   // accumulator uses by this warp
+      uint32_t su = 0;   // super-blocks (A units 2su, 2su+1; B slot and accumulator slot by su)
+      uint32_t last = 0; // 1 + the last super-block this warp issued
       bool ok = true;
       for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
         const int nb = P.e[locate(t)].K >> 8;
@@ -317,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           if ((su & 1u) != mine) continue;
           const uint32_t u0 = 2 * su, u1 = 2 * su + 1;
           const uint32_t a0 = u0 % kASlots, a1 = u1 % kASlots;
-          const uint32_t bm = su, bs = bm % kBSlots, es = mine;
-          if (!wait(kBarAccEmpty + es, (em & 1u) ^ 1u) ||
+          const uint32_t bm = su, bs = bm % kBSlots, es = su % kAccSlots;
+          if (!wait(kBarAccEmpty + es, ((su / kAccSlots) & 1u) ^ 1u) ||
               !wait(kBarBFull + bs, (bm / kBSlots) & 1u) ||
               !wait(kBarAFull + a0, (u0 / kASlots) & 1u)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t d1 = tmem + acc1_col(es);
-          const uint32_t d2 = tmem + acc2_col(es);
+          const uint32_t d1 = tmem + acc1_col(MPAD, es);
+          const uint32_t d2 = tmem + acc2_col(MPAD, es);
           const uint32_t bslot = sB + bs * kBB;
           const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
           tc::mma_f16_ts_x8(d1, tmem + a_col(a0), bdesc, 16, idesc, 0);
@@ -335,11 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           tc::commit(bar(kBarAccFull + es));
           tc::commit(bar(kBarAEmpty + a1));
           tc::commit(bar(kBarBEmpty + bs));
-          ++em;
+          last = su + 1;
         }
       }
-      if (!ok && em > 0)   // let issued MMAs finish before TMEM is released
-        mbar_wait(bar(kBarAccFull + mine), (em - 1) & 1u, kWaitLimit);
+      if (!ok && last > 0)   // let issued MMAs finish before TMEM is released
+        mbar_wait(bar(kBarAccFull + (last - 1) % kAccSlots), ((last - 1) / kAccSlots) & 1u, kWaitLimit);
     }
   } else if (warp >= kWProdWarp0 && warp < kWProdWarp0 + kWProdWarps) {
     // ------------------------------------------------------------------ weight copies
@@ -384,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     const __half2 kn64 = __float2half2_rn(-64.f);
     bool ok = true;
     uint32_t G = 0;   // weight stages consumed
+    bool pending = false;      // a unit whose TMEM stores are issued but not yet published
+    uint32_t pending_as = 0;
     for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
       const TcEntry& E = P.e[locate(t)];
       const int nb = E.K >> 8;
@@ -391,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
         const uint32_t st = G % kWStages;
         if ((sb % kWGroupSB) == 0 && !wait(kBarWFull + st, (G / kWStages) & 1u)) { ok = false; break; }
         float sigma = 1.f;
-        if (h == 0) {
+        if (h == 1) {   // odd-half warps: activation scale, and the epilogue's per-row scales below
           const uint32_t bs = bc % kBSlots;
           if (!wait(kBarBFull + bs, (bc / kBSlots) & 1u)) { ok = false; break; }
           sigma = *reinterpret_cast<const float*>(smem + L::kB + bs * kBB + MPAD * 544);
@@ -399,8 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
         }
         const uint32_t u = 2 * su + h;
         const uint32_t as = u % kASlots;
-        if (!wait(kBarAEmpty + as, ((u / kASlots) & 1u) ^ 1u)) { ok = false; break; }
-        tc::fence_after_sync();
 
         // ---- this row's half super-block from shared memory
         const uint32_t rb = sW + st * kWStageBytes + r * kWRowStride + (sb % kWGroupSB) * kBlockBytes;
@@ -415,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           ++G;
         }
 
-        // ---- scales of this super-block for the epilogue (even-half warps)
-        if (h == 0) {
+        // ---- scales of this super-block for the epilogue (odd-half warps)
+        if (h == 1) {
           const float2 dd = __half22float2(bits2h(hd.x));
           const uint32_t ss = sc_cnt % kScaleSlots;
           if (!wait(kBarScEmpty + ss, ((sc_cnt / kScaleSlots) & 1u) ^ 1u)) { ok = false; break; }
@@ -425,6 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(bar(kBarScFull + ss));
           ++sc_cnt;
         }
+
+        // ---- the previous unit's TMEM stores have had the loads above to land: publish it
+        if (pending) {
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
+          pending = false;
+        }
+        if (!wait(kBarAEmpty + as, ((u / kASlots) & 1u) ^ 1u)) { ok = false; break; }
+        tc::fence_after_sync();
 
         // ---- the 12-bit (sc, m) groups of this half's sub-blocks 4h .. 4h+3
         const uint64_t F = h ? ((uint64_t)hd.w << 32 | hd.z) : ((uint64_t)hd.z << 32 | hd.y);
@@ -477,10 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
                 h2bits(__hsub2(bits2h((mm[2 * c] | 0x6400u) | ((mm[2 * c + 1] | 0x6400u) << 16)), k1024));
           tc::st_x8(aaddr + 64, ext);
         }
+        // published (wait::st + arrive) after the next unit's loads, or below
+        pending = true;
+        pending_as = as;
+      }
+      if (ok && pending) {   // last unit of the task
         tc::wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarAFull + as));
+        if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
+        pending = false;
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -503,24 +532,27 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
             !wait(kBarAccFull + es, (ec / kAccSlots) & 1u)) { ok = false; break; }
         tc::fence_after_sync();
         const float2 sc = scale_ring[ss * kTileRows + r];
-        // read the accumulators 16 tokens at a time (keeps the register footprint small)
+        // read the accumulators 16 tokens at a time (keeps the register footprint small); the
+        // slots are handed back as soon as the last read has landed, before the arithmetic
 #pragma unroll
         for (int c0 = 0; c0 < MPAD; c0 += 16) {
           float a1[16], a2[16];
-          tc::ld_x16(tl + acc1_col(es) + c0, a1);
-          tc::ld_x16(tl + acc2_col(es) + c0, a2);
+          tc::ld_x16(tl + acc1_col(MPAD, es) + c0, a1);
+          tc::ld_x16(tl + acc2_col(MPAD, es) + c0, a2);
           tc::wait_ld();
+          if (c0 + 16 == MPAD) {
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(bar(kBarAccEmpty + es));
+              mbar_arrive(bar(kBarScEmpty + ss));
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             y[c0 + c] = fmaf(sc.x, a1[c], y[c0 + c]);
             y[c0 + c] = fmaf(-sc.y, a2[c], y[c0 + c]);
           }
-        }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(kBarAccEmpty + es));
-          mbar_arrive(bar(kBarScEmpty + ss));
         }
         ++ec;
         ++scc;
