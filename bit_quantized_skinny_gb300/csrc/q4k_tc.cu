@@ -73,7 +73,7 @@ constexpr int kWRowStride = kWGroupSB * kBlockBytes + 16;   // 592: conflict-fre
 constexpr int kWStageBytes = kTileRows * kWRowStride;      // 38912
 constexpr int kMaxASlots = 5;      // half-super-block A units in TMEM
 constexpr int kMaxAccSlots = 4;
-constexpr int kScaleSlots = 4;
+constexpr int kScaleStages = 2;   // per-row (d, dmin) of one weight stage per slot
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxE = 512;
@@ -102,16 +102,16 @@ enum : int {
   kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
   kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kMaxASlots,
   kBarAccFull = kBarAEmpty + kMaxASlots, kBarAccEmpty = kBarAccFull + kMaxAccSlots,
-  kBarScFull = kBarAccEmpty + kMaxAccSlots, kBarScEmpty = kBarScFull + kScaleSlots,
-  kNumBars = kBarScEmpty + kScaleSlots
+  kBarScFull = kBarAccEmpty + kMaxAccSlots, kBarScEmpty = kBarScFull + kScaleStages,
+  kNumBars = kBarScEmpty + kScaleStages
 };
 
 template <int MPAD>
 struct TcSmem {
   static constexpr int kW = 0;
   static constexpr int kB = kW + kWStages * kWStageBytes;
-  static constexpr int kScale = kB + b_slots(MPAD) * bblock_bytes(MPAD);   // [slot][row] float2
-  static constexpr int kBars = kScale + kScaleSlots * kTileRows * 8;
+  static constexpr int kScale = kB + b_slots(MPAD) * bblock_bytes(MPAD);   // [slot][sb][row] (d, dmin) fp16
+  static constexpr int kBars = kScale + kScaleStages * kWGroupSB * kTileRows * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
 };
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   const uint32_t sW = smem_addr(smem + L::kW);
   const uint32_t sB = smem_addr(smem + L::kB);
-  float2* scale_ring = reinterpret_cast<float2*>(smem + L::kScale);
+  uint32_t* scale_ring = reinterpret_cast<uint32_t*>(smem + L::kScale);
   const uint32_t bars = smem_addr(smem + L::kBars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     for (int k = 0; k < kBSlots; ++k) { mbar_init(bar(kBarBFull + k), 1); mbar_init(bar(kBarBEmpty + k), 1); }
     for (int k = 0; k < kASlots; ++k) { mbar_init(bar(kBarAFull + k), 4); mbar_init(bar(kBarAEmpty + k), 1); }
     for (int k = 0; k < kAccSlots; ++k) { mbar_init(bar(kBarAccFull + k), 1); mbar_init(bar(kBarAccEmpty + k), kEpiWarps); }
-    for (int k = 0; k < kScaleSlots; ++k) { mbar_init(bar(kBarScFull + k), 4); mbar_init(bar(kBarScEmpty + k), kEpiWarps); }
+    for (int k = 0; k < kScaleStages; ++k) { mbar_init(bar(kBarScFull + k), 4); mbar_init(bar(kBarScEmpty + k), kEpiWarps); }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     const int h = warp >> 2;         // K half of each super-block (A unit parity)
     const int r = 32 * q + lane;     // row inside the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t su = 0, bc = 0, sc_cnt = 0;
+    uint32_t su = 0;
     const __half2 k1024 = bits2h(0x64006400u);
     const __half2 kn1024 = __float2half2_rn(-1024.f);
     const __half2 k1o16 = __float2half2_rn(0.0625f);
@@ -403,13 +403,19 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
       const int nb = E.K >> 8;
       for (int sb = 0; sb < nb && ok; ++sb, ++su) {
         const uint32_t st = G % kWStages;
-        if ((sb % kWGroupSB) == 0 && !wait(kBarWFull + st, (G / kWStages) & 1u)) { ok = false; break; }
-        float sigma = 1.f;
-        if (h == 1) {   // odd-half warps: activation scale, and the epilogue's per-row scales below
-          const uint32_t bs = bc % kBSlots;
-          if (!wait(kBarBFull + bs, (bc / kBSlots) & 1u)) { ok = false; break; }
-          sigma = *reinterpret_cast<const float*>(smem + L::kB + bs * kBB + MPAD * 544);
-          ++bc;
+        if ((sb % kWGroupSB) == 0) {
+          if (!wait(kBarWFull + st, (G / kWStages) & 1u)) { ok = false; break; }
+          if (h == 0) {
+            // the epilogue's per-row (d, dmin) of every super-block of this stage
+            const uint32_t ss = G % kScaleStages;
+            if (!wait(kBarScEmpty + ss, ((G / kScaleStages) & 1u) ^ 1u)) { ok = false; break; }
+            const int nsb = min(kWGroupSB, nb - sb);
+            const uint8_t* row = smem + L::kW + st * kWStageBytes + r * kWRowStride;
+            for (int i = 0; i < nsb; ++i)
+              scale_ring[(ss * kWGroupSB + i) * kTileRows + r] = *reinterpret_cast<const uint32_t*>(row + i * kBlockBytes);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarScFull + ss));
+          }
         }
         const uint32_t u = 2 * su + h;
         const uint32_t as = u % kASlots;
@@ -425,17 +431,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + st));
           ++G;
-        }
-
-        // ---- scales of this super-block for the epilogue (odd-half warps)
-        if (h == 1) {
-          const float2 dd = __half22float2(bits2h(hd.x));
-          const uint32_t ss = sc_cnt % kScaleSlots;
-          if (!wait(kBarScEmpty + ss, ((sc_cnt / kScaleSlots) & 1u) ^ 1u)) { ok = false; break; }
-          scale_ring[ss * kTileRows + r] = make_float2(dd.x * sigma, dd.y * sigma * 64.f);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarScFull + ss));
-          ++sc_cnt;
         }
 
         // ---- the previous unit's TMEM stores have had the loads above to land: publish it
@@ -517,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t ec = 0, scc = 0;
+    uint32_t ec = 0, eg = 0;   // super-blocks and weight stages consumed
     bool ok = true;
     float y[MPAD];
     for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
@@ -527,11 +522,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < MPAD; ++c) y[c] = 0.f;
       for (int sb = 0; sb < nb; ++sb) {
-        const uint32_t es = ec % kAccSlots, ss = scc % kScaleSlots;
-        if (!wait(kBarScFull + ss, (scc / kScaleSlots) & 1u) ||
+        const uint32_t es = ec % kAccSlots, ss = eg % kScaleStages;
+        const int sbi = sb % kWGroupSB;
+        const bool stage_end = sbi == kWGroupSB - 1 || sb == nb - 1;
+        // 2^s of this super-block's activations (written by the preparation kernel)
+        const float sigma = __ldg(reinterpret_cast<const float*>(E.B + (int64_t)sb * kBB + MPAD * 544));
+        if ((sbi == 0 && !wait(kBarScFull + ss, (eg / kScaleStages) & 1u)) ||
             !wait(kBarAccFull + es, (ec / kAccSlots) & 1u)) { ok = false; break; }
         tc::fence_after_sync();
-        const float2 sc = scale_ring[ss * kTileRows + r];
+        const float2 dd = __half22float2(bits2h(scale_ring[(ss * kWGroupSB + sbi) * kTileRows + r]));
+        const float2 sc = make_float2(dd.x * sigma, dd.y * sigma * 64.f);
         // read the accumulators 16 tokens at a time (keeps the register footprint small); the
         // slots are handed back as soon as the last read has landed, before the arithmetic
 #pragma unroll
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(bar(kBarAccEmpty + es));
-              mbar_arrive(bar(kBarScEmpty + ss));
+              if (stage_end) mbar_arrive(bar(kBarScEmpty + ss));
             }
           }
 #pragma unroll
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           }
         }
         ++ec;
-        ++scc;
+        if (stage_end) ++eg;
       }
       if (!ok) break;
       if (row0 + r < E.N) {
