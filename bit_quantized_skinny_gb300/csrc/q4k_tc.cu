@@ -60,47 +60,55 @@ __device__ unsigned g_status;   // this file's kernels' status word
 constexpr int kTileRows = 128;
 constexpr int kDqWarps = 8;        // warps 0..7: dequant (0..3 even K halves, 4..7 odd K halves)
 constexpr int kProdWarp = 8;       // bulk copies of the prepared activations
-constexpr int kMmaWarp = 9;        // warps 9, 10: MMA issue (super-blocks alternate); 9 owns TMEM
-constexpr int kMmaWarps = 2;
-constexpr int kWProdWarp0 = 11;    // warps 11..14: weight copies, 32 rows each
+constexpr int kMmaWarp = 9;        // warps 9..11: MMA issue (super-blocks round robin); 9 owns TMEM
+constexpr int kMmaWarps = 3;
+constexpr int kWProdWarp0 = 12;    // warps 12..15: weight copies, 32 rows each
 constexpr int kWProdWarps = 4;
-constexpr int kEpiWarp0 = 15;      // warps 15..18: epilogue
+constexpr int kEpiWarp0 = 16;      // warps 16..19: epilogue
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // 608
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // 640
 constexpr int kWGroupSB = 4;                         // super-blocks per W stage (576-byte row copies)
 constexpr int kWStages = 2;
 constexpr int kWRowStride = kWGroupSB * kBlockBytes + 16;   // 592: conflict-free 16-byte reads
 constexpr int kWStageBytes = kTileRows * kWRowStride;      // 38912
-constexpr int kMaxASlots = 5;      // half-super-block A units in TMEM
-constexpr int kMaxAccSlots = 4;
+constexpr int kMaxASlots = 6;      // A slots of both K halves together (upper bound)
+constexpr int kMaxAccSlots = 3;
 constexpr int kScaleStages = 2;   // per-row (d, dmin) of one weight stage per slot
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
+constexpr uint32_t kCountPolls = 1u << 22;   // bounded polls of a shared-memory counter
 constexpr int kMaxE = 512;
 
 __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
 // activation-block ring depth: as deep as shared memory allows next to the weight stages
 __host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 8 : 4; }
-// TMEM columns.  A unit slot: 64 columns of sc*q pairs (128 k) + 8 columns of (m_j) pairs for
-// the dmin MMA.  Accumulator slot: Mpad columns of the product, Mpad columns of the dmin term.
-// Mpad = 16: 5 A slots (0..359) + 4 accumulator slots (384..511); Mpad = 32: 5 + 2 (384..511).
-// Each MMA warp cycles through its own accumulator slots (super-block su uses su % slots), so
-// with four it can issue the next super-block while the epilogue still reads the last one.
-__host__ __device__ constexpr int a_slots(int) { return 5; }
-__host__ __device__ constexpr int acc_slots(int mpad) { return mpad <= 16 ? 4 : 2; }
-__host__ __device__ constexpr uint32_t a_col(int slot) { return 72u * slot; }
+// TMEM columns.  An even-half A unit: 64 columns of sc*q pairs (128 k); an odd-half unit adds 8
+// columns of (m_j) pairs for the dmin MMA.  Accumulator slot: Mpad columns of the product, Mpad
+// columns of the dmin term.  Each K half has its own ring of A slots (ar0 / ar1 deep):
+//   Mpad 16: even 3 x 64 (0..191), odd 3 x 72 (192..407), 3 accumulator slots (416..511)
+//   Mpad 32: even 2 x 64 (0..127), odd 3 x 72 (128..343), 2 accumulator slots (384..511)
+// Super-block su goes to MMA warp su % acc_slots, which owns accumulator slot su % acc_slots:
+// one issuing thread spends ~90 cycles per MMA, so the issue rate grows with the issuers.
+__host__ __device__ constexpr int acc_slots(int mpad) { return mpad <= 16 ? 3 : 2; }
+__host__ __device__ constexpr int ar0(int mpad) { return mpad <= 16 ? 3 : 2; }
+__host__ __device__ constexpr int ar1(int) { return 3; }
+__host__ __device__ constexpr uint32_t a0_col(int slot) { return 64u * slot; }
+__host__ __device__ constexpr uint32_t a1_col(int mpad, int slot) { return 64u * ar0(mpad) + 72u * slot; }
 __host__ __device__ constexpr uint32_t acc1_col(int mpad, int slot) {
   return 512u - 2u * mpad * acc_slots(mpad) + 2u * mpad * slot;
 }
 __host__ __device__ constexpr uint32_t acc2_col(int mpad, int slot) { return acc1_col(mpad, slot) + mpad; }
-static_assert(72 * 5 <= 512 - 2 * 16 * 4 && 72 * 5 <= 512 - 2 * 32 * 2, "TMEM column plan overlaps");
+static_assert(a1_col(16, ar1(16)) <= acc1_col(16, 0) && a1_col(32, ar1(32)) <= acc1_col(32, 0),
+              "TMEM column plan overlaps");
+static_assert(ar0(16) + ar1(16) <= kMaxASlots && ar0(32) + ar1(32) <= kMaxASlots, "A slot count");
+static_assert(acc_slots(16) <= kMmaWarps && acc_slots(32) <= kMmaWarps, "one MMA warp per accumulator slot");
 
 // barrier indices inside the barrier block
 constexpr int kMaxBSlots = 8;
 enum : int {
   kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages,
   kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
-  kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kMaxASlots,
+  kBarAEmpty = kBarBEmpty + kMaxBSlots,
   kBarAccFull = kBarAEmpty + kMaxASlots, kBarAccEmpty = kBarAccFull + kMaxAccSlots,
   kBarScFull = kBarAccEmpty + kMaxAccSlots, kBarScEmpty = kBarScFull + kScaleStages,
   kNumBars = kBarScEmpty + kScaleStages
@@ -113,7 +121,7 @@ struct TcSmem {
   static constexpr int kScale = kB + b_slots(MPAD) * bblock_bytes(MPAD);   // [slot][sb][row] (d, dmin) fp16
   static constexpr int kBars = kScale + kScaleStages * kWGroupSB * kTileRows * 4;
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, per-A-slot unit counters
 };
 
 struct TcEntry {
@@ -248,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   using L = TcSmem<MPAD>;
   constexpr int kBB = bblock_bytes(MPAD);
   constexpr int kBSlots = b_slots(MPAD);
-  constexpr int kASlots = a_slots(MPAD);
-  constexpr int kAccSlots = acc_slots(MPAD);
+  constexpr int kAccSlots = acc_slots(MPAD);   // also the number of MMA warps that issue
+  constexpr int kAR0 = ar0(MPAD), kAR1 = ar1(MPAD);   // A ring depths of the two K halves
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t sW = smem_addr(smem + L::kW);
@@ -258,15 +266,21 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   const uint32_t bars = smem_addr(smem + L::kBars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  // publications per A slot: each of the four dequant warps of the slot's K half adds one per
+  // use, and none can add for the next use before the MMAs of this one have completed, so a
+  // count of 4 (m + 1) means that all four wrote use m
+  const uint32_t a_count = smem_addr(smem + L::kMisc + 8);
+  static_assert(kMaxASlots <= 6, "A-slot counters exceed the misc block");
   auto bar = [&](int k) { return bars + 8u * k; };
 
   if (threadIdx.x == 0) {
     for (int k = 0; k < kWStages; ++k) { mbar_init(bar(kBarWFull + k), kWProdWarps); mbar_init(bar(kBarWEmpty + k), kDqWarps); }
     for (int k = 0; k < kBSlots; ++k) { mbar_init(bar(kBarBFull + k), 1); mbar_init(bar(kBarBEmpty + k), 1); }
-    for (int k = 0; k < kASlots; ++k) { mbar_init(bar(kBarAFull + k), 4); mbar_init(bar(kBarAEmpty + k), 1); }
+    for (int k = 0; k < kMaxASlots; ++k) mbar_init(bar(kBarAEmpty + k), 1);
     for (int k = 0; k < kAccSlots; ++k) { mbar_init(bar(kBarAccFull + k), 1); mbar_init(bar(kBarAccEmpty + k), kEpiWarps); }
     for (int k = 0; k < kScaleStages; ++k) { mbar_init(bar(kBarScFull + k), 4); mbar_init(bar(kBarScEmpty + k), kEpiWarps); }
     *abort_flag = 0;
+    for (int k = 0; k < kMaxASlots; ++k) reinterpret_cast<uint32_t*>(smem + L::kMisc + 8)[k] = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -282,6 +296,18 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     if (mbar_try(bar(k), parity)) return true;
     if (*abort_flag) return false;
     if (mbar_wait(bar(k), parity, kWaitLimit)) return true;
+    atomicOr(&g_status, kErrWaitTimeout);
+    *abort_flag = 1;
+    return false;
+  };
+  // wait until the counter at `addr` reaches `target` (release/acquire; no phase to alias)
+  auto wait_count = [&](uint32_t addr, uint32_t target) -> bool {
+    if ((int32_t)(ld_acquire_shared(addr) - target) >= 0) return true;
+    for (uint32_t it = 0; it < kCountPolls; ++it) {
+      if (*abort_flag) return false;
+      if (it >= 64) __nanosleep(64);
+      if ((int32_t)(ld_acquire_shared(addr) - target) >= 0) return true;
+    }
     atomicOr(&g_status, kErrWaitTimeout);
     *abort_flag = 1;
     return false;
@@ -315,35 +341,36 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     }
   } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
     // ------------------------------------------------------------------ MMA issue
-    // Two warps issue alternate super-blocks: a single thread spends ~45 cycles per MMA issue,
-    // two threads keep the tensor pipe busy about twice as long.
-    if (lane == 0) {
+    // Super-block su goes to warp su % kAccSlots (four issuers at Mpad 16, two at 32), which
+    // accumulates into its own TMEM slot.  A units come from per-K-half rings: kAR0 slots for the
+    // even half, kAR1 for the odd half; their publication is counted per slot, so issuers may
+    // wait on any future unit.
+    const uint32_t mine = warp - kMmaWarp;
+    if (lane == 0 && mine < (uint32_t)kAccSlots) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
-      const uint32_t mine = warp - kMmaWarp;
-      uint32_t su = 0;   // super-blocks (A units 2su, 2su+1; B slot and accumulator slot by su)
+      uint32_t su = 0;   // super-blocks of this CTA so far
       uint32_t last = 0; // 1 + the last super-block this warp issued
       bool ok = true;
       for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
         const int nb = P.e[locate(t)].K >> 8;
         for (int sb = 0; sb < nb; ++sb, ++su) {
-          if ((su & 1u) != mine) continue;
-          const uint32_t u0 = 2 * su, u1 = 2 * su + 1;
-          const uint32_t a0 = u0 % kASlots, a1 = u1 % kASlots;
-          const uint32_t bm = su, bs = bm % kBSlots, es = su % kAccSlots;
+          if (su % kAccSlots != mine) continue;
+          const uint32_t a0 = su % kAR0, a1 = kAR0 + su % kAR1;
+          const uint32_t bs = su % kBSlots, es = mine;
           if (!wait(kBarAccEmpty + es, ((su / kAccSlots) & 1u) ^ 1u) ||
-              !wait(kBarBFull + bs, (bm / kBSlots) & 1u) ||
-              !wait(kBarAFull + a0, (u0 / kASlots) & 1u)) { ok = false; break; }
+              !wait(kBarBFull + bs, (su / kBSlots) & 1u) ||
+              !wait_count(a_count + 4 * a0, 4 * (su / kAR0 + 1))) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t d1 = tmem + acc1_col(MPAD, es);
           const uint32_t d2 = tmem + acc2_col(MPAD, es);
           const uint32_t bslot = sB + bs * kBB;
           const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
-          tc::mma_f16_ts_x8(d1, tmem + a_col(a0), bdesc, 16, idesc, 0);
+          tc::mma_f16_ts_x8(d1, tmem + a0_col(a0), bdesc, 16, idesc, 0);
           tc::commit(bar(kBarAEmpty + a0));
-          if (!wait(kBarAFull + a1, (u1 / kASlots) & 1u)) { ok = false; break; }
+          if (!wait_count(a_count + 4 * a1, 4 * (su / kAR1 + 1))) { ok = false; break; }
           tc::fence_after_sync();
-          tc::mma_f16_ts_x8(d1, tmem + a_col(a1), bdesc + 8 * 16, 16, idesc, 1);
-          tc::mma_f16_ts(d2, tmem + a_col(a1) + 64, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
+          tc::mma_f16_ts_x8(d1, tmem + a1_col(MPAD, a1 - kAR0), bdesc + 8 * 16, 16, idesc, 1);
+          tc::mma_f16_ts(d2, tmem + a1_col(MPAD, a1 - kAR0) + 64, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
           tc::commit(bar(kBarAccFull + es));
           tc::commit(bar(kBarAEmpty + a1));
           tc::commit(bar(kBarBEmpty + bs));
@@ -397,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     bool ok = true;
     uint32_t G = 0;   // weight stages consumed
     bool pending = false;      // a unit whose TMEM stores are issued but not yet published
-    uint32_t pending_as = 0;
+    uint32_t pending_as = 0;   // and its A slot
     for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
       const TcEntry& E = P.e[locate(t)];
       const int nb = E.K >> 8;
@@ -417,8 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
             if (lane == 0) mbar_arrive(bar(kBarScFull + ss));
           }
         }
-        const uint32_t u = 2 * su + h;
-        const uint32_t as = u % kASlots;
+        // this half's A ring: slot and how many times it was used before
+        const uint32_t as = h ? kAR0 + su % kAR1 : su % kAR0;
+        const uint32_t use = h ? su / kAR1 : su / kAR0;
 
         // ---- this row's half super-block from shared memory
         const uint32_t rb = sW + st * kWStageBytes + r * kWRowStride + (sb % kWGroupSB) * kBlockBytes;
@@ -438,10 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           tc::wait_st();
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
+          if (lane == 0) red_release_add_shared(a_count + 4 * pending_as, 1);
           pending = false;
         }
-        if (!wait(kBarAEmpty + as, ((u / kASlots) & 1u) ^ 1u)) { ok = false; break; }
+        if (!wait(kBarAEmpty + as, (use & 1u) ^ 1u)) { ok = false; break; }
         tc::fence_after_sync();
 
         // ---- the 12-bit (sc, m) groups of this half's sub-blocks 4h .. 4h+3
@@ -459,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
         }
 
         // ---- A = sc*q as fp16 pairs, 16 columns per sub-block, into TMEM
-        const uint32_t aaddr = tl + a_col(as);
+        const uint32_t aaddr = tl + (h ? a1_col(MPAD, as - kAR0) : a0_col(as));
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t words[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
@@ -495,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
                 h2bits(__hsub2(bits2h((mm[2 * c] | 0x6400u) | ((mm[2 * c + 1] | 0x6400u) << 16)), k1024));
           tc::st_x8(aaddr + 64, ext);
         }
-        // published (wait::st + arrive) after the next unit's loads, or below
+        // published (wait::st + count) after the next unit's loads, or below
         pending = true;
         pending_as = as;
       }
@@ -503,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
         tc::wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
+        if (lane == 0) red_release_add_shared(a_count + 4 * pending_as, 1);
         pending = false;
       }
     }
