@@ -24,13 +24,15 @@
 // 8w+c+4 (high half), and the activations are laid out in B with the same permutation.
 //
 // Pipeline (one CTA per SM, persistent over 128-row tiles of every product in the launch):
-//   warp 8      producer: per-row bulk copies of two super-blocks per row into a 3-stage ring
-//               (row stride 304 bytes: bank-conflict-free 16-byte reads), and one bulk copy per
-//               super-block of the prepared B block into a 4-slot ring
-//   warps 0..7  dequant: warp w owns TMEM lanes 32*(w%4).. and K half w/4 of each super-block;
-//               then the epilogue of the previous super-block (token half w/4)
-//   warp 9      allocates TMEM; one thread issues 17 MMAs per super-block and commits them to
-//               the accumulator / A-slot / B-slot barriers
+//   warp 8        weights: one 2D TMA tile copy per super-block (128 rows x 144 bytes, rows
+//                 dense at 144 bytes: 16-byte reads of 8 consecutive rows hit 32 distinct banks)
+//                 into a 10-deep ring, evict-first in L2
+//   warp 9        one bulk copy per super-block of the prepared activation block into a ring
+//   warps 0..7    dequant: warp w owns TMEM lanes 32*(w%4).. and K half w/4 of each super-block,
+//                 writes A units into its half's ring of TMEM slots and counts them published
+//   warps 10..12  MMA issue, super-blocks round robin (one issuing thread spends ~90 cycles per
+//                 MMA, so the issue rate grows with the issuers); warp 10 owns TMEM
+//   warps 13..16  epilogue: per super-block, read the accumulators and (d, dmin) of each row
 // Every wait is bounded; on timeout the kernel records an error in the status word and drains.
 //
 // Activation preparation (q4k_xprep_kernel, one CTA per super-block of each distinct X): picks
@@ -42,8 +44,11 @@
 #include <cstdio>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 #include <vector>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "q4k_device.cuh"
@@ -59,36 +64,32 @@ __device__ unsigned g_status;   // this file's kernels' status word
 
 constexpr int kTileRows = 128;
 constexpr int kDqWarps = 8;        // warps 0..7: dequant (0..3 even K halves, 4..7 odd K halves)
-constexpr int kProdWarp = 8;       // bulk copies of the prepared activations
-constexpr int kMmaWarp = 9;        // warps 9..11: MMA issue (super-blocks round robin); 9 owns TMEM
+constexpr int kWProdWarp = 8;      // TMA tiles of the weights
+constexpr int kBProdWarp = 9;      // bulk copies of the prepared activations
+constexpr int kMmaWarp = 10;       // warps 10..12: MMA issue; 10 owns TMEM
 constexpr int kMmaWarps = 3;
-constexpr int kWProdWarp0 = 12;    // warps 12..15: weight copies, 32 rows each
-constexpr int kWProdWarps = 4;
-constexpr int kEpiWarp0 = 16;      // warps 16..19: epilogue
+constexpr int kEpiWarp0 = 13;      // warps 13..16: epilogue
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // 640
-constexpr int kWGroupSB = 4;                         // super-blocks per W stage (576-byte row copies)
-constexpr int kWStages = 2;
-constexpr int kWRowStride = kWGroupSB * kBlockBytes + 16;   // 592: conflict-free 16-byte reads
-constexpr int kWStageBytes = kTileRows * kWRowStride;      // 38912
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // 544
+constexpr int kWStageBytes = kTileRows * kBlockBytes;    // 18432: one super-block of a tile
+constexpr int kWStages = 10;
 constexpr int kMaxASlots = 6;      // A slots of both K halves together (upper bound)
 constexpr int kMaxAccSlots = 3;
-constexpr int kScaleStages = 2;   // per-row (d, dmin) of one weight stage per slot
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr uint32_t kCountPolls = 1u << 22;   // bounded polls of a shared-memory counter
-constexpr int kMaxE = 512;
+constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
+constexpr int kMaxPrep = 512;      // distinct activations per preparation launch
 
 __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
-// activation-block ring depth: as deep as shared memory allows next to the weight stages
-__host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 8 : 4; }
+// activation-block ring depth; at least the number of MMA issuers (see the MMA warps)
+__host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 4 : 2; }
 // TMEM columns.  An even-half A unit: 64 columns of sc*q pairs (128 k); an odd-half unit adds 8
 // columns of (m_j) pairs for the dmin MMA.  Accumulator slot: Mpad columns of the product, Mpad
 // columns of the dmin term.  Each K half has its own ring of A slots (ar0 / ar1 deep):
 //   Mpad 16: even 3 x 64 (0..191), odd 3 x 72 (192..407), 3 accumulator slots (416..511)
 //   Mpad 32: even 2 x 64 (0..127), odd 3 x 72 (128..343), 2 accumulator slots (384..511)
-// Super-block su goes to MMA warp su % acc_slots, which owns accumulator slot su % acc_slots:
-// one issuing thread spends ~90 cycles per MMA, so the issue rate grows with the issuers.
+// Super-block su goes to MMA warp su % acc_slots, which owns accumulator slot su % acc_slots.
 __host__ __device__ constexpr int acc_slots(int mpad) { return mpad <= 16 ? 3 : 2; }
 __host__ __device__ constexpr int ar0(int mpad) { return mpad <= 16 ? 3 : 2; }
 __host__ __device__ constexpr int ar1(int) { return 3; }
@@ -102,30 +103,29 @@ static_assert(a1_col(16, ar1(16)) <= acc1_col(16, 0) && a1_col(32, ar1(32)) <= a
               "TMEM column plan overlaps");
 static_assert(ar0(16) + ar1(16) <= kMaxASlots && ar0(32) + ar1(32) <= kMaxASlots, "A slot count");
 static_assert(acc_slots(16) <= kMmaWarps && acc_slots(32) <= kMmaWarps, "one MMA warp per accumulator slot");
+static_assert(b_slots(16) >= acc_slots(16) && b_slots(32) >= acc_slots(32), "B ring shallower than the issuers");
 
 // barrier indices inside the barrier block
-constexpr int kMaxBSlots = 8;
+constexpr int kMaxBSlots = 4;
 enum : int {
   kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages,
   kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
   kBarAEmpty = kBarBEmpty + kMaxBSlots,
   kBarAccFull = kBarAEmpty + kMaxASlots, kBarAccEmpty = kBarAccFull + kMaxAccSlots,
-  kBarScFull = kBarAccEmpty + kMaxAccSlots, kBarScEmpty = kBarScFull + kScaleStages,
-  kNumBars = kBarScEmpty + kScaleStages
+  kNumBars = kBarAccEmpty + kMaxAccSlots
 };
 
 template <int MPAD>
 struct TcSmem {
   static constexpr int kW = 0;
   static constexpr int kB = kW + kWStages * kWStageBytes;
-  static constexpr int kScale = kB + b_slots(MPAD) * bblock_bytes(MPAD);   // [slot][sb][row] (d, dmin) fp16
-  static constexpr int kBars = kScale + kScaleStages * kWGroupSB * kTileRows * 4;
+  static constexpr int kBars = kB + b_slots(MPAD) * bblock_bytes(MPAD);
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, per-A-slot unit counters
 };
+static_assert(TcSmem<16>::kTotal <= 232448 && TcSmem<32>::kTotal <= 232448, "shared memory");
 
 struct TcEntry {
-  const uint8_t* W;
   float* Y;
   const uint8_t* B;    // prepared activation blocks of this entry's X
   int N;
@@ -134,12 +134,16 @@ struct TcEntry {
   int task_begin;
 };
 
+// Launch parameters: the weights of entry e are reached through maps[e], a 2D tensor map over
+// the packed rows (inner dimension: the row's bytes, outer: the N rows).
+template <int MAXE>
 struct TcParams {
+  CUtensorMap maps[MAXE];
+  TcEntry e[MAXE];
   int count;
   int M;
   int tasks_total;
   int pad_;
-  TcEntry e[kMaxE];
 };
 
 struct PrepEntry {
@@ -154,7 +158,7 @@ struct PrepParams {
   int M;
   int blocks_total;
   int pad_;
-  PrepEntry e[kMaxE];
+  PrepEntry e[kMaxPrep];
 };
 
 __device__ __forceinline__ uint32_t h2bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
@@ -250,8 +254,18 @@ __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_consta
 }
 
 // ------------------------------------------------------------------------------------------
-template <int MPAD>
-__global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_constant__ TcParams P) {
+// 2D TMA tile copy global -> shared (this CTA), completing on the mbarrier; x is the byte offset
+// in the row (a multiple of 16), y the first row.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
+}
+
+template <int MPAD, int MAXE>
+__global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = TcSmem<MPAD>;
   constexpr int kBB = bblock_bytes(MPAD);
@@ -262,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   const uint32_t sW = smem_addr(smem + L::kW);
   const uint32_t sB = smem_addr(smem + L::kB);
-  uint32_t* scale_ring = reinterpret_cast<uint32_t*>(smem + L::kScale);
   const uint32_t bars = smem_addr(smem + L::kBars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
@@ -270,15 +283,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   // use, and none can add for the next use before the MMAs of this one have completed, so a
   // count of 4 (m + 1) means that all four wrote use m
   const uint32_t a_count = smem_addr(smem + L::kMisc + 8);
-  static_assert(kMaxASlots <= 6, "A-slot counters exceed the misc block");
   auto bar = [&](int k) { return bars + 8u * k; };
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < kWStages; ++k) { mbar_init(bar(kBarWFull + k), kWProdWarps); mbar_init(bar(kBarWEmpty + k), kDqWarps); }
+    for (int k = 0; k < kWStages; ++k) {
+      mbar_init(bar(kBarWFull + k), 1);
+      mbar_init(bar(kBarWEmpty + k), kDqWarps + kEpiWarps);   // dequant reads quants, epilogue (d, dmin)
+    }
     for (int k = 0; k < kBSlots; ++k) { mbar_init(bar(kBarBFull + k), 1); mbar_init(bar(kBarBEmpty + k), 1); }
     for (int k = 0; k < kMaxASlots; ++k) mbar_init(bar(kBarAEmpty + k), 1);
     for (int k = 0; k < kAccSlots; ++k) { mbar_init(bar(kBarAccFull + k), 1); mbar_init(bar(kBarAccEmpty + k), kEpiWarps); }
-    for (int k = 0; k < kScaleStages; ++k) { mbar_init(bar(kBarScFull + k), 4); mbar_init(bar(kBarScEmpty + k), kEpiWarps); }
     *abort_flag = 0;
     for (int k = 0; k < kMaxASlots; ++k) reinterpret_cast<uint32_t*>(smem + L::kMisc + 8)[k] = 0;
     fence_barrier_init();
@@ -321,30 +335,50 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     return lo;
   };
 
-  if (warp == kProdWarp) {
+  if (warp == kWProdWarp) {
+    // ------------------------------------------------------------------ weight tiles
+    // One TMA copy per super-block: rows row0 .. row0+127 (rows past N read as zeros), bytes
+    // 144 sb .. 144 sb + 143 of each row.  The ring runs kWStages - 1 super-blocks ahead.
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t su = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+        const int e = locate(t);
+        const TcEntry& E = P.e[e];
+        const int nb = E.K >> 8;
+        const int row0 = (t - E.task_begin) * kTileRows;
+        for (int sb = 0; sb < nb; ++sb, ++su) {
+          const uint32_t ws = su % kWStages;
+          if (!wait(kBarWEmpty + ws, ((su / kWStages) & 1u) ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(kBarWFull + ws), kWStageBytes);
+          tma_load_2d(sW + ws * kWStageBytes, &P.maps[e], sb * kBlockBytes, row0, bar(kBarWFull + ws), pol);
+        }
+      }
+    }
+  } else if (warp == kBProdWarp) {
     // ------------------------------------------------------------------ activation blocks
-    uint32_t bq = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-      const TcEntry& E = P.e[locate(t)];
-      const int nb = E.K >> 8;
-      for (int sb = 0; sb < nb; ++sb) {
-        const uint32_t bs = bq % kBSlots;
-        if (!wait(kBarBEmpty + bs, ((bq / kBSlots) & 1u) ^ 1u)) { ok = false; break; }
-        if (lane == 0) {
+    if (lane == 0) {
+      uint32_t su = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
+        const TcEntry& E = P.e[locate(t)];
+        const int nb = E.K >> 8;
+        for (int sb = 0; sb < nb; ++sb, ++su) {
+          const uint32_t bs = su % kBSlots;
+          if (!wait(kBarBEmpty + bs, ((su / kBSlots) & 1u) ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(kBarBFull + bs), kBB);
           bulk_g2s(sB + bs * kBB, E.B + (int64_t)sb * kBB, kBB, bar(kBarBFull + bs), 0ull);
         }
-        __syncwarp();
-        ++bq;
       }
     }
   } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
     // ------------------------------------------------------------------ MMA issue
-    // Super-block su goes to warp su % kAccSlots (four issuers at Mpad 16, two at 32), which
+    // Super-block su goes to warp su % kAccSlots (three issuers at Mpad 16, two at 32), which
     // accumulates into its own TMEM slot.  A units come from per-K-half rings: kAR0 slots for the
     // even half, kAR1 for the odd half; their publication is counted per slot, so issuers may
-    // wait on any future unit.
+    // wait on any future unit.  The B ring is at least kAccSlots deep, so an issuer that saw
+    // super-block su - kAccSlots's block arrive waits on the right phase of su's slot.
     const uint32_t mine = warp - kMmaWarp;
     if (lane == 0 && mine < (uint32_t)kAccSlots) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
@@ -380,86 +414,38 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
       if (!ok && last > 0)   // let issued MMAs finish before TMEM is released
         mbar_wait(bar(kBarAccFull + (last - 1) % kAccSlots), ((last - 1) / kAccSlots) & 1u, kWaitLimit);
     }
-  } else if (warp >= kWProdWarp0 && warp < kWProdWarp0 + kWProdWarps) {
-    // ------------------------------------------------------------------ weight copies
-    // Warp p copies rows 32p .. 32p+31 of every stage, one row (576 bytes) per lane: bulk copies
-    // from one warp are processed one after another, so four warps issue in parallel.
-    const int p = warp - kWProdWarp0;
-    const uint64_t pol = policy_evict_first();
-    uint32_t G = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-      const TcEntry& E = P.e[locate(t)];
-      const int nb = E.K >> 8;
-      const int row0 = (t - E.task_begin) * kTileRows;
-      const int nrows = min(kTileRows, E.N - row0);
-      const int64_t rowbytes = (int64_t)nb * kBlockBytes;
-      const int rr = 32 * p + lane;
-      const int mine = max(0, min(32, nrows - 32 * p));
-      for (int g = 0; g < (nb + kWGroupSB - 1) / kWGroupSB; ++g, ++G) {
-        const uint32_t st = G % kWStages;
-        if (!wait(kBarWEmpty + st, ((G / kWStages) & 1u) ^ 1u)) { ok = false; break; }
-        fence_proxy_async_smem();
-        const int nsb = min(kWGroupSB, nb - g * kWGroupSB);
-        const uint32_t bytes_row = nsb * kBlockBytes;
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarWFull + st), mine * bytes_row);
-        __syncwarp();
-        if (rr < nrows)
-          bulk_g2s(sW + st * kWStageBytes + rr * kWRowStride,
-                   E.W + (int64_t)(row0 + rr) * rowbytes + (int64_t)g * (kWGroupSB * kBlockBytes),
-                   bytes_row, bar(kBarWFull + st), pol);
-      }
-    }
   } else if (warp < kDqWarps) {
     // ------------------------------------------------------------------ dequant
     const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
-    const int h = warp >> 2;         // K half of each super-block (A unit parity)
+    const int h = warp >> 2;         // K half of each super-block
     const int r = 32 * q + lane;     // row inside the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t su = 0;
     const __half2 k1024 = bits2h(0x64006400u);
     const __half2 kn1024 = __float2half2_rn(-1024.f);
     const __half2 k1o16 = __float2half2_rn(0.0625f);
     const __half2 kn64 = __float2half2_rn(-64.f);
+    uint32_t su = 0;
     bool ok = true;
-    uint32_t G = 0;   // weight stages consumed
     bool pending = false;      // a unit whose TMEM stores are issued but not yet published
     uint32_t pending_as = 0;   // and its A slot
     for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
       const TcEntry& E = P.e[locate(t)];
       const int nb = E.K >> 8;
       for (int sb = 0; sb < nb && ok; ++sb, ++su) {
-        const uint32_t st = G % kWStages;
-        if ((sb % kWGroupSB) == 0) {
-          if (!wait(kBarWFull + st, (G / kWStages) & 1u)) { ok = false; break; }
-          if (h == 0) {
-            // the epilogue's per-row (d, dmin) of every super-block of this stage
-            const uint32_t ss = G % kScaleStages;
-            if (!wait(kBarScEmpty + ss, ((G / kScaleStages) & 1u) ^ 1u)) { ok = false; break; }
-            const int nsb = min(kWGroupSB, nb - sb);
-            const uint8_t* row = smem + L::kW + st * kWStageBytes + r * kWRowStride;
-            for (int i = 0; i < nsb; ++i)
-              scale_ring[(ss * kWGroupSB + i) * kTileRows + r] = *reinterpret_cast<const uint32_t*>(row + i * kBlockBytes);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarScFull + ss));
-          }
-        }
+        const uint32_t ws = su % kWStages;
+        if (!wait(kBarWFull + ws, (su / kWStages) & 1u)) { ok = false; break; }
         // this half's A ring: slot and how many times it was used before
         const uint32_t as = h ? kAR0 + su % kAR1 : su % kAR0;
         const uint32_t use = h ? su / kAR1 : su / kAR0;
 
-        // ---- this row's half super-block from shared memory
-        const uint32_t rb = sW + st * kWStageBytes + r * kWRowStride + (sb % kWGroupSB) * kBlockBytes;
+        // ---- this row's half super-block from shared memory; the stage is then released
+        const uint32_t rb = sW + ws * kWStageBytes + r * kBlockBytes;
         const uint4 hd = lds128(rb);
         uint4 qv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
-        if ((sb % kWGroupSB) == kWGroupSB - 1 || sb == nb - 1) {
-          // stage consumed by this warp (the producers refill it once all eight are done)
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarWEmpty + st));
-          ++G;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
 
         // ---- the previous unit's TMEM stores have had the loads above to land: publish it
         if (pending) {
@@ -540,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t ec = 0, eg = 0;   // super-blocks and weight stages consumed
+    uint32_t ec = 0;   // super-blocks consumed
     bool ok = true;
     float y[MPAD];
     for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
@@ -550,15 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < MPAD; ++c) y[c] = 0.f;
       for (int sb = 0; sb < nb; ++sb) {
-        const uint32_t es = ec % kAccSlots, ss = eg % kScaleStages;
-        const int sbi = sb % kWGroupSB;
-        const bool stage_end = sbi == kWGroupSB - 1 || sb == nb - 1;
+        const uint32_t es = ec % kAccSlots, ws = ec % kWStages;
         // 2^s of this super-block's activations (written by the preparation kernel)
         const float sigma = __ldg(reinterpret_cast<const float*>(E.B + (int64_t)sb * kBB + MPAD * 544));
-        if ((sbi == 0 && !wait(kBarScFull + ss, (eg / kScaleStages) & 1u)) ||
-            !wait(kBarAccFull + es, (ec / kAccSlots) & 1u)) { ok = false; break; }
+        if (!wait(kBarWFull + ws, (ec / kWStages) & 1u)) { ok = false; break; }
+        const uint32_t dpair = *reinterpret_cast<const uint32_t*>(smem + L::kW + ws * kWStageBytes + r * kBlockBytes);
+        if (!wait(kBarAccFull + es, (ec / kAccSlots) & 1u)) { ok = false; break; }
         tc::fence_after_sync();
-        const float2 dd = __half22float2(bits2h(scale_ring[(ss * kWGroupSB + sbi) * kTileRows + r]));
+        const float2 dd = __half22float2(bits2h(dpair));
         const float2 sc = make_float2(dd.x * sigma, dd.y * sigma * 64.f);
         // read the accumulators 16 tokens at a time (keeps the register footprint small); the
         // slots are handed back as soon as the last read has landed, before the arithmetic
@@ -573,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(bar(kBarAccEmpty + es));
-              if (stage_end) mbar_arrive(bar(kBarScEmpty + ss));
+              mbar_arrive(bar(kBarWEmpty + ws));
             }
           }
 #pragma unroll
@@ -583,7 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           }
         }
         ++ec;
-        if (stage_end) ++eg;
       }
       if (!ok) break;
       if (row0 + r < E.N) {
@@ -638,9 +622,104 @@ int num_sms() {
   return sms;
 }
 
+// ------------------------------------------------------------------------------------------
+// Tensor maps.  cuTensorMapEncodeTiled is a driver entry point, looked up through the runtime
+// (no link against the driver library).  A map depends only on (W, N, K), so encoded maps are
+// kept in a small cache.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Map of a packed Q4K matrix as a 2D byte array: inner dimension the K/256*144 bytes of a row,
+// outer dimension the N rows; the box is one super-block (144 bytes) of 128 rows.
+cudaError_t weight_map(const void* W, int64_t N, int64_t K, CUtensorMap* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int64_t, int64_t>, CUtensorMap> cache;
+  std::lock_guard<std::mutex> g(mu);
+  const auto key = std::make_tuple(W, N, K);
+  auto it = cache.find(key);
+  if (it != cache.end()) { *out = it->second; return cudaSuccess; }
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t rowbytes = (cuuint64_t)(K / 256) * kBlockBytes;
+  const cuuint64_t dims[2] = {rowbytes, (cuuint64_t)N};
+  const cuuint64_t strides[1] = {rowbytes};
+  const cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)kTileRows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (cache.size() >= 4096) cache.clear();
+  cache.emplace(key, m);
+  *out = m;
+  return cudaSuccess;
+}
+
+template <int MPAD, int MAXE>
+cudaError_t set_smem_attr() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  err = cudaFuncSetAttribute(q4k_tc_kernel<MPAD, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<MPAD>::kTotal);
+  if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return err;
+}
+
+// The main kernel over jobs[0 .. count) (count <= MAXE), whose prepared activations start at
+// bsrc[k].  Parameters are built in a static block under the caller's lock.
+template <int MPAD, int MAXE>
+cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, int count, int M, cudaStream_t stream) {
+  static TcParams<MAXE> par;
+  par.count = count;
+  par.M = M;
+  int tasks = 0;
+  for (int k = 0; k < count; ++k) {
+    cudaError_t err = weight_map(jobs[k].W, jobs[k].N, jobs[k].K, &par.maps[k]);
+    if (err != cudaSuccess) return err;
+    const int tiles = (int)((jobs[k].N + kTileRows - 1) / kTileRows);
+    par.e[k] = TcEntry{jobs[k].Y, bsrc[k], (int)jobs[k].N, (int)jobs[k].K, tiles, tasks};
+    tasks += tiles;
+  }
+  par.tasks_total = tasks;
+  cudaError_t err = set_smem_attr<MPAD, MAXE>();
+  if (err != cudaSuccess) return err;
+  const int grid = std::min(tasks, num_sms());
+  q4k_tc_kernel<MPAD, MAXE><<<grid, kThreads, TcSmem<MPAD>::kTotal, stream>>>(par);
+  return cudaGetLastError();
+}
+
+template <int MPAD>
+cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
+                        int M, cudaStream_t stream) {
+  static PrepParams prep;   // large: built on the host, passed by value at launch
+  prep.count = (int)xs.size();
+  prep.M = M;
+  int blocks = 0;
+  for (size_t u = 0; u < xs.size(); ++u) {
+    prep.e[u] = PrepEntry{xs[u].first, outs[u], (int)xs[u].second, blocks};
+    blocks += (int)(xs[u].second / 256);
+  }
+  prep.blocks_total = blocks;
+  q4k_xprep_kernel<MPAD><<<blocks, 8 * MPAD, 0, stream>>>(prep);
+  return cudaGetLastError();
+}
+
 template <int MPAD>
 cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) {
-  static_assert(sizeof(TcParams) < 32000 && sizeof(PrepParams) < 32000, "kernel parameters too large");
+  static_assert(sizeof(TcParams<kMaxEBatch>) < 32000 && sizeof(PrepParams) < 32000, "kernel parameters too large");
   constexpr int kBB = bblock_bytes(MPAD);
   // distinct activations (an X pointer with its K) get one prepared block run each
   std::vector<std::pair<const uint16_t*, int64_t>> xs;
@@ -652,9 +731,8 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
     if (found < 0) { found = (int)xs.size(); xs.push_back({jobs[k].X, jobs[k].K}); }
     xidx[k] = found;
   }
-  std::vector<size_t> xoff(xs.size());
   size_t bytes = 0;
-  int blocks = 0;
+  std::vector<size_t> xoff(xs.size());
   for (size_t u = 0; u < xs.size(); ++u) {
     xoff[u] = bytes;
     bytes += (size_t)(xs[u].second / 256) * kBB;
@@ -663,46 +741,21 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
   cudaError_t err = Workspace::get(stream, bytes, &wsp);
   if (err != cudaSuccess) return err;
   uint8_t* ws = static_cast<uint8_t*>(wsp);
+  std::vector<uint8_t*> outs(xs.size());
+  for (size_t u = 0; u < xs.size(); ++u) outs[u] = ws + xoff[u];
+  std::vector<const uint8_t*> bsrc(count);
+  for (int k = 0; k < count; ++k) bsrc[k] = outs[xidx[k]];
 
-  static PrepParams prep;   // large: built on the host, passed by value at launch
-  static TcParams par;
   static std::mutex mu;
   std::lock_guard<std::mutex> g(mu);
-  prep.count = (int)xs.size();
-  prep.M = M;
-  for (size_t u = 0; u < xs.size(); ++u) {
-    prep.e[u] = PrepEntry{xs[u].first, ws + xoff[u], (int)xs[u].second, blocks};
-    blocks += (int)(xs[u].second / 256);
-  }
-  prep.blocks_total = blocks;
-  q4k_xprep_kernel<MPAD><<<blocks, 8 * MPAD, 0, stream>>>(prep);
-  err = cudaGetLastError();
+  err = launch_prep<MPAD>(xs, outs, M, stream);
   if (err != cudaSuccess) return err;
-
-  par.count = count;
-  par.M = M;
-  int tasks = 0;
-  for (int k = 0; k < count; ++k) {
-    const int tiles = (int)((jobs[k].N + kTileRows - 1) / kTileRows);
-    par.e[k] = TcEntry{static_cast<const uint8_t*>(jobs[k].W), jobs[k].Y, ws + xoff[xidx[k]],
-                       (int)jobs[k].N, (int)jobs[k].K, tiles, tasks};
-    tasks += tiles;
-  }
-  par.tasks_total = tasks;
-  const int smem = TcSmem<MPAD>::kTotal;
-  auto kern = q4k_tc_kernel<MPAD>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (count == 1) return launch_main<MPAD, 1>(jobs, bsrc.data(), 1, M, stream);
+  for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
+    err = launch_main<MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
     if (err != cudaSuccess) return err;
-    if (dev < 64) attr_set[dev] = true;
   }
-  const int grid = std::min(tasks, num_sms());
-  kern<<<grid, kThreads, smem, stream>>>(par);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -714,37 +767,14 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes]
 
 template <int MPAD>
 cudaError_t launch_tc_noalloc_t(const Job& job, int M, cudaStream_t stream, uint8_t* scratch) {
-  constexpr int kBB = bblock_bytes(MPAD);
-  static PrepParams prep;   // separate from the workspace path: built here, passed by value
-  static TcParams par;
   static std::mutex mu;
-  static bool attr_set[64] = {};
   std::lock_guard<std::mutex> g(mu);
-  const int nb = (int)(job.K / 256);
-  prep.count = 1;
-  prep.M = M;
-  prep.e[0] = PrepEntry{job.X, scratch, (int)job.K, 0};
-  prep.blocks_total = nb;
-  q4k_xprep_kernel<MPAD><<<nb, 8 * MPAD, 0, stream>>>(prep);
-  cudaError_t err = cudaGetLastError();
+  const std::vector<std::pair<const uint16_t*, int64_t>> xs{{job.X, job.K}};
+  const std::vector<uint8_t*> outs{scratch};
+  cudaError_t err = launch_prep<MPAD>(xs, outs, M, stream);
   if (err != cudaSuccess) return err;
-  const int tiles = (int)((job.N + kTileRows - 1) / kTileRows);
-  par.count = 1;
-  par.M = M;
-  par.e[0] = TcEntry{static_cast<const uint8_t*>(job.W), job.Y, scratch, (int)job.N, (int)job.K, tiles, 0};
-  par.tasks_total = tiles;
-  const int smem = TcSmem<MPAD>::kTotal;
-  int dev = 0;
-  err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev >= 64 || !attr_set[dev]) {
-    err = cudaFuncSetAttribute(q4k_tc_kernel<MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) attr_set[dev] = true;
-  }
-  (void)kBB;
-  q4k_tc_kernel<MPAD><<<std::min(tiles, num_sms()), kThreads, smem, stream>>>(par);
-  return cudaGetLastError();
+  const uint8_t* bsrc = scratch;
+  return launch_main<MPAD, 1>(&job, &bsrc, 1, M, stream);
 }
 
 }  // namespace
@@ -793,7 +823,7 @@ cudaError_t launch_tc_noalloc(const Job& job, int M, cudaStream_t stream) {
 }
 
 cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream) {
-  if (count < 1 || count > kMaxE) return cudaErrorInvalidValue;
+  if (count < 1 || count > kMaxPrep) return cudaErrorInvalidValue;
   return (M <= 16) ? launch_tc_t<16>(jobs, count, M, stream) : launch_tc_t<32>(jobs, count, M, stream);
 }
 
