@@ -159,17 +159,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return false;
 }
 
-// Release-add to / acquire-load of a 32-bit counter in this CTA's shared memory: a producer
-// publishes work by counting it, consumers wait for the count they need.
-__device__ __forceinline__ void red_release_add_shared(uint32_t addr, uint32_t v) {
-  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 // Bulk copy global -> shared (this CTA), completing `bytes` on the mbarrier.  Both addresses
 // 16-byte aligned, bytes a multiple of 16.  The weights are read once: evict-first in L2.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,

@@ -29,7 +29,7 @@
 //                 into a 10-deep ring, evict-first in L2
 //   warp 9        one bulk copy per super-block of the prepared activation block into a ring
 //   warps 0..7    dequant: warp w owns TMEM lanes 32*(w%4).. and K half w/4 of each super-block,
-//                 writes A units into its half's ring of TMEM slots and counts them published
+//                 writes A units into its half's ring of TMEM slots
 //   warps 10..12  MMA issue, super-blocks round robin (one issuing thread spends ~90 cycles per
 //                 MMA, so the issue rate grows with the issuers); warp 10 owns TMEM
 //   warps 13..16  epilogue: per super-block, read the accumulators and (d, dmin) of each row
@@ -77,7 +77,6 @@ constexpr int kMaxASlots = 6;      // A slots of both K halves together (upper b
 constexpr int kMaxAccSlots = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
-constexpr uint32_t kCountPolls = 1u << 22;   // bounded polls of a shared-memory counter
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
 constexpr int kMaxPrep = 512;      // distinct activations per preparation launch
 
@@ -86,13 +85,15 @@ __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 1
 __host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 4 : 2; }
 // TMEM columns.  An even-half A unit: 64 columns of sc*q pairs (128 k); an odd-half unit adds 8
 // columns of (m_j) pairs for the dmin MMA.  Accumulator slot: Mpad columns of the product, Mpad
-// columns of the dmin term.  Each K half has its own ring of A slots (ar0 / ar1 deep):
-//   Mpad 16: even 3 x 64 (0..191), odd 3 x 72 (192..407), 3 accumulator slots (416..511)
-//   Mpad 32: even 2 x 64 (0..127), odd 3 x 72 (128..343), 2 accumulator slots (384..511)
-// Super-block su goes to MMA warp su % acc_slots, which owns accumulator slot su % acc_slots.
+// columns of the dmin term.  Each K half has its own ring of A slots, as deep as there are MMA
+// issuers, so super-block su uses slot su % issuers of each ring and accumulator slot
+// su % issuers, all owned by issuer su % issuers:
+//   Mpad 16: 3 issuers; even 3 x 64 (0..191), odd 3 x 72 (192..407), accumulators 416..511
+//   Mpad 32: 2 issuers; even 2 x 64 (0..127), odd 2 x 72 (128..271), accumulators 384..511
+// Every slot thus has one waiting issuer, which sees its phases in order.
 __host__ __device__ constexpr int acc_slots(int mpad) { return mpad <= 16 ? 3 : 2; }
-__host__ __device__ constexpr int ar0(int mpad) { return mpad <= 16 ? 3 : 2; }
-__host__ __device__ constexpr int ar1(int) { return 3; }
+__host__ __device__ constexpr int ar0(int mpad) { return acc_slots(mpad); }
+__host__ __device__ constexpr int ar1(int mpad) { return acc_slots(mpad); }
 __host__ __device__ constexpr uint32_t a0_col(int slot) { return 64u * slot; }
 __host__ __device__ constexpr uint32_t a1_col(int mpad, int slot) { return 64u * ar0(mpad) + 72u * slot; }
 __host__ __device__ constexpr uint32_t acc1_col(int mpad, int slot) {
@@ -110,7 +111,7 @@ constexpr int kMaxBSlots = 4;
 enum : int {
   kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages,
   kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
-  kBarAEmpty = kBarBEmpty + kMaxBSlots,
+  kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kMaxASlots,
   kBarAccFull = kBarAEmpty + kMaxASlots, kBarAccEmpty = kBarAccFull + kMaxAccSlots,
   kNumBars = kBarAccEmpty + kMaxAccSlots
 };
@@ -121,7 +122,7 @@ struct TcSmem {
   static constexpr int kB = kW + kWStages * kWStageBytes;
   static constexpr int kBars = kB + b_slots(MPAD) * bblock_bytes(MPAD);
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, per-A-slot unit counters
+  static constexpr int kTotal = kMisc + 16;   // TMEM address, abort flag
 };
 static_assert(TcSmem<16>::kTotal <= 232448 && TcSmem<32>::kTotal <= 232448, "shared memory");
 
@@ -279,10 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   const uint32_t bars = smem_addr(smem + L::kBars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-  // publications per A slot: each of the four dequant warps of the slot's K half adds one per
-  // use, and none can add for the next use before the MMAs of this one have completed, so a
-  // count of 4 (m + 1) means that all four wrote use m
-  const uint32_t a_count = smem_addr(smem + L::kMisc + 8);
   auto bar = [&](int k) { return bars + 8u * k; };
 
   if (threadIdx.x == 0) {
@@ -291,10 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
       mbar_init(bar(kBarWEmpty + k), kDqWarps + kEpiWarps);   // dequant reads quants, epilogue (d, dmin)
     }
     for (int k = 0; k < kBSlots; ++k) { mbar_init(bar(kBarBFull + k), 1); mbar_init(bar(kBarBEmpty + k), 1); }
-    for (int k = 0; k < kMaxASlots; ++k) mbar_init(bar(kBarAEmpty + k), 1);
+    for (int k = 0; k < kMaxASlots; ++k) { mbar_init(bar(kBarAFull + k), 4); mbar_init(bar(kBarAEmpty + k), 1); }
     for (int k = 0; k < kAccSlots; ++k) { mbar_init(bar(kBarAccFull + k), 1); mbar_init(bar(kBarAccEmpty + k), kEpiWarps); }
     *abort_flag = 0;
-    for (int k = 0; k < kMaxASlots; ++k) reinterpret_cast<uint32_t*>(smem + L::kMisc + 8)[k] = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -310,18 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
     if (mbar_try(bar(k), parity)) return true;
     if (*abort_flag) return false;
     if (mbar_wait(bar(k), parity, kWaitLimit)) return true;
-    atomicOr(&g_status, kErrWaitTimeout);
-    *abort_flag = 1;
-    return false;
-  };
-  // wait until the counter at `addr` reaches `target` (release/acquire; no phase to alias)
-  auto wait_count = [&](uint32_t addr, uint32_t target) -> bool {
-    if ((int32_t)(ld_acquire_shared(addr) - target) >= 0) return true;
-    for (uint32_t it = 0; it < kCountPolls; ++it) {
-      if (*abort_flag) return false;
-      if (it >= 64) __nanosleep(64);
-      if ((int32_t)(ld_acquire_shared(addr) - target) >= 0) return true;
-    }
     atomicOr(&g_status, kErrWaitTimeout);
     *abort_flag = 1;
     return false;
@@ -375,10 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
     // ------------------------------------------------------------------ MMA issue
     // Super-block su goes to warp su % kAccSlots (three issuers at Mpad 16, two at 32), which
-    // accumulates into its own TMEM slot.  A units come from per-K-half rings: kAR0 slots for the
-    // even half, kAR1 for the odd half; their publication is counted per slot, so issuers may
-    // wait on any future unit.  The B ring is at least kAccSlots deep, so an issuer that saw
-    // super-block su - kAccSlots's block arrive waits on the right phase of su's slot.
+    // owns accumulator slot su % kAccSlots and A slot su % kAccSlots of each K half's ring.  The
+    // B ring is at least kAccSlots deep, so an issuer that saw super-block su - kAccSlots's block
+    // arrive waits on the right phase of su's slot.
     const uint32_t mine = warp - kMmaWarp;
     if (lane == 0 && mine < (uint32_t)kAccSlots) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
@@ -389,11 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
         const int nb = P.e[locate(t)].K >> 8;
         for (int sb = 0; sb < nb; ++sb, ++su) {
           if (su % kAccSlots != mine) continue;
-          const uint32_t a0 = su % kAR0, a1 = kAR0 + su % kAR1;
+          const uint32_t a0 = mine, a1 = kAR0 + mine;
           const uint32_t bs = su % kBSlots, es = mine;
-          if (!wait(kBarAccEmpty + es, ((su / kAccSlots) & 1u) ^ 1u) ||
+          const uint32_t use = (su / kAccSlots) & 1u;   // phase parity of this warp's slots
+          if (!wait(kBarAccEmpty + es, use ^ 1u) ||
               !wait(kBarBFull + bs, (su / kBSlots) & 1u) ||
-              !wait_count(a_count + 4 * a0, 4 * (su / kAR0 + 1))) { ok = false; break; }
+              !wait(kBarAFull + a0, use)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t d1 = tmem + acc1_col(MPAD, es);
           const uint32_t d2 = tmem + acc2_col(MPAD, es);
@@ -401,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
           tc::mma_f16_ts_x8(d1, tmem + a0_col(a0), bdesc, 16, idesc, 0);
           tc::commit(bar(kBarAEmpty + a0));
-          if (!wait_count(a_count + 4 * a1, 4 * (su / kAR1 + 1))) { ok = false; break; }
+          if (!wait(kBarAFull + a1, use)) { ok = false; break; }
           tc::fence_after_sync();
           tc::mma_f16_ts_x8(d1, tmem + a1_col(MPAD, a1 - kAR0), bdesc + 8 * 16, 16, idesc, 1);
           tc::mma_f16_ts(d2, tmem + a1_col(MPAD, a1 - kAR0) + 64, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
@@ -452,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           tc::wait_st();
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) red_release_add_shared(a_count + 4 * pending_as, 1);
+          if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
           pending = false;
         }
         if (!wait(kBarAEmpty + as, (use & 1u) ^ 1u)) { ok = false; break; }
@@ -509,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
                 h2bits(__hsub2(bits2h((mm[2 * c] | 0x6400u) | ((mm[2 * c + 1] | 0x6400u) << 16)), k1024));
           tc::st_x8(aaddr + 64, ext);
         }
-        // published (wait::st + count) after the next unit's loads, or below
+        // published (wait::st + arrive) after the next unit's loads, or below
         pending = true;
         pending_as = as;
       }
@@ -517,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
         tc::wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) red_release_add_shared(a_count + 4 * pending_as, 1);
+        if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
         pending = false;
       }
     }
