@@ -23,17 +23,34 @@
 // fp16 pairs (q0,q4) (q1,q5) (q2,q6) (q3,q7); TMEM column 4w+c holds k = 8w+c (low half) and
 // 8w+c+4 (high half), and the activations are laid out in B with the same permutation.
 //
-// Pipeline (one CTA per SM, persistent over 128-row tiles of every product in the launch):
-//   warp 8        weights: one 2D TMA tile copy per super-block (128 rows x 144 bytes, rows
-//                 dense at 144 bytes: 16-byte reads of 8 consecutive rows hit 32 distinct banks)
-//                 into a 10-deep ring, evict-first in L2
-//   warp 9        one bulk copy per super-block of the prepared activation block into a ring
-//   warps 0..7    dequant: warp w owns TMEM lanes 32*(w%4).. and K half w/4 of each super-block,
-//                 writes A units into its half's ring of TMEM slots
-//   warps 10..12  MMA issue, super-blocks round robin (one issuing thread spends ~90 cycles per
-//                 MMA, so the issue rate grows with the issuers); warp 10 owns TMEM
-//   warps 13..16  epilogue: per super-block, read the accumulators and (d, dmin) of each row
-// Every wait is bounded; on timeout the kernel records an error in the status word and drains.
+// Work: a task is one 128-row tile of one product over a range of its super-blocks (a K split).
+// Summation order: a row's super-blocks are summed in chunks of 4 (each chunk from zero, in order
+// of k) and the chunk sums are added in chunk order; splits cut only at chunk boundaries, so a
+// product's bits depend neither on M nor on how its work is split or batched.  One CTA per SM.
+//
+// Roles (448 threads at Mpad 16, 320 at Mpad 32):
+//   dequant groups (3 at Mpad 16, 2 at Mpad 32; 4 warps each, warp q <-> TMEM lanes 32q..32q+31,
+//                the rows of the tile).  The CTA's tasks are dealt to the groups round robin; a
+//                group walks its tasks' super-blocks in order.  Each group owns one A slot and
+//                one accumulator in TMEM.  Per super-block: read the stage, write the A slot one
+//                K half at a time (each half handed to the MMA lane as soon as it is written),
+//                wait for the MMAs, read the accumulator and scale it into y.
+//   copy warp    per super-block one 2D TMA tile copy of the weights (128 rows x 144 bytes) and
+//                one bulk copy of the prepared activation block into a stage of an 8-deep ring
+//                (6 at Mpad 32), in the CTA's super-block order: rounds over the groups.
+//   MMA warp     owns TMEM; one elected lane issues each super-block's 17 MMAs (8 per K half and
+//                one for the dmin term) in the same order.  Issuing from an elect.sync branch
+//                keeps the operands in uniform registers (~14 cycles per MMA).
+// Every barrier is waited on only by threads that see all of its phases in order (a parity wait
+// is exact only then): full barriers per (group, stage), handoff and completion barriers per
+// group.  Every wait is bounded; on timeout the kernel records an error in the status word, the
+// other roles stop at their next wait, and in-flight copies and MMAs are waited for before the
+// CTA ends.
+//
+// Split K (single products with few tiles): a split task stores its chunk sums to a per-call
+// workspace; the last split of a (tile, lane quarter) slice to finish (an atomic counter per
+// slice, zeroed by the preparation kernel of the same call) adds all chunk sums of the tile in
+// chunk order and writes Y.
 //
 // Activation preparation (q4k_xprep_kernel, one CTA per super-block of each distinct X): picks
 // s so that the largest |x| of the super-block lands in [2^14, 2^15); a bf16 value is then exact
@@ -63,75 +80,79 @@ namespace {
 __device__ unsigned g_status;   // this file's kernels' status word
 
 constexpr int kTileRows = 128;
-constexpr int kDqWarps = 8;        // warps 0..7: dequant (0..3 even K halves, 4..7 odd K halves)
-constexpr int kWProdWarp = 8;      // TMA tiles of the weights
-constexpr int kBProdWarp = 9;      // bulk copies of the prepared activations
-constexpr int kMmaWarp = 10;       // warps 10..12: MMA issue; 10 owns TMEM
-constexpr int kMmaWarps = 3;
-constexpr int kEpiWarp0 = 13;      // warps 13..16: epilogue
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // 544
+constexpr int kGroupWarps = 4;     // a dequant group: one warp per TMEM lane quarter (32 rows)
+constexpr int kMaxGroups = 3;
+// Dequant groups: three at Mpad 16, two at Mpad 32 (what tensor memory holds, below).  With the
+// copy and MMA warps that is at most 14 warps, at most 4 per SM sub-partition, which leaves each
+// thread 128 registers (a sub-partition holds 16384).
+__host__ __device__ constexpr int groups(int mpad) { return mpad <= 16 ? 3 : 2; }
+__host__ __device__ constexpr int threads(int mpad) { return 32 * (groups(mpad) * kGroupWarps + 2); }
 constexpr int kWStageBytes = kTileRows * kBlockBytes;    // 18432: one super-block of a tile
-constexpr int kWStages = 10;
-constexpr int kMaxASlots = 6;      // A slots of both K halves together (upper bound)
-constexpr int kMaxAccSlots = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
 constexpr int kMaxPrep = 512;      // distinct activations per preparation launch
 
 __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
-// activation-block ring depth; at least the number of MMA issuers (see the MMA warps)
-__host__ __device__ constexpr int b_slots(int mpad) { return mpad <= 16 ? 4 : 2; }
-// TMEM columns.  An even-half A unit: 64 columns of sc*q pairs (128 k); an odd-half unit adds 8
-// columns of (m_j) pairs for the dmin MMA.  Accumulator slot: Mpad columns of the product, Mpad
-// columns of the dmin term.  Each K half has its own ring of A slots, as deep as there are MMA
-// issuers, so super-block su uses slot su % issuers of each ring and accumulator slot
-// su % issuers, all owned by issuer su % issuers:
-//   Mpad 16: 3 issuers; even 3 x 64 (0..191), odd 3 x 72 (192..407), accumulators 416..511
-//   Mpad 32: 2 issuers; even 2 x 64 (0..127), odd 2 x 72 (128..271), accumulators 384..511
-// Every slot thus has one waiting issuer, which sees its phases in order.
-__host__ __device__ constexpr int acc_slots(int mpad) { return mpad <= 16 ? 3 : 2; }
-__host__ __device__ constexpr int ar0(int mpad) { return acc_slots(mpad); }
-__host__ __device__ constexpr int ar1(int mpad) { return acc_slots(mpad); }
-__host__ __device__ constexpr uint32_t a0_col(int slot) { return 64u * slot; }
-__host__ __device__ constexpr uint32_t a1_col(int mpad, int slot) { return 64u * ar0(mpad) + 72u * slot; }
-__host__ __device__ constexpr uint32_t acc1_col(int mpad, int slot) {
-  return 512u - 2u * mpad * acc_slots(mpad) + 2u * mpad * slot;
-}
-__host__ __device__ constexpr uint32_t acc2_col(int mpad, int slot) { return acc1_col(mpad, slot) + mpad; }
-static_assert(a1_col(16, ar1(16)) <= acc1_col(16, 0) && a1_col(32, ar1(32)) <= acc1_col(32, 0),
+// A stage holds one super-block of a tile (the weight rows) and the prepared activation block
+// of the same super-block: both arrive on one barrier, issued the same distance ahead.
+// (rounded up to 128 bytes: a TMA tile copy writes to a 128-byte aligned address)
+__host__ __device__ constexpr int stage_bytes(int mpad) { return (kWStageBytes + bblock_bytes(mpad) + 127) / 128 * 128; }
+__host__ __device__ constexpr int stages(int mpad) { return mpad <= 16 ? 8 : 6; }
+constexpr int kMaxStages = 8;
+// TMEM columns.  Each group owns one A slot (one super-block: 64 columns of sc*q pairs per K
+// half and 8 columns of (m_j) pairs for the dmin MMA, 136 in all) and one accumulator (Mpad
+// columns of the product and Mpad of the dmin term, at the top of the 512 columns):
+//   Mpad 16: A slots 0..407, accumulators 416..511
+//   Mpad 32: A slots 0..271, accumulators 384..511
+constexpr uint32_t kACols = 136;
+// Summation order of a product: the super-blocks of a row are summed in chunks of kChunkSb (each
+// chunk from zero, in order of k), and the chunk sums are then added in chunk order.  A K split
+// only ever cuts at chunk boundaries, so the bits of a product do not depend on the split.
+constexpr int kChunkSb = 4;
+__host__ __device__ constexpr uint32_t a_col(int g) { return kACols * g; }
+__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g) { return 512u - 2u * mpad * groups(mpad) + 2u * mpad * g; }
+__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g) { return acc1_col(mpad, g) + mpad; }
+static_assert(a_col(groups(16)) <= acc1_col(16, 0) && a_col(groups(32)) <= acc1_col(32, 0),
               "TMEM column plan overlaps");
-static_assert(ar0(16) + ar1(16) <= kMaxASlots && ar0(32) + ar1(32) <= kMaxASlots, "A slot count");
-static_assert(acc_slots(16) <= kMmaWarps && acc_slots(32) <= kMmaWarps, "one MMA warp per accumulator slot");
-static_assert(b_slots(16) >= acc_slots(16) && b_slots(32) >= acc_slots(32), "B ring shallower than the issuers");
 
-// barrier indices inside the barrier block
-constexpr int kMaxBSlots = 4;
+// Barrier indices inside the barrier block.  Every barrier is waited on by threads that see
+// all of its phases in order (a parity wait is only exact then):
+//   GFull[g][s]  stage s holds a super-block of group g (copies landed); group g, MMA lane
+//   WEmpty[s]    stage s consumed (the group's 4 warps + the MMA commit); copy lane
+//   AFull[g][h]  K half h of group g's A slot written; MMA lane
+//   GDone[g]     the MMAs of group g's latest super-block completed; group g
+//   Drain        the last MMAs of the CTA completed; MMA lane
 enum : int {
-  kBarWFull = 0, kBarWEmpty = kBarWFull + kWStages,
-  kBarBFull = kBarWEmpty + kWStages, kBarBEmpty = kBarBFull + kMaxBSlots,
-  kBarAFull = kBarBEmpty + kMaxBSlots, kBarAEmpty = kBarAFull + kMaxASlots,
-  kBarAccFull = kBarAEmpty + kMaxASlots, kBarAccEmpty = kBarAccFull + kMaxAccSlots,
-  kNumBars = kBarAccEmpty + kMaxAccSlots
+  kBarGFull = 0, kBarWEmpty = kBarGFull + kMaxGroups * kMaxStages,
+  kBarAFull = kBarWEmpty + kMaxStages, kBarGDone = kBarAFull + 2 * kMaxGroups,
+  kBarDrain = kBarGDone + kMaxGroups,
+  kNumBars = kBarDrain + 1
 };
 
 template <int MPAD>
 struct TcSmem {
   static constexpr int kW = 0;
-  static constexpr int kB = kW + kWStages * kWStageBytes;
-  static constexpr int kBars = kB + b_slots(MPAD) * bblock_bytes(MPAD);
+  static constexpr int kBars = kW + stages(MPAD) * stage_bytes(MPAD);
   static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 16;   // TMEM address, abort flag
+  static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
 static_assert(TcSmem<16>::kTotal <= 232448 && TcSmem<32>::kTotal <= 232448, "shared memory");
+static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
+static_assert(stage_bytes(16) % 128 == 0 && stage_bytes(32) % 128 == 0 && kWStageBytes % 128 == 0, "stage alignment");
+static_assert(stages(16) <= kMaxStages && stages(32) <= kMaxStages, "stage barriers");
 
 struct TcEntry {
   float* Y;
   const uint8_t* B;    // prepared activation blocks of this entry's X
+  float* partial;      // split > 1: tiles x chunks x Mpad x 128 chunk partial sums
+  unsigned* counters;  // split > 1: tiles x 4 arrival counters (zeroed by the preparation)
   int N;
   int K;
   int tiles;
+  int splits;          // K splits per tile
+  int chunk;           // super-blocks per split, a multiple of kChunkSb (the last may have fewer)
+  int chunks;          // summation chunks per row: ceil(K/256 / kChunkSb)
   int task_begin;
 };
 
@@ -158,7 +179,8 @@ struct PrepParams {
   int count;
   int M;
   int blocks_total;
-  int pad_;
+  int zero_words;      // split counters of the main launches of this call, zeroed here
+  unsigned* zero;
   PrepEntry e[kMaxPrep];
 };
 
@@ -184,6 +206,7 @@ __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_consta
   const PrepEntry& E = P.e[e];
   const int sb = b - E.block_begin;
   const int t = threadIdx.x;
+  for (int z = b * (8 * MPAD) + t; z < P.zero_words; z += P.blocks_total * (8 * MPAD)) P.zero[z] = 0u;
   const int i = t >> 3, j = t & 7;
   const bool valid = i < P.M;
   uint4 v[4];
@@ -265,33 +288,119 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
 }
 
+// The last split of a (tile, lane quarter) slice: this thread's row of the tile, the sum of
+// every chunk partial in chunk order, tokens below M, to y (nullptr: the row is past N).  Out of
+// line: it runs once per split tile and would otherwise take registers from the hot loop.
+template <int MPAD>
+__device__ __noinline__ void reduce_chunks(const float* part, int chunks, int M, float* y, int N) {
+  float v[MPAD];
+#pragma unroll
+  for (int k = 0; k < MPAD; ++k) v[k] = (k < M) ? __ldcg(&part[k * kTileRows]) : 0.f;
+  for (int ch = 1; ch < chunks; ++ch) {
+#pragma unroll
+    for (int k = 0; k < MPAD; ++k)
+      if (k < M) v[k] = v[k] + __ldcg(&part[((size_t)ch * MPAD + k) * kTileRows]);
+  }
+  if (y) {
+#pragma unroll
+    for (int k = 0; k < MPAD; ++k)
+      if (k < M) y[(int64_t)k * N] = v[k];
+  }
+}
+
+// Task t of the launch: its entry, tile and K split, and its super-block range.
+template <int MAXE>
+struct TaskView {
+  int e, tile, split, sb0, sb1;
+  __device__ __forceinline__ TaskView(const TcParams<MAXE>& P, int t) {
+    int lo = 0, hi = P.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (P.e[mid].task_begin <= t) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const TcEntry& E = P.e[e];
+    const int u = t - E.task_begin;
+    tile = u / E.splits;
+    split = u - tile * E.splits;
+    sb0 = split * E.chunk;
+    sb1 = min(E.K >> 8, sb0 + E.chunk);
+  }
+};
+
+// Walk over the tasks of one dequant group: the CTA's local tasks j = g, g + NG, ... (task index
+// blockIdx.x + j * gridDim.x), each super-block of each task in order.
+template <int MAXE, int NG>
+struct GroupCursor {
+  int j, t, e, tile, split, sb, end;
+  __device__ __forceinline__ void load(const TcParams<MAXE>& P) {
+    t = (int)blockIdx.x + j * (int)gridDim.x;
+    if (t >= P.tasks_total) { t = -1; return; }
+    const TaskView<MAXE> T(P, t);
+    e = T.e; tile = T.tile; split = T.split; sb = T.sb0; end = T.sb1;
+  }
+  __device__ __forceinline__ void start(const TcParams<MAXE>& P, int g) { j = g; load(P); }
+  // after the current super-block: true if it was the last of its task
+  __device__ __forceinline__ bool advance(const TcParams<MAXE>& P) {
+    if (++sb < end) return false;
+    j += NG;
+    load(P);
+    return true;
+  }
+};
+
+// The CTA's super-block sequence su = 0, 1, ... runs in rounds: round i takes the i-th
+// super-block of every group that has one, in group order.  With n_g super-blocks in group g,
+// the i-th super-block of group g is
+//   su = sum_h min(n_h, i) + #{h < g : n_h > i}.
+template <int NG>
+__device__ __forceinline__ uint32_t su_of(const int (&n)[NG], int g, int i) {
+  uint32_t s = 0;
+#pragma unroll
+  for (int h = 0; h < NG; ++h) s += (uint32_t)min(n[h], i) + ((h < g && n[h] > i) ? 1u : 0u);
+  return s;
+}
+
 template <int MPAD, int MAXE>
-__global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
+__global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = TcSmem<MPAD>;
+  constexpr int NG = groups(MPAD);
+  constexpr int kProdWarp = NG * kGroupWarps;   // copies
+  constexpr int kMmaWarp = kProdWarp + 1;       // MMA issue; owns TMEM
   constexpr int kBB = bblock_bytes(MPAD);
-  constexpr int kBSlots = b_slots(MPAD);
-  constexpr int kAccSlots = acc_slots(MPAD);   // also the number of MMA warps that issue
-  constexpr int kAR0 = ar0(MPAD), kAR1 = ar1(MPAD);   // A ring depths of the two K halves
+  constexpr int kS = stages(MPAD);
+  constexpr int kSB = stage_bytes(MPAD);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t sW = smem_addr(smem + L::kW);
-  const uint32_t sB = smem_addr(smem + L::kB);
+  const uint32_t sW = smem_addr(smem + L::kW);   // stage k: weights at sW + k*kSB, activations 18432 further
   const uint32_t bars = smem_addr(smem + L::kBars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  int* group_sbs = reinterpret_cast<int*>(smem + L::kMisc + 16);   // n_g, g < NG
   auto bar = [&](int k) { return bars + 8u * k; };
+  auto gfull = [&](int g, uint32_t s) { return bar(kBarGFull + g * kMaxStages + (int)s); };
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < kWStages; ++k) {
-      mbar_init(bar(kBarWFull + k), 1);
-      mbar_init(bar(kBarWEmpty + k), kDqWarps + kEpiWarps);   // dequant reads quants, epilogue (d, dmin)
+    for (int g = 0; g < NG; ++g) {
+      for (int k = 0; k < kS; ++k) mbar_init(gfull(g, k), 1);
+      mbar_init(bar(kBarAFull + 2 * g), kGroupWarps);
+      mbar_init(bar(kBarAFull + 2 * g + 1), kGroupWarps);
+      mbar_init(bar(kBarGDone + g), 1);
     }
-    for (int k = 0; k < kBSlots; ++k) { mbar_init(bar(kBarBFull + k), 1); mbar_init(bar(kBarBEmpty + k), 1); }
-    for (int k = 0; k < kMaxASlots; ++k) { mbar_init(bar(kBarAFull + k), 4); mbar_init(bar(kBarAEmpty + k), 1); }
-    for (int k = 0; k < kAccSlots; ++k) { mbar_init(bar(kBarAccFull + k), 1); mbar_init(bar(kBarAccEmpty + k), kEpiWarps); }
+    // the consuming group's warps once they hold their bytes, and the MMA commit once the MMAs
+    // have read the activations
+    for (int k = 0; k < kS; ++k) mbar_init(bar(kBarWEmpty + k), kGroupWarps + 1);
+    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if (warp == 0 && lane < NG) {   // super-blocks of each group
+    GroupCursor<MAXE, NG> cur;
+    cur.start(P, lane);
+    int cnt = 0;
+    while (cur.t >= 0) { cnt += cur.end - cur.sb; cur.j += NG; cur.load(P); }
+    group_sbs[lane] = cnt;
   }
   if (warp == kMmaWarp) {
     tc::tmem_alloc(smem_addr(tmem_holder), kTmemCols);
@@ -301,166 +410,173 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
+  int n[NG];
+  int nmax = 0;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) { n[g] = group_sbs[g]; nmax = max(nmax, n[g]); }
 
-  auto wait = [&](int k, uint32_t parity) -> bool {
-    if (mbar_try(bar(k), parity)) return true;
+  auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+    if (mbar_try(b, parity)) return true;
     if (*abort_flag) return false;
-    if (mbar_wait(bar(k), parity, kWaitLimit)) return true;
+    if (mbar_wait(b, parity, kWaitLimit)) return true;
     atomicOr(&g_status, kErrWaitTimeout);
     *abort_flag = 1;
     return false;
   };
-  auto locate = [&](int t) {
-    int lo = 0, hi = P.count - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (P.e[mid].task_begin <= t) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  };
 
-  if (warp == kWProdWarp) {
-    // ------------------------------------------------------------------ weight tiles
-    // One TMA copy per super-block: rows row0 .. row0+127 (rows past N read as zeros), bytes
-    // 144 sb .. 144 sb + 143 of each row.  The ring runs kWStages - 1 super-blocks ahead.
-    if (lane == 0) {
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------------ copies
+    // Per super-block one TMA copy of the weights (rows row0 .. row0+127, rows past N read as
+    // zeros; bytes 144 sb .. 144 sb + 143 of each row) and one bulk copy of the prepared
+    // activation block, into the same stage, completing on that stage's barrier of the owning
+    // group.  The ring runs kS - 1 super-blocks ahead, in the CTA's super-block order.
+    if (elect_one()) {
       const uint64_t pol = policy_evict_first();
+      GroupCursor<MAXE, NG> cur[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) cur[g].start(P, g);
       uint32_t su = 0;
+      uint32_t gbits = 0;    // parity of the next phase of each (group, stage) full barrier
+      uint32_t owner = 0;    // group of the copies last issued into each stage, 2 bits a stage
       bool ok = true;
-      for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-        const int e = locate(t);
-        const TcEntry& E = P.e[e];
-        const int nb = E.K >> 8;
-        const int row0 = (t - E.task_begin) * kTileRows;
-        for (int sb = 0; sb < nb; ++sb, ++su) {
-          const uint32_t ws = su % kWStages;
-          if (!wait(kBarWEmpty + ws, ((su / kWStages) & 1u) ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(kBarWFull + ws), kWStageBytes);
-          tma_load_2d(sW + ws * kWStageBytes, &P.maps[e], sb * kBlockBytes, row0, bar(kBarWFull + ws), pol);
+      for (int i = 0; i < nmax && ok; ++i) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          if (ok && i < n[g]) ok = wait(bar(kBarWEmpty + su % kS), ((su / kS) & 1u) ^ 1u);
+          if (ok && i < n[g]) {
+            const uint32_t ws = su % kS;
+            gbits ^= 1u << (g * kMaxStages + ws);
+            owner = (owner & ~(3u << (2 * ws))) | ((uint32_t)g << (2 * ws));
+            const uint32_t st = sW + ws * kSB;
+            const int e = cur[g].e, sb = cur[g].sb;
+            mbar_arrive_expect_tx(gfull(g, ws), kWStageBytes + kBB);
+            tma_load_2d(st, &P.maps[e], sb * kBlockBytes, cur[g].tile * kTileRows, gfull(g, ws), pol);
+            bulk_g2s(st + kWStageBytes, P.e[e].B + (int64_t)sb * kBB, kBB, gfull(g, ws), 0ull);
+            cur[g].advance(P);
+            ++su;
+          }
         }
       }
-    }
-  } else if (warp == kBProdWarp) {
-    // ------------------------------------------------------------------ activation blocks
-    if (lane == 0) {
-      uint32_t su = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-        const TcEntry& E = P.e[locate(t)];
-        const int nb = E.K >> 8;
-        for (int sb = 0; sb < nb; ++sb, ++su) {
-          const uint32_t bs = su % kBSlots;
-          if (!wait(kBarBEmpty + bs, ((su / kBSlots) & 1u) ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(kBarBFull + bs), kBB);
-          bulk_g2s(sB + bs * kBB, E.B + (int64_t)sb * kBB, kBB, bar(kBarBFull + bs), 0ull);
-        }
+      // copies still in flight land before the CTA can end: wait for the last phase armed on
+      // each stage's full barrier (complete already, or once its bytes have arrived)
+      for (uint32_t k = (su > (uint32_t)kS ? su - kS : 0u); k < su; ++k) {
+        const uint32_t ws = k % kS, g = (owner >> (2 * ws)) & 3u;
+        mbar_wait(gfull((int)g, ws), ((gbits >> (g * kMaxStages + ws)) & 1u) ^ 1u, kWaitLimit);
       }
     }
-  } else if (warp >= kMmaWarp && warp < kMmaWarp + kMmaWarps) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
-    // Super-block su goes to warp su % kAccSlots (three issuers at Mpad 16, two at 32), which
-    // owns accumulator slot su % kAccSlots and A slot su % kAccSlots of each K half's ring.  The
-    // B ring is at least kAccSlots deep, so an issuer that saw super-block su - kAccSlots's block
-    // arrive waits on the right phase of su's slot.
-    const uint32_t mine = warp - kMmaWarp;
-    if (lane == 0 && mine < (uint32_t)kAccSlots) {
+    // Super-block su of group g: its A slot, handed over one K half at a time (each half full
+    // once the group's 4 warps have arrived, so the first 8 MMAs run while the group still
+    // dequantizes the second half), its activations in stage su % kS, its accumulator (read by
+    // the group before it wrote the A slot again).  One elected lane waits, issues and commits,
+    // in super-block order.
+    if (elect_one()) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
-      uint32_t su = 0;   // super-blocks of this CTA so far
-      uint32_t last = 0; // 1 + the last super-block this warp issued
+      uint32_t gbits = 0;   // parity of each (group, stage) full barrier
+      uint32_t su = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-        const int nb = P.e[locate(t)].K >> 8;
-        for (int sb = 0; sb < nb; ++sb, ++su) {
-          if (su % kAccSlots != mine) continue;
-          const uint32_t a0 = mine, a1 = kAR0 + mine;
-          const uint32_t bs = su % kBSlots, es = mine;
-          const uint32_t use = (su / kAccSlots) & 1u;   // phase parity of this warp's slots
-          if (!wait(kBarAccEmpty + es, use ^ 1u) ||
-              !wait(kBarBFull + bs, (su / kBSlots) & 1u) ||
-              !wait(kBarAFull + a0, use)) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint32_t d1 = tmem + acc1_col(MPAD, es);
-          const uint32_t d2 = tmem + acc2_col(MPAD, es);
-          const uint32_t bslot = sB + bs * kBB;
-          const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
-          tc::mma_f16_ts_x8(d1, tmem + a0_col(a0), bdesc, 16, idesc, 0);
-          tc::commit(bar(kBarAEmpty + a0));
-          if (!wait(kBarAFull + a1, use)) { ok = false; break; }
-          tc::fence_after_sync();
-          tc::mma_f16_ts_x8(d1, tmem + a1_col(MPAD, a1 - kAR0), bdesc + 8 * 16, 16, idesc, 1);
-          tc::mma_f16_ts(d2, tmem + a1_col(MPAD, a1 - kAR0) + 64, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
-          tc::commit(bar(kBarAccFull + es));
-          tc::commit(bar(kBarAEmpty + a1));
-          tc::commit(bar(kBarBEmpty + bs));
-          last = su + 1;
+      for (int i = 0; i < nmax && ok; ++i) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const uint32_t ws = su % kS;
+          const uint32_t bit = 1u << (g * kMaxStages + ws);
+          if (ok && i < n[g])
+            ok = wait(bar(kBarAFull + 2 * g), (uint32_t)i & 1u) && wait(gfull(g, ws), (gbits & bit) ? 1u : 0u);
+          if (ok && i < n[g]) {
+            gbits ^= bit;
+            tc::fence_after_sync();
+            const uint64_t bdesc = tc::smem_desc_kmajor(sW + ws * kSB + kWStageBytes, 128, 4096);   // + 16 per MMA: 256 bytes
+            tc::mma_f16_ts_x8(tmem + acc1_col(MPAD, g), tmem + a_col(g), bdesc, 16, idesc, 0);
+            ok = wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u);
+          }
+          if (ok && i < n[g]) {
+            tc::fence_after_sync();
+            const uint32_t abase = tmem + a_col(g);
+            const uint32_t d1 = tmem + acc1_col(MPAD, g);
+            const uint32_t d2 = tmem + acc2_col(MPAD, g);
+            const uint32_t bslot = sW + ws * kSB + kWStageBytes;
+            const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);
+            tc::mma_f16_ts_x8(d1, abase + 64, bdesc + 8 * 16, 16, idesc, 1);
+            tc::mma_f16_ts(d2, abase + 128, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
+            tc::commit(bar(kBarGDone + g));
+            tc::commit(bar(kBarWEmpty + ws));
+            ++su;
+          }
         }
       }
-      if (!ok && last > 0)   // let issued MMAs finish before TMEM is released
-        mbar_wait(bar(kBarAccFull + (last - 1) % kAccSlots), ((last - 1) / kAccSlots) & 1u, kWaitLimit);
+      // every MMA issued has finished before TMEM is released
+      tc::commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0u, kWaitLimit);
     }
-  } else if (warp < kDqWarps) {
-    // ------------------------------------------------------------------ dequant
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ dequant + epilogue
+    const int grp = warp >> 2;       // dequant group: the CTA's local tasks j % NG == grp
     const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
-    const int h = warp >> 2;         // K half of each super-block
     const int r = 32 * q + lane;     // row inside the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
     const __half2 k1024 = bits2h(0x64006400u);
     const __half2 kn1024 = __float2half2_rn(-1024.f);
     const __half2 k1o16 = __float2half2_rn(0.0625f);
     const __half2 kn64 = __float2half2_rn(-64.f);
-    uint32_t su = 0;
-    bool ok = true;
-    bool pending = false;      // a unit whose TMEM stores are issued but not yet published
-    uint32_t pending_as = 0;   // and its A slot
-    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-      const TcEntry& E = P.e[locate(t)];
-      const int nb = E.K >> 8;
-      for (int sb = 0; sb < nb && ok; ++sb, ++su) {
-        const uint32_t ws = su % kWStages;
-        if (!wait(kBarWFull + ws, (su / kWStages) & 1u)) { ok = false; break; }
-        // this half's A ring: slot and how many times it was used before
-        const uint32_t as = h ? kAR0 + su % kAR1 : su % kAR0;
-        const uint32_t use = h ? su / kAR1 : su / kAR0;
+    auto wait_w = [&](uint32_t k, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(k, parity)); };
 
-        // ---- this row's half super-block from shared memory; the stage is then released
-        const uint32_t rb = sW + ws * kWStageBytes + r * kBlockBytes;
-        const uint4 hd = lds128(rb);
+    float y[MPAD];   // the current chunk's sum, tokens 0 .. MPAD-1 of this thread's row
+#pragma unroll
+    for (int k = 0; k < MPAD; ++k) y[k] = 0.f;
+    float ytot[MPAD];   // the task's running sum of chunk sums
+#pragma unroll
+    for (int k = 0; k < MPAD; ++k) ytot[k] = 0.f;
+
+    const uint32_t aslot = tl + a_col(grp);         // this group's A slot (this warp's lanes)
+    const uint32_t acc1 = tl + acc1_col(MPAD, grp);  // and accumulators
+    const uint32_t acc2 = tl + acc2_col(MPAD, grp);
+    uint32_t sbits = 0;   // parity of this group's full barrier of each stage
+    GroupCursor<MAXE, NG> cur;
+    cur.start(P, grp);
+    for (int i = 0; cur.t >= 0; ++i) {
+      const uint32_t su = su_of<NG>(n, grp, i);
+      const uint32_t ws = su % kS;
+      if (!wait_w(gfull(grp, ws), (sbits >> ws) & 1u)) break;
+      sbits ^= 1u << ws;
+
+      // ---- this row's super-block (quants one K half at a time) and 2^s of the activation
+      // block from the stage; this warp's part of the stage is released once all are read
+      const uint32_t rb = sW + ws * kSB + r * kBlockBytes;
+      const uint4 hd = lds128(rb);
+      const float sigma = lds_f32(sW + ws * kSB + kWStageBytes + MPAD * 544);
+
+      // (the A slot is free: this group waited for its previous MMAs below)
+
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         uint4 qv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-
-        // ---- the previous unit's TMEM stores have had the loads above to land: publish it
-        if (pending) {
-          tc::wait_st();
-          tc::fence_before_sync();
+        if (h == 1) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
-          pending = false;
+          if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         }
-        if (!wait(kBarAEmpty + as, (use & 1u) ^ 1u)) { ok = false; break; }
-        tc::fence_after_sync();
-
-        // ---- the 12-bit (sc, m) groups of this half's sub-blocks 4h .. 4h+3
+        // the 12-bit (sc, m) groups of sub-blocks 4h .. 4h+3
         const uint64_t F = h ? ((uint64_t)hd.w << 32 | hd.z) : ((uint64_t)hd.z << 32 | hd.y);
         const int fbase = h ? 16 : 0;
         __half2 sc2[4], scm[4], sc16[4], sc64[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t g = (uint32_t)(F >> (fbase + 12 * jj)) & 0xFFFu;
-          const uint32_t scb = ((g & 63u) | 0x6400u) * 0x10001u;       // (1024+sc, 1024+sc)
+          const uint32_t gr = (uint32_t)(F >> (fbase + 12 * jj)) & 0xFFFu;
+          const uint32_t scb = ((gr & 63u) | 0x6400u) * 0x10001u;      // (1024+sc, 1024+sc)
           sc2[jj] = __hsub2(bits2h(scb), k1024);                       // (sc, sc) exact
           scm[jj] = __hmul2(sc2[jj], kn1024);                           // -1024 sc
           sc16[jj] = __hmul2(sc2[jj], k1o16);                           // sc / 16
           sc64[jj] = __hmul2(sc2[jj], kn64);                            // -64 sc
         }
-
-        // ---- A = sc*q as fp16 pairs, 16 columns per sub-block, into TMEM
-        const uint32_t aaddr = tl + (h ? a1_col(MPAD, as - kAR0) : a0_col(as));
+        // A = sc*q as fp16 pairs, 16 columns per sub-block
+        const uint32_t aaddr = aslot + 64u * h;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint32_t words[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+          const uint4 v = qv[k];
+          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
           uint32_t cols[16];
 #pragma unroll
           for (int ww = 0; ww < 4; ++ww) {
@@ -478,86 +594,113 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_tc_kernel(const __grid_consta
           }
           tc::st_x16(aaddr + 16 * k, cols);
         }
-        if (h == 1) {
-          // A_ext (odd unit): (m_0..m_7) at k = 0..7 and again at k = 8..15
-          const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 (bits 0..47)
-          const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 (bits 16..63)
-          uint32_t mm[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
-            mm[jj] = (uint32_t)((jj < 4 ? (G >> (12 * jj)) : (H >> (16 + 12 * (jj - 4)))) >> 6) & 63u;
-          uint32_t ext[8];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            ext[c] = ext[c + 4] =
-                h2bits(__hsub2(bits2h((mm[2 * c] | 0x6400u) | ((mm[2 * c + 1] | 0x6400u) << 16)), k1024));
-          tc::st_x8(aaddr + 64, ext);
+        if (h == 0) {   // the first K half goes to the MMA warp now
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp));
         }
-        // published (wait::st + arrive) after the next unit's loads, or below
-        pending = true;
-        pending_as = as;
       }
-      if (ok && pending) {   // last unit of the task
-        tc::wait_st();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarAFull + pending_as));
-        pending = false;
+      {
+        // A_ext: (m_0..m_7) at k = 0..7 and again at k = 8..15
+        const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 (bits 0..47)
+        const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 (bits 16..63)
+        uint32_t mm[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          mm[jj] = (uint32_t)((jj < 4 ? (G >> (12 * jj)) : (H >> (16 + 12 * (jj - 4)))) >> 6) & 63u;
+        uint32_t ext[8];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          ext[cc] = ext[cc + 4] =
+              h2bits(__hsub2(bits2h((mm[2 * cc] | 0x6400u) | ((mm[2 * cc + 1] | 0x6400u) << 16)), k1024));
+        tc::st_x8(aslot + 128u, ext);
       }
-    }
-  } else if (warp >= kEpiWarp0) {
-    // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int r = 32 * q + lane;
-    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    uint32_t ec = 0;   // super-blocks consumed
-    bool ok = true;
-    float y[MPAD];
-    for (int t = blockIdx.x; t < P.tasks_total && ok; t += gridDim.x) {
-      const TcEntry& E = P.e[locate(t)];
-      const int nb = E.K >> 8;
-      const int row0 = (t - E.task_begin) * kTileRows;
+      // ---- hand the second K half (and A_ext) to the MMA warp
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp + 1));
+
+      // ---- the accumulator of this super-block into y (tokens below M only)
+      if (!wait_w(bar(kBarGDone + grp), (uint32_t)i & 1u)) break;
+      tc::fence_after_sync();
+      const float2 dd = __half22float2(bits2h(hd.x));   // (D, Dm) of this row
+      const float sx = dd.x * sigma, sy = dd.y * sigma * 64.f;
 #pragma unroll
-      for (int c = 0; c < MPAD; ++c) y[c] = 0.f;
-      for (int sb = 0; sb < nb; ++sb) {
-        const uint32_t es = ec % kAccSlots, ws = ec % kWStages;
-        // 2^s of this super-block's activations (written by the preparation kernel)
-        const float sigma = __ldg(reinterpret_cast<const float*>(E.B + (int64_t)sb * kBB + MPAD * 544));
-        if (!wait(kBarWFull + ws, (ec / kWStages) & 1u)) { ok = false; break; }
-        const uint32_t dpair = *reinterpret_cast<const uint32_t*>(smem + L::kW + ws * kWStageBytes + r * kBlockBytes);
-        if (!wait(kBarAccFull + es, (ec / kAccSlots) & 1u)) { ok = false; break; }
-        tc::fence_after_sync();
-        const float2 dd = __half22float2(bits2h(dpair));
-        const float2 sc = make_float2(dd.x * sigma, dd.y * sigma * 64.f);
-        // read the accumulators 16 tokens at a time (keeps the register footprint small); the
-        // slots are handed back as soon as the last read has landed, before the arithmetic
-#pragma unroll
-        for (int c0 = 0; c0 < MPAD; c0 += 16) {
-          float a1[16], a2[16];
-          tc::ld_x16(tl + acc1_col(MPAD, es) + c0, a1);
-          tc::ld_x16(tl + acc2_col(MPAD, es) + c0, a2);
+      for (int c0 = 0; c0 < MPAD; c0 += 16) {
+        if (c0 < P.M) {
+          const bool two = c0 + 8 < P.M;
+          float a1[8], a2[8], b1[8], b2[8];
+          tc::ld_x8(acc1 + c0, a1);
+          tc::ld_x8(acc2 + c0, a2);
+          if (two) {
+            tc::ld_x8(acc1 + c0 + 8, b1);
+            tc::ld_x8(acc2 + c0 + 8, b2);
+          }
           tc::wait_ld();
-          if (c0 + 16 == MPAD) {
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(bar(kBarAccEmpty + es));
-              mbar_arrive(bar(kBarWEmpty + ws));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            y[c0 + k] = fmaf(sx, a1[k], y[c0 + k]);
+            y[c0 + k] = fmaf(-sy, a2[k], y[c0 + k]);
+          }
+          if (two) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              y[c0 + 8 + k] = fmaf(sx, b1[k], y[c0 + 8 + k]);
+              y[c0 + 8 + k] = fmaf(-sy, b2[k], y[c0 + 8 + k]);
             }
           }
+        }
+      }
+
+      // ---- end of a chunk: y (this chunk's sum) is added to the task's running sum, or, for a
+      // split task, stored as the chunk's partial.  End of a task: the running
+      // sum goes to Y; a split task counts itself in, and the last split of this (tile, lane
+      // quarter) slice adds every chunk partial of the tile in chunk order.
+      const int e = cur.e, tile = cur.tile, sb = cur.sb;
+      const TcEntry& E = P.e[e];
+      const int nb = E.K >> 8;
+      const bool task_end = cur.advance(P);
+      if ((sb + 1) % kChunkSb == 0 || sb + 1 == nb) {
+        if (E.splits == 1) {
+          const bool first = sb < kChunkSb;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            y[c0 + c] = fmaf(sc.x, a1[c], y[c0 + c]);
-            y[c0 + c] = fmaf(-sc.y, a2[c], y[c0 + c]);
+          for (int k = 0; k < MPAD; ++k)
+            if (k < P.M) ytot[k] = first ? y[k] : ytot[k] + y[k];
+        } else {
+          float* part = E.partial + ((size_t)tile * E.chunks + sb / kChunkSb) * (MPAD * kTileRows) + r;
+#pragma unroll
+          for (int k = 0; k < MPAD; ++k)
+            if (k < P.M) part[k * kTileRows] = y[k];
+        }
+#pragma unroll
+        for (int k = 0; k < MPAD; ++k) y[k] = 0.f;
+      }
+      if (task_end) {
+        const int row = tile * kTileRows + r;
+        if (E.splits == 1) {
+          if (row < E.N) {
+#pragma unroll
+            for (int k = 0; k < MPAD; ++k)
+              if (k < P.M) E.Y[(int64_t)k * E.N + row] = ytot[k];
+          }
+        } else {
+          // the warp's partial stores, then one release of them (the warp barrier orders the
+          // other lanes' stores before lane 0's fence) and the arrival count of this slice
+          __syncwarp();
+          unsigned old = 0;
+          if (lane == 0) {
+            __threadfence();
+            old = atomicAdd(&E.counters[tile * kGroupWarps + q], 1u);
+          }
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old == (unsigned)(E.splits - 1)) {
+            __threadfence();
+            reduce_chunks<MPAD>(E.partial + (size_t)tile * E.chunks * (MPAD * kTileRows) + r, E.chunks, P.M,
+                                row < E.N ? E.Y + row : nullptr, E.N);
           }
         }
-        ++ec;
-      }
-      if (!ok) break;
-      if (row0 + r < E.N) {
-#pragma unroll
-        for (int c = 0; c < MPAD; ++c)
-          if (c < P.M) E.Y[(int64_t)c * E.N + row0 + r] = y[c];
       }
     }
   }
@@ -662,10 +805,62 @@ cudaError_t set_smem_attr() {
   return err;
 }
 
+// K split of a product: the number of splits of every 128-row tile and the super-blocks per
+// split (a multiple of kChunkSb, so that the split does not change the summation order).  A
+// batched launch has work enough for every SM and does not split; a single product picks the
+// split that minimizes
+//   (tasks per SM, rounded up) x (super-blocks per task) + 0.5 x (split tasks per SM)
+//     + 0.25 x (chunks summed by the last split)
+// in units of one super-block of a tile: the busiest SM's work, the cost of publishing a split
+// task's partial sums, and the final reduction's chain of partial-sum loads.
+struct Split {
+  int splits;
+  int chunk;
+};
+
+int chunks_of(int64_t K) { return (int)((K / 256 + kChunkSb - 1) / kChunkSb); }
+
+Split split_for(int64_t N, int64_t K, int sms, bool batched) {
+  const int64_t tiles = (N + kTileRows - 1) / kTileRows;
+  const int nb = (int)(K / 256);
+  const int nch = chunks_of(K);
+  Split best{1, nb};
+  if (batched) return best;
+  double best_cost = 1e300;
+  for (int cps = nch; cps >= 1; --cps) {   // chunks per split
+    const int splits = (nch + cps - 1) / cps;
+    if (cps != nch && (nch + splits - 1) / splits != cps) continue;   // same splits, larger chunk seen
+    const double per_sm = std::ceil((double)(tiles * splits) / (double)std::max(1, sms));
+    const int chunk_sb = std::min(nb, cps * kChunkSb);
+    const double cost = per_sm * chunk_sb + (splits > 1 ? 0.5 * per_sm + 0.25 * nch : 0.0);
+    if (cost < best_cost - 1e-9) { best_cost = cost; best = Split{splits, splits == 1 ? nb : chunk_sb}; }
+  }
+  return best;
+}
+
+// Bytes of split workspace (partials, then counters) that a job needs.
+struct SplitSpace {
+  size_t partial_bytes = 0;
+  size_t counter_words = 0;
+};
+
+template <int MPAD>
+SplitSpace split_space(int64_t N, int64_t K, const Split& s) {
+  SplitSpace r;
+  if (s.splits > 1) {
+    const size_t tiles = (size_t)((N + kTileRows - 1) / kTileRows);
+    r.partial_bytes = tiles * (size_t)chunks_of(K) * MPAD * 128 * sizeof(float);
+    r.counter_words = tiles * kGroupWarps;
+  }
+  return r;
+}
+
 // The main kernel over jobs[0 .. count) (count <= MAXE), whose prepared activations start at
-// bsrc[k].  Parameters are built in a static block under the caller's lock.
+// bsrc[k], with K splits sp[k] and split workspace part[k] / ctr[k].  Parameters are built in a
+// static block under the caller's lock.
 template <int MPAD, int MAXE>
-cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, int count, int M, cudaStream_t stream) {
+cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split* sp, float* const* part,
+                        unsigned* const* ctr, int count, int M, cudaStream_t stream) {
   static TcParams<MAXE> par;
   par.count = count;
   par.M = M;
@@ -674,23 +869,26 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, int count, 
     cudaError_t err = weight_map(jobs[k].W, jobs[k].N, jobs[k].K, &par.maps[k]);
     if (err != cudaSuccess) return err;
     const int tiles = (int)((jobs[k].N + kTileRows - 1) / kTileRows);
-    par.e[k] = TcEntry{jobs[k].Y, bsrc[k], (int)jobs[k].N, (int)jobs[k].K, tiles, tasks};
-    tasks += tiles;
+    par.e[k] = TcEntry{jobs[k].Y, bsrc[k], part[k], ctr[k], (int)jobs[k].N, (int)jobs[k].K,
+                       tiles, sp[k].splits, sp[k].chunk, chunks_of(jobs[k].K), tasks};
+    tasks += tiles * sp[k].splits;
   }
   par.tasks_total = tasks;
   cudaError_t err = set_smem_attr<MPAD, MAXE>();
   if (err != cudaSuccess) return err;
   const int grid = std::min(tasks, num_sms());
-  q4k_tc_kernel<MPAD, MAXE><<<grid, kThreads, TcSmem<MPAD>::kTotal, stream>>>(par);
+  q4k_tc_kernel<MPAD, MAXE><<<grid, threads(MPAD), TcSmem<MPAD>::kTotal, stream>>>(par);
   return cudaGetLastError();
 }
 
 template <int MPAD>
 cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
-                        int M, cudaStream_t stream) {
+                        unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
   static PrepParams prep;   // large: built on the host, passed by value at launch
   prep.count = (int)xs.size();
   prep.M = M;
+  prep.zero = zero;
+  prep.zero_words = (int)zero_words;
   int blocks = 0;
   for (size_t u = 0; u < xs.size(); ++u) {
     prep.e[u] = PrepEntry{xs[u].first, outs[u], (int)xs[u].second, blocks};
@@ -699,6 +897,40 @@ cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& 
   prep.blocks_total = blocks;
   q4k_xprep_kernel<MPAD><<<blocks, 8 * MPAD, 0, stream>>>(prep);
   return cudaGetLastError();
+}
+
+// Shared by the workspace and the no-allocation paths: prepare the distinct activations into
+// `prep_base` (laid out by the caller), zero the split counters, and run the main kernel(s).
+template <int MPAD>
+cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
+                   const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
+                   const std::vector<int>& xidx, const std::vector<Split>& sp, uint8_t* split_base,
+                   size_t zero_words) {
+  std::vector<const uint8_t*> bsrc(count);
+  std::vector<float*> part(count, nullptr);
+  std::vector<unsigned*> ctr(count, nullptr);
+  size_t off = 0, words = 0;
+  for (int k = 0; k < count; ++k) {
+    bsrc[k] = outs[xidx[k]];
+    const SplitSpace s = split_space<MPAD>(jobs[k].N, jobs[k].K, sp[k]);
+    if (s.partial_bytes) { part[k] = reinterpret_cast<float*>(split_base + off); off += s.partial_bytes; }
+  }
+  unsigned* counters = reinterpret_cast<unsigned*>(split_base + off);
+  for (int k = 0; k < count; ++k) {
+    const SplitSpace s = split_space<MPAD>(jobs[k].N, jobs[k].K, sp[k]);
+    if (s.counter_words) { ctr[k] = counters + words; words += s.counter_words; }
+  }
+  static std::mutex mu;
+  std::lock_guard<std::mutex> g(mu);
+  cudaError_t err = launch_prep<MPAD>(xs, outs, counters, zero_words, M, stream);
+  if (err != cudaSuccess) return err;
+  if (count == 1) return launch_main<MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M, stream);
+  for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
+    err = launch_main<MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, sp.data() + k0, part.data() + k0,
+                                        ctr.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
 }
 
 template <int MPAD>
@@ -721,44 +953,42 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
     xoff[u] = bytes;
     bytes += (size_t)(xs[u].second / 256) * kBB;
   }
+  const int sms = num_sms();
+  std::vector<Split> sp(count);
+  size_t split_bytes = 0, zero_words = 0;
+  for (int k = 0; k < count; ++k) {
+    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, count > 1);
+    const SplitSpace s = split_space<MPAD>(jobs[k].N, jobs[k].K, sp[k]);
+    split_bytes += s.partial_bytes;
+    zero_words += s.counter_words;
+  }
+  bytes = (bytes + 255) & ~(size_t)255;
+  const size_t split_off = bytes;
+  bytes += split_bytes + zero_words * sizeof(unsigned);
   void* wsp = nullptr;
   cudaError_t err = Workspace::get(stream, bytes, &wsp);
   if (err != cudaSuccess) return err;
   uint8_t* ws = static_cast<uint8_t*>(wsp);
   std::vector<uint8_t*> outs(xs.size());
   for (size_t u = 0; u < xs.size(); ++u) outs[u] = ws + xoff[u];
-  std::vector<const uint8_t*> bsrc(count);
-  for (int k = 0; k < count; ++k) bsrc[k] = outs[xidx[k]];
-
-  static std::mutex mu;
-  std::lock_guard<std::mutex> g(mu);
-  err = launch_prep<MPAD>(xs, outs, M, stream);
-  if (err != cudaSuccess) return err;
-  if (count == 1) return launch_main<MPAD, 1>(jobs, bsrc.data(), 1, M, stream);
-  for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
-    err = launch_main<MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
-    if (err != cudaSuccess) return err;
-  }
-  return cudaSuccess;
+  return run_tc<MPAD>(jobs, count, M, stream, xs, outs, xidx, sp, ws + split_off, zero_words);
 }
 
 // ------------------------------------------------------------------------------------------
 // Allocation-free entry (qmm_run_noalloc): the same two kernels, with the prepared activations
 // in a fixed buffer that is part of this library's device image instead of the per-stream
-// workspace.  Every GPU that loads the library holds the buffer until the process exits.
+// workspace, and no K split (a split needs workspace for its partial sums).  Every GPU that
+// loads the library holds the buffer until the process exits.
 constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
 template <int MPAD>
 cudaError_t launch_tc_noalloc_t(const Job& job, int M, cudaStream_t stream, uint8_t* scratch) {
-  static std::mutex mu;
-  std::lock_guard<std::mutex> g(mu);
   const std::vector<std::pair<const uint16_t*, int64_t>> xs{{job.X, job.K}};
   const std::vector<uint8_t*> outs{scratch};
-  cudaError_t err = launch_prep<MPAD>(xs, outs, M, stream);
-  if (err != cudaSuccess) return err;
-  const uint8_t* bsrc = scratch;
-  return launch_main<MPAD, 1>(&job, &bsrc, 1, M, stream);
+  const std::vector<int> xidx{0};
+  const std::vector<Split> sp{Split{1, (int)(job.K / 256)}};
+  return run_tc<MPAD>(&job, 1, M, stream, xs, outs, xidx, sp, scratch, 0);
 }
 
 }  // namespace
