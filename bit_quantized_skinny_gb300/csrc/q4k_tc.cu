@@ -291,19 +291,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 // The last split of a (tile, lane quarter) slice: this thread's row of the tile, the sum of
 // every chunk partial in chunk order, tokens below M, to y (nullptr: the row is past N).  Out of
 // line: it runs once per split tile and would otherwise take registers from the hot loop.
-template <int MPAD>
+template <int MPAD, int MT>
 __device__ __noinline__ void reduce_chunks(const float* part, int chunks, int M, float* y, int N) {
-  float v[MPAD];
+  float v[MT];
 #pragma unroll
-  for (int k = 0; k < MPAD; ++k) v[k] = (k < M) ? __ldcg(&part[k * kTileRows]) : 0.f;
+  for (int k = 0; k < MT; ++k) v[k] = (k < M) ? __ldcg(&part[k * kTileRows]) : 0.f;
   for (int ch = 1; ch < chunks; ++ch) {
 #pragma unroll
-    for (int k = 0; k < MPAD; ++k)
+    for (int k = 0; k < MT; ++k)
       if (k < M) v[k] = v[k] + __ldcg(&part[((size_t)ch * MPAD + k) * kTileRows]);
   }
   if (y) {
 #pragma unroll
-    for (int k = 0; k < MPAD; ++k)
+    for (int k = 0; k < MT; ++k)
       if (k < M) y[(int64_t)k * N] = v[k];
   }
 }
@@ -361,8 +361,11 @@ __device__ __forceinline__ uint32_t su_of(const int (&n)[NG], int g, int i) {
   return s;
 }
 
-template <int MPAD, int MAXE>
+// MPAD: MMA width (token columns of B and of the accumulators, 16 or 32).  MT: the token columns
+// the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M hold zeros.
+template <int MPAD, int MT, int MAXE>
 __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
+  static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = TcSmem<MPAD>;
   constexpr int NG = groups(MPAD);
@@ -522,12 +525,12 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     const __half2 kn64 = __float2half2_rn(-64.f);
     auto wait_w = [&](uint32_t k, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(k, parity)); };
 
-    float y[MPAD];   // the current chunk's sum, tokens 0 .. MPAD-1 of this thread's row
+    float y[MT];   // the current chunk's sum, tokens 0 .. MT-1 of this thread's row
 #pragma unroll
-    for (int k = 0; k < MPAD; ++k) y[k] = 0.f;
-    float ytot[MPAD];   // the task's running sum of chunk sums
+    for (int k = 0; k < MT; ++k) y[k] = 0.f;
+    float ytot[MT];   // the task's running sum of chunk sums
 #pragma unroll
-    for (int k = 0; k < MPAD; ++k) ytot[k] = 0.f;
+    for (int k = 0; k < MT; ++k) ytot[k] = 0.f;
 
     const uint32_t aslot = tl + a_col(grp);         // this group's A slot (this warp's lanes)
     const uint32_t acc1 = tl + acc1_col(MPAD, grp);  // and accumulators
@@ -622,35 +625,27 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp + 1));
 
-      // ---- the accumulator of this super-block into y (tokens below M only)
+      // ---- the accumulator of this super-block into y (MT token columns)
       if (!wait_w(bar(kBarGDone + grp), (uint32_t)i & 1u)) break;
       tc::fence_after_sync();
       const float2 dd = __half22float2(bits2h(hd.x));   // (D, Dm) of this row
       const float sx = dd.x * sigma, sy = dd.y * sigma * 64.f;
+      constexpr int kW = MT == 16 ? 16 : 8;   // token columns per TMEM read round
 #pragma unroll
-      for (int c0 = 0; c0 < MPAD; c0 += 16) {
-        if (c0 < P.M) {
-          const bool two = c0 + 8 < P.M;
-          float a1[8], a2[8], b1[8], b2[8];
+      for (int c0 = 0; c0 < MT; c0 += kW) {
+        float a1[kW], a2[kW];
+        if constexpr (kW == 8) {
           tc::ld_x8(acc1 + c0, a1);
           tc::ld_x8(acc2 + c0, a2);
-          if (two) {
-            tc::ld_x8(acc1 + c0 + 8, b1);
-            tc::ld_x8(acc2 + c0 + 8, b2);
-          }
-          tc::wait_ld();
+        } else {
+          tc::ld_x16(acc1 + c0, a1);
+          tc::ld_x16(acc2 + c0, a2);
+        }
+        tc::wait_ld();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            y[c0 + k] = fmaf(sx, a1[k], y[c0 + k]);
-            y[c0 + k] = fmaf(-sy, a2[k], y[c0 + k]);
-          }
-          if (two) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              y[c0 + 8 + k] = fmaf(sx, b1[k], y[c0 + 8 + k]);
-              y[c0 + 8 + k] = fmaf(-sy, b2[k], y[c0 + 8 + k]);
-            }
-          }
+        for (int k = 0; k < kW; ++k) {
+          y[c0 + k] = fmaf(sx, a1[k], y[c0 + k]);
+          y[c0 + k] = fmaf(-sy, a2[k], y[c0 + k]);
         }
       }
 
@@ -664,25 +659,28 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
       const bool task_end = cur.advance(P);
       if ((sb + 1) % kChunkSb == 0 || sb + 1 == nb) {
         if (E.splits == 1) {
-          const bool first = sb < kChunkSb;
+          if (sb < kChunkSb) {
 #pragma unroll
-          for (int k = 0; k < MPAD; ++k)
-            if (k < P.M) ytot[k] = first ? y[k] : ytot[k] + y[k];
+            for (int k = 0; k < MT; ++k) ytot[k] = y[k];
+          } else {
+#pragma unroll
+            for (int k = 0; k < MT; ++k) ytot[k] = ytot[k] + y[k];
+          }
         } else {
           float* part = E.partial + ((size_t)tile * E.chunks + sb / kChunkSb) * (MPAD * kTileRows) + r;
 #pragma unroll
-          for (int k = 0; k < MPAD; ++k)
+          for (int k = 0; k < MT; ++k)
             if (k < P.M) part[k * kTileRows] = y[k];
         }
 #pragma unroll
-        for (int k = 0; k < MPAD; ++k) y[k] = 0.f;
+        for (int k = 0; k < MT; ++k) y[k] = 0.f;
       }
       if (task_end) {
         const int row = tile * kTileRows + r;
         if (E.splits == 1) {
           if (row < E.N) {
 #pragma unroll
-            for (int k = 0; k < MPAD; ++k)
+            for (int k = 0; k < MT; ++k)
               if (k < P.M) E.Y[(int64_t)k * E.N + row] = ytot[k];
           }
         } else {
@@ -697,7 +695,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           old = __shfl_sync(0xffffffffu, old, 0);
           if (old == (unsigned)(E.splits - 1)) {
             __threadfence();
-            reduce_chunks<MPAD>(E.partial + (size_t)tile * E.chunks * (MPAD * kTileRows) + r, E.chunks, P.M,
+            reduce_chunks<MPAD, MT>(E.partial + (size_t)tile * E.chunks * (MPAD * kTileRows) + r, E.chunks, P.M,
                                 row < E.N ? E.Y + row : nullptr, E.N);
           }
         }
@@ -793,14 +791,14 @@ cudaError_t weight_map(const void* W, int64_t N, int64_t K, CUtensorMap* out) {
   return cudaSuccess;
 }
 
-template <int MPAD, int MAXE>
+template <int MPAD, int MT, int MAXE>
 cudaError_t set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(q4k_tc_kernel<MPAD, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<MPAD>::kTotal);
+  err = cudaFuncSetAttribute(q4k_tc_kernel<MPAD, MT, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<MPAD>::kTotal);
   if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return err;
 }
@@ -874,10 +872,18 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
     tasks += tiles * sp[k].splits;
   }
   par.tasks_total = tasks;
-  cudaError_t err = set_smem_attr<MPAD, MAXE>();
-  if (err != cudaSuccess) return err;
   const int grid = std::min(tasks, num_sms());
-  q4k_tc_kernel<MPAD, MAXE><<<grid, threads(MPAD), TcSmem<MPAD>::kTotal, stream>>>(par);
+  if constexpr (MPAD == 16) {
+    if (M <= 8) {
+      cudaError_t err = set_smem_attr<MPAD, 8, MAXE>();
+      if (err != cudaSuccess) return err;
+      q4k_tc_kernel<MPAD, 8, MAXE><<<grid, threads(MPAD), TcSmem<MPAD>::kTotal, stream>>>(par);
+      return cudaGetLastError();
+    }
+  }
+  cudaError_t err = set_smem_attr<MPAD, MPAD, MAXE>();
+  if (err != cudaSuccess) return err;
+  q4k_tc_kernel<MPAD, MPAD, MAXE><<<grid, threads(MPAD), TcSmem<MPAD>::kTotal, stream>>>(par);
   return cudaGetLastError();
 }
 
