@@ -125,6 +125,11 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
   return v;
 }
 
+// Release/acquire fence at GPU scope: with an atomic between two of them it orders the writes
+// before the first one ahead of the reads after the second one (cheaper than a sequentially
+// consistent fence).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
 // (bulk copy) writes to the same shared memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

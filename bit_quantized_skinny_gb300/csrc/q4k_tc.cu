@@ -98,7 +98,7 @@ __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 1
 // of the same super-block: both arrive on one barrier, issued the same distance ahead.
 // (rounded up to 128 bytes: a TMA tile copy writes to a 128-byte aligned address)
 __host__ __device__ constexpr int stage_bytes(int mpad) { return (kWStageBytes + bblock_bytes(mpad) + 127) / 128 * 128; }
-__host__ __device__ constexpr int stages(int mpad) { return mpad <= 16 ? 8 : 6; }
+__host__ __device__ constexpr int stages(int mpad) { return mpad <= 16 ? 8 : 5; }
 constexpr int kMaxStages = 8;
 // TMEM columns.  Each group owns one A slot (one super-block: 64 columns of sc*q pairs per K
 // half and 8 columns of (m_j) pairs for the dmin MMA, 136 in all) and one accumulator (Mpad
@@ -133,7 +133,10 @@ enum : int {
 template <int MPAD>
 struct TcSmem {
   static constexpr int kW = 0;
-  static constexpr int kBars = kW + stages(MPAD) * stage_bytes(MPAD);
+  // Mpad 32: each group's running sum of chunk sums (32 tokens x 128 rows of fp32) lives here,
+  // not in registers
+  static constexpr int kYtot = kW + stages(MPAD) * stage_bytes(MPAD);
+  static constexpr int kBars = kYtot + (MPAD == 32 ? groups(MPAD) * 32 * kTileRows * 4 : 0);
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
@@ -528,9 +531,14 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     float y[MT];   // the current chunk's sum, tokens 0 .. MT-1 of this thread's row
 #pragma unroll
     for (int k = 0; k < MT; ++k) y[k] = 0.f;
-    float ytot[MT];   // the task's running sum of chunk sums
+    // the task's running sum of chunk sums: registers, or shared memory (token k at [k * 128])
+    // for 32 tokens
+    constexpr bool kYtotSmem = MT == 32;
+    float ytot_r[kYtotSmem ? 1 : MT];
+    float* ytot_s = reinterpret_cast<float*>(smem + L::kYtot) + (size_t)grp * MT * kTileRows + r;
 #pragma unroll
-    for (int k = 0; k < MT; ++k) ytot[k] = 0.f;
+    for (int k = 0; k < (kYtotSmem ? 1 : MT); ++k) ytot_r[k] = 0.f;
+    auto ytot = [&](int k) -> float& { if constexpr (kYtotSmem) return ytot_s[k * kTileRows]; else return ytot_r[k]; };
 
     const uint32_t aslot = tl + a_col(grp);         // this group's A slot (this warp's lanes)
     const uint32_t acc1 = tl + acc1_col(MPAD, grp);  // and accumulators
@@ -661,10 +669,10 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
         if (E.splits == 1) {
           if (sb < kChunkSb) {
 #pragma unroll
-            for (int k = 0; k < MT; ++k) ytot[k] = y[k];
+            for (int k = 0; k < MT; ++k) ytot(k) = y[k];
           } else {
 #pragma unroll
-            for (int k = 0; k < MT; ++k) ytot[k] = ytot[k] + y[k];
+            for (int k = 0; k < MT; ++k) ytot(k) = ytot(k) + y[k];
           }
         } else {
           float* part = E.partial + ((size_t)tile * E.chunks + sb / kChunkSb) * (MPAD * kTileRows) + r;
@@ -681,7 +689,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           if (row < E.N) {
 #pragma unroll
             for (int k = 0; k < MT; ++k)
-              if (k < P.M) E.Y[(int64_t)k * E.N + row] = ytot[k];
+              if (k < P.M) E.Y[(int64_t)k * E.N + row] = ytot(k);
           }
         } else {
           // the warp's partial stores, then one release of them (the warp barrier orders the
@@ -689,12 +697,12 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           __syncwarp();
           unsigned old = 0;
           if (lane == 0) {
-            __threadfence();
+            fence_acq_rel_gpu();   // release of the warp's partial sums
             old = atomicAdd(&E.counters[tile * kGroupWarps + q], 1u);
           }
           old = __shfl_sync(0xffffffffu, old, 0);
           if (old == (unsigned)(E.splits - 1)) {
-            __threadfence();
+            fence_acq_rel_gpu();   // acquire of the other splits' partial sums
             reduce_chunks<MPAD, MT>(E.partial + (size_t)tile * E.chunks * (MPAD * kTileRows) + r, E.chunks, P.M,
                                 row < E.N ? E.Y + row : nullptr, E.N);
           }
