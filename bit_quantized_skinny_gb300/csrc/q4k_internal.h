@@ -21,6 +21,8 @@ cudaError_t launch_fma(const Job* jobs, int count, int M, cudaStream_t stream);
 // Launch the tensor-core (tcgen05) kernel; cudaErrorNotSupported when it cannot run the shape.
 cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream);
 bool tc_supports(int M, int64_t N, int64_t K);
+// Modelled duration (us) of a tensor-core launch over these jobs (the dispatcher's cost model).
+double tc_estimate_us(const Job* jobs, int count, int M);
 
 // Tensor-core product with the prepared activations in the library's fixed device buffer
 // (no allocation).  noalloc_scratch_needed(M, K) must not exceed noalloc_scratch_bytes().

@@ -178,13 +178,14 @@ struct PrepEntry {
   int block_begin;   // first CTA index of this X
 };
 
+template <int NX>   // capacity: distinct activations of one preparation launch
 struct PrepParams {
   int count;
   int M;
   int blocks_total;
   int zero_words;      // split counters of the main launches of this call, zeroed here
   unsigned* zero;
-  PrepEntry e[kMaxPrep];
+  PrepEntry e[NX];
 };
 
 __device__ __forceinline__ uint32_t h2bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
@@ -193,8 +194,11 @@ __device__ __forceinline__ __half2 bits2h(uint32_t v) { return *reinterpret_cast
 // ------------------------------------------------------------------------------------------
 // Activation preparation.  Block = 8*MPAD threads; thread (i = t/8, j = t%8) handles token i,
 // sub-block j (32 activations) of one super-block.
-template <int MPAD>
-__global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_constant__ PrepParams P) {
+template <int MPAD, int NX>
+__global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_constant__ PrepParams<NX> P) {
+  // the product kernel that follows may start its prologue now (programmatic dependent launch);
+  // it waits for this grid's completion before it reads what this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ unsigned s_max[8];
   const int b = blockIdx.x;
   int e = 0;
@@ -436,6 +440,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     // zeros; bytes 144 sb .. 144 sb + 143 of each row) and one bulk copy of the prepared
     // activation block, into the same stage, completing on that stage's barrier of the owning
     // group.  The ring runs kS - 1 super-blocks ahead, in the CTA's super-block order.
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the prepared activations are written
     if (elect_one()) {
       const uint64_t pol = policy_evict_first();
       GroupCursor<MAXE, NG> cur[NG];
@@ -543,6 +548,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     const uint32_t aslot = tl + a_col(grp);         // this group's A slot (this warp's lanes)
     const uint32_t acc1 = tl + acc1_col(MPAD, grp);  // and accumulators
     const uint32_t acc2 = tl + acc2_col(MPAD, grp);
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // split counters zeroed, activations written
     uint32_t sbits = 0;   // parity of this group's full barrier of each stage
     GroupCursor<MAXE, NG> cur;
     cur.start(P, grp);
@@ -880,25 +886,34 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
     tasks += tiles * sp[k].splits;
   }
   par.tasks_total = tasks;
-  const int grid = std::min(tasks, num_sms());
+  // Programmatic dependent launch: the kernel may start while the preparation kernel before it
+  // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)std::min(tasks, num_sms()));
+  cfg.blockDim = dim3(threads(MPAD));
+  cfg.dynamicSmemBytes = TcSmem<MPAD>::kTotal;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if constexpr (MPAD == 16) {
     if (M <= 8) {
       cudaError_t err = set_smem_attr<MPAD, 8, MAXE>();
       if (err != cudaSuccess) return err;
-      q4k_tc_kernel<MPAD, 8, MAXE><<<grid, threads(MPAD), TcSmem<MPAD>::kTotal, stream>>>(par);
-      return cudaGetLastError();
+      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<MPAD, 8, MAXE>, par);
     }
   }
   cudaError_t err = set_smem_attr<MPAD, MPAD, MAXE>();
   if (err != cudaSuccess) return err;
-  q4k_tc_kernel<MPAD, MPAD, MAXE><<<grid, threads(MPAD), TcSmem<MPAD>::kTotal, stream>>>(par);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<MPAD, MPAD, MAXE>, par);
 }
 
-template <int MPAD>
-cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
-                        unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
-  static PrepParams prep;   // large: built on the host, passed by value at launch
+template <int MPAD, int NX>
+cudaError_t launch_prep_n(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
+                          unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
+  static PrepParams<NX> prep;   // built on the host, passed by value at launch
   prep.count = (int)xs.size();
   prep.M = M;
   prep.zero = zero;
@@ -909,8 +924,17 @@ cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& 
     blocks += (int)(xs[u].second / 256);
   }
   prep.blocks_total = blocks;
-  q4k_xprep_kernel<MPAD><<<blocks, 8 * MPAD, 0, stream>>>(prep);
+  q4k_xprep_kernel<MPAD, NX><<<blocks, 8 * MPAD, 0, stream>>>(prep);
   return cudaGetLastError();
+}
+
+// The parameter block is copied at every launch: size it to the distinct activations.
+template <int MPAD>
+cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
+                        unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
+  if (xs.size() <= 1) return launch_prep_n<MPAD, 1>(xs, outs, zero, zero_words, M, stream);
+  if (xs.size() <= 16) return launch_prep_n<MPAD, 16>(xs, outs, zero, zero_words, M, stream);
+  return launch_prep_n<MPAD, kMaxPrep>(xs, outs, zero, zero_words, M, stream);
 }
 
 // Shared by the workspace and the no-allocation paths: prepare the distinct activations into
@@ -949,7 +973,7 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
 
 template <int MPAD>
 cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) {
-  static_assert(sizeof(TcParams<kMaxEBatch>) < 32000 && sizeof(PrepParams) < 32000, "kernel parameters too large");
+  static_assert(sizeof(TcParams<kMaxEBatch>) < 32000 && sizeof(PrepParams<kMaxPrep>) < 32000, "kernel parameters too large");
   constexpr int kBB = bblock_bytes(MPAD);
   // distinct activations (an X pointer with its K) get one prepared block run each
   std::vector<std::pair<const uint16_t*, int64_t>> xs;
@@ -1014,6 +1038,26 @@ cudaError_t read_and_clear_tc_status(unsigned* out) {
   e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
   *out = v;
   return e;
+}
+
+// Time model of a tensor-core launch over jobs[0 .. count), fitted to GB300 timings: a fixed
+// ~14 us (two launches, pipeline fill), the busiest SM's super-blocks of a tile at 0.55 / 0.62 /
+// 0.78 us each for M <= 8 / 16 / 32, and ~2 us per split task on it (partial sums, fences).
+double tc_estimate_us(const Job* jobs, int count, int M) {
+  const int sms = std::max(1, num_sms());
+  double tasks = 0, sbs = 0, split_tasks = 0;
+  for (int k = 0; k < count; ++k) {
+    const Split sp = split_for(jobs[k].N, jobs[k].K, sms, count > 1);
+    const double tiles = std::ceil((double)jobs[k].N / kTileRows);
+    tasks += tiles * sp.splits;
+    sbs += tiles * (double)(jobs[k].K / 256);
+    if (sp.splits > 1) split_tasks += tiles * sp.splits;
+  }
+  // whole tasks per SM, each of the average size
+  const double per_sm_tasks = std::ceil(tasks / sms);
+  const double per_sm_sbs = per_sm_tasks * (sbs / std::max(1.0, tasks));
+  const double rate = M <= 8 ? 0.55 : (M <= 16 ? 0.62 : 0.78);
+  return 14.0 + per_sm_sbs * rate + 2.0 * std::ceil(split_tasks / sms);
 }
 
 bool tc_supports(int M, int64_t N, int64_t K) {

@@ -4,6 +4,7 @@
 // row count at which the skinny product moves from one kernel family to another, tuned per
 // GPU).  Here the families are the CUDA-core kernel (q4k_fma.cu) and the tensor-core kernel;
 // the switch point below is the measured one for GB300.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -43,44 +44,22 @@ qmm_status check_job(const void* W, int64_t N, int64_t K, const uint16_t* X, con
 // Switch point between the two kernel families, measured on GB300 (the pages tune the same
 // kind of switch point per GPU: "sixi-asi 0.9", section "The patch").  Each family gets a
 // small cost model fitted to its measured timings; the cheaper one runs.
-//   CUDA cores: ceil(M / rows-per-pass) passes, each streaming all weights at ~2.6 TB/s
-//               (1 activation row per pass) or ~1.8 TB/s (2 rows per pass).
-//   tensor cores: one CTA per SM walks 128-row tiles; a 256-weight super-block of a tile takes
-//               ~1.02 us whatever M is, so time = tiles-per-SM x super-blocks x 1.02 us.
+//   CUDA cores: ceil(M / rows-per-pass) passes, each streaming all weights at ~2.4 TB/s
+//               (1 activation row per pass) or ~1.8 TB/s (2 rows per pass) and taking at
+//               least ~2.5 us, plus ~5 us.
+//   tensor cores: q4k::tc_estimate_us (fixed cost, per-SM super-blocks, split tasks).
 struct CostModel {
   double fma_us = 0, tc_us = 0;
 };
 
-int device_sms() {
-  static int cache[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
-    cache[dev] = sms;
-  }
-  return cache[dev];
-}
-
 CostModel model(const q4k::Job* jobs, int count, int M) {
   CostModel c;
-  const int sms = device_sms();
-  double bytes = 0, tile_sbs = 0;
-  for (int k = 0; k < count; ++k) {
-    const double nb = (double)(jobs[k].K / 256);
-    bytes += (double)jobs[k].N * nb * 144.0;
-    tile_sbs += std::ceil((double)jobs[k].N / 128.0) * nb;
-  }
+  double bytes = 0;
+  for (int k = 0; k < count; ++k) bytes += (double)jobs[k].N * (double)(jobs[k].K / 256) * 144.0;
   const double passes = (M == 1) ? 1.0 : std::ceil(M / 2.0);
-  const double bw = (M == 1) ? 2.6e6 : 1.8e6;   // bytes per microsecond
-  c.fma_us = 4.0 + passes * bytes / bw;
-  double per_sm = tile_sbs / sms;
-  if (count == 1) {   // a single matrix: whole tiles per CTA
-    const double tiles = std::ceil((double)jobs[0].N / 128.0);
-    per_sm = std::ceil(tiles / sms) * (double)(jobs[0].K / 256);
-  }
-  c.tc_us = 6.0 + per_sm * 1.02;
+  const double bw = (M == 1) ? 2.4e6 : 1.8e6;   // bytes per microsecond
+  c.fma_us = 5.0 + passes * std::max(2.5, bytes / bw);
+  c.tc_us = q4k::tc_estimate_us(jobs, count, M);
   return c;
 }
 
