@@ -78,7 +78,8 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str, M: int):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    """DRAM bytes of one step (all its product launches) from a committed ncu summary, if taken on
+    the current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -89,7 +90,7 @@ def recorded_traffic(kernel: str, workload: str, M: int):
     ent = rec.get(key)
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent.get("dram_bytes_per_step")
 
 
 # ----------------------------------------------------------------------------- clocks ----
@@ -263,7 +264,9 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
 
     variant = qmm.select_variant_batched(entries, M)
     kernel = "q4k_tc_kernel" if variant == qmm.VARIANT_TC else "q4k_fma_kernel"
-    launches_per_step = 2 if variant == qmm.VARIANT_TC else 1   # activation prep + product
+    # tensor cores: one activation-prep launch and one product launch per 160 matrices (their
+    # tensor maps ride in the launch parameters); CUDA cores: one launch
+    launches_per_step = (1 + -(-len(entries) // 160)) if variant == qmm.VARIANT_TC else 1
     step = lambda: qmm.run_batched(entries, M)
     step()
     torch.cuda.synchronize()
@@ -337,10 +340,13 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": recorded_traffic(kernel, "pass64", M),
                      "kernel": kernel,
-                     "timed": "whole step on the launching stream (the product kernel plus the "
-                              "activation-prep kernel, <0.2% of the step by ncu)" if launches_per_step == 2
+                     "timed": "whole step on the launching stream (the product launches plus the "
+                              "activation-prep launch, 0.15% of the step by ncu)" if variant == qmm.VARIANT_TC
                               else "whole step on the launching stream (one kernel)",
-                     "algorithmic_bytes_per_launch": info["algo_bytes"]},
+                     "algorithmic_bytes_per_step": info["algo_bytes"],
+                     "unit_of_measure": "one step = one qmm_run_batched call over the 384 matrices: one "
+                                        "activation-prep launch and ceil(384/160) = 3 product launches; "
+                                        "achieved and traffic are per step"},
         "e2e": {"value": round(weight_gbps(wb * world, ms_e2e), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 5),

@@ -1041,8 +1041,8 @@ cudaError_t read_and_clear_tc_status(unsigned* out) {
 }
 
 // Time model of a tensor-core launch over jobs[0 .. count), fitted to GB300 timings: a fixed
-// ~14 us (two launches, pipeline fill), the busiest SM's super-blocks of a tile at 0.55 / 0.62 /
-// 0.78 us each for M <= 8 / 16 / 32, and ~2 us per split task on it (partial sums, fences).
+// ~10 us (two launches, pipeline fill), the busiest SM's super-blocks of a tile at 0.53 / 0.60 /
+// 0.79 us each for M <= 8 / 16 / 32, and ~1.5 us per split task on it (partial sums, fences).
 double tc_estimate_us(const Job* jobs, int count, int M) {
   const int sms = std::max(1, num_sms());
   double tasks = 0, sbs = 0, split_tasks = 0;
@@ -1056,8 +1056,8 @@ double tc_estimate_us(const Job* jobs, int count, int M) {
   // whole tasks per SM, each of the average size
   const double per_sm_tasks = std::ceil(tasks / sms);
   const double per_sm_sbs = per_sm_tasks * (sbs / std::max(1.0, tasks));
-  const double rate = M <= 8 ? 0.55 : (M <= 16 ? 0.62 : 0.78);
-  return 14.0 + per_sm_sbs * rate + 2.0 * std::ceil(split_tasks / sms);
+  const double rate = M <= 8 ? 0.53 : (M <= 16 ? 0.60 : 0.79);
+  return 10.0 + per_sm_sbs * rate + 1.5 * std::ceil(split_tasks / sms);
 }
 
 bool tc_supports(int M, int64_t N, int64_t K) {
