@@ -552,17 +552,32 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     uint32_t sbits = 0;   // parity of this group's full barrier of each stage
     GroupCursor<MAXE, NG> cur;
     cur.start(P, grp);
+    // With two groups (Mpad 32) the stage, header and 2^s of a group's next super-block are
+    // fetched while the MMAs of the current one run (measured faster there; with three groups,
+    // fetching them at the start of the iteration measured faster).
+    constexpr bool kFetchEarly = NG == 2;
+    uint32_t ws_n = 0;
+    uint4 hd_n = make_uint4(0, 0, 0, 0);
+    float sigma_n = 0.f;
     for (int i = 0; cur.t >= 0; ++i) {
-      const uint32_t su = su_of<NG>(n, grp, i);
-      const uint32_t ws = su % kS;
-      if (!wait_w(gfull(grp, ws), (sbits >> ws) & 1u)) break;
-      sbits ^= 1u << ws;
-
-      // ---- this row's super-block (quants one K half at a time) and 2^s of the activation
-      // block from the stage; this warp's part of the stage is released once all are read
+      uint32_t ws;
+      uint4 hd;
+      float sigma;
+      if (kFetchEarly && i > 0) {
+        ws = ws_n;
+        hd = hd_n;
+        sigma = sigma_n;
+      } else {
+        ws = su_of<NG>(n, grp, i) % kS;
+        if (!wait_w(gfull(grp, ws), (sbits >> ws) & 1u)) break;
+        sbits ^= 1u << ws;
+        // this row's header and 2^s of the activation block from the stage
+        hd = lds128(sW + ws * kSB + r * kBlockBytes);
+        sigma = lds_f32(sW + ws * kSB + kWStageBytes + MPAD * 544);
+      }
+      // ---- the rest of this row's super-block (quants one K half at a time) from the stage;
+      // this warp's part of the stage is released once all are read
       const uint32_t rb = sW + ws * kSB + r * kBlockBytes;
-      const uint4 hd = lds128(rb);
-      const float sigma = lds_f32(sW + ws * kSB + kWStageBytes + MPAD * 544);
 
       // (the A slot is free: this group waited for its previous MMAs below)
 
@@ -638,6 +653,15 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp + 1));
+      if constexpr (kFetchEarly) {
+        if (i + 1 < n[grp]) {
+          ws_n = su_of<NG>(n, grp, i + 1) % kS;
+          if (!wait_w(gfull(grp, ws_n), (sbits >> ws_n) & 1u)) break;
+          sbits ^= 1u << ws_n;
+          hd_n = lds128(sW + ws_n * kSB + r * kBlockBytes);
+          sigma_n = lds_f32(sW + ws_n * kSB + kWStageBytes + MPAD * 544);
+        }
+      }
 
       // ---- the accumulator of this super-block into y (MT token columns)
       if (!wait_w(bar(kBarGDone + grp), (uint32_t)i & 1u)) break;
