@@ -10,6 +10,7 @@ larger than L2 (129 MB), so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--M 8] [--impl ours|reference]
   python bench.py --single gate_up|down|q|k|lm_head|all [--Ms 1,2,...] [--variant fma|tc|auto|both]
+  python bench.py --ffn [--Ms 1,2,...]     (one feed-forward block per call: gate/up, gate, down)
 
 `--single` times one matrix product per launch instead (weights cycled over copies totalling
 more than 4x the L2 size), for the switch-point sweep between the two kernel families and as
@@ -422,6 +423,41 @@ def run_single(args):
                       "l2": f"weights cycled over copies >= 4x L2 ({l2 >> 20} MB)", "shapes": results}), flush=True)
 
 
+def run_ffn(args):
+    """One feed-forward block per call (qmm_run_ffn: gate/up product, SiLU-gated bf16 step, down
+    product) at the configurations' FFN shapes, weights cycled over copies totalling more than
+    4x L2.  GB/s counts both matrices' packed weights.  Prints one JSON line."""
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, inputs, qmm, workloads
+
+    build_lib.build()
+    qmm.load()
+    torch.cuda.set_device(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    F, K = 17408, 5120
+    Wgu, _ = workloads.packed_weights(2 * F, K, inputs.seed_for(2, 0), device="cuda")
+    Wdn, _ = workloads.packed_weights(K, F, inputs.seed_for(2, 1), device="cuda")
+    wbytes = Wgu.numel() + Wdn.numel()
+    copies = max(1, -(-4 * l2 // wbytes))
+    pairs = [(Wgu, Wdn)] + [(Wgu.clone(), Wdn.clone()) for _ in range(copies - 1)]
+    stream = torch.cuda.current_stream()
+    res = {}
+    for M in args.Ms:
+        X, _ = workloads.activations(M, K, inputs.seed_for(2, 50 + M), device="cuda")
+        Y = torch.empty((M, K), dtype=torch.float32, device="cuda")
+        ws = torch.empty(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
+        fn = lambda: [qmm.run_ffn(g, d, F, K, X, Y, ws, M=M) for g, d in pairs]
+        ms = time_steps(fn, max(2, args.steps // 5), 3, stream, lambda: None) / len(pairs)
+        res[str(M)] = {"us": round(ms * 1e3, 2), "gbps": round(weight_gbps(wbytes, ms), 1),
+                       "variants": [qmm.VARIANT_NAMES[qmm.select_variant(M, 2 * F, K)],
+                                    qmm.VARIANT_NAMES[qmm.select_variant(M, K, F)]]}
+        if qmm.device_status() != 0:
+            raise RuntimeError("kernel reported a device-side error")
+    print(json.dumps({"metric": "weight-read GB/s of one feed-forward block (gate/up -> SiLU gate -> down)",
+                      "unit": UNIT, "F": F, "K": K, "weight_bytes": wbytes, "copies": copies,
+                      "l2": f"weights cycled over copies >= 4x L2 ({l2 >> 20} MB)", "per_M": res}), flush=True)
+
+
 def run_reference(args, rank: int):
     """The oracle (plain fp64 C, host cores) on a bounded sample of the same workload."""
     if rank != 0:
@@ -490,6 +526,7 @@ def main(argv=None):
     ap.add_argument("--single", choices=list(SINGLE_SHAPES) + ["all"], default=None)
     ap.add_argument("--Ms", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 3, 4, 7, 8, 9, 12, 16])
     ap.add_argument("--variant", choices=["fma", "tc", "auto", "both"], default="both")
+    ap.add_argument("--ffn", action="store_true", help="time one feed-forward block per call instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -503,6 +540,10 @@ def main(argv=None):
     if args.single:
         if rank == 0:
             run_single(args)
+        return
+    if args.ffn:
+        if rank == 0:
+            run_ffn(args)
         return
     dist_ok = False
     if world > 1:

@@ -30,6 +30,10 @@ cudaError_t launch_tc_noalloc(const Job& job, int M, cudaStream_t stream);
 size_t noalloc_scratch_bytes();
 size_t noalloc_scratch_needed(int M, int64_t K);
 
+// The feed-forward step between the gate/up product and the down product: H[M x F] bf16 from
+// G[M x 2F] fp32 (gate columns 0..F-1, up columns F..2F-1), H = bf16(silu(gate) * up).
+cudaError_t launch_swiglu(const float* G, int64_t F, int M, uint16_t* H, cudaStream_t stream);
+
 // Device dequantization test hook.
 cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 

@@ -148,6 +148,34 @@ qmm_status qmm_run_noalloc(const void* Wq_dev, int64_t N, int64_t K, const uint1
   return e == cudaSuccess ? QMM_OK : cuda_fail(e);
 }
 
+size_t qmm_ffn_workspace_bytes(int M, int64_t F) {
+  if (M < 1 || M > QMM_MAX_M || check_shape(1, F) != QMM_OK) return 0;
+  const size_t g = ((size_t)M * 2 * (size_t)F * sizeof(float) + 15) & ~(size_t)15;
+  return g + (size_t)M * (size_t)F * sizeof(uint16_t);
+}
+
+qmm_status qmm_run_ffn(const void* Wgu_dev, const void* Wdown_dev, int64_t F, int64_t K, const uint16_t* X_dev,
+                       float* Y_dev, int M, void* workspace_dev, size_t workspace_bytes, cudaStream_t stream) {
+  if (!workspace_dev) return QMM_ERR_NULL;
+  qmm_status s = check_job(Wgu_dev, 2 * F, K, X_dev, Y_dev);
+  if (s != QMM_OK) return s;
+  s = check_job(Wdown_dev, K, F, X_dev, Y_dev);   // the down product: K outputs over F inputs
+  if (s != QMM_OK) return s;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  if (!aligned(workspace_dev, 16)) return QMM_ERR_ALIGN;
+  if (workspace_bytes < qmm_ffn_workspace_bytes(M, F)) return QMM_ERR_BUFSIZE;
+  float* G = static_cast<float*>(workspace_dev);
+  uint16_t* H = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace_dev) +
+                                            (((size_t)M * 2 * (size_t)F * sizeof(float) + 15) & ~(size_t)15));
+  const q4k::Job gate_up{Wgu_dev, X_dev, G, 2 * F, K};
+  s = run_jobs(&gate_up, 1, M, QMM_VARIANT_AUTO, stream);
+  if (s != QMM_OK) return s;
+  cudaError_t e = q4k::launch_swiglu(G, F, M, H, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const q4k::Job down{Wdown_dev, H, Y_dev, K, F};
+  return run_jobs(&down, 1, M, QMM_VARIANT_AUTO, stream);
+}
+
 qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev, cudaStream_t stream) {
   if (!Wq_dev || !out_dev) return QMM_ERR_NULL;
   qmm_status s = check_shape(N, K);

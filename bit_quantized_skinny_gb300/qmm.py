@@ -29,7 +29,8 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANG
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
-           "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched"]
+           "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
+           "qmm_ffn_workspace_bytes", "qmm_run_ffn"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -79,6 +80,10 @@ def load(path: str | None = None):
     lib.qmm_select_variant.restype = i32
     lib.qmm_select_variant_batched.argtypes = [ctypes.POINTER(_Entry), i32, i32]
     lib.qmm_select_variant_batched.restype = i32
+    lib.qmm_ffn_workspace_bytes.argtypes = [i32, i64]
+    lib.qmm_ffn_workspace_bytes.restype = ctypes.c_size_t
+    lib.qmm_run_ffn.argtypes = [vp, vp, i64, i64, vp, vp, i32, vp, ctypes.c_size_t, vp]
+    lib.qmm_run_ffn.restype = i32
     lib.qmm_device_status.argtypes = [ctypes.POINTER(u32)]
     lib.qmm_device_status.restype = i32
     lib.qmm_strerror.argtypes = [i32]
@@ -159,6 +164,22 @@ def run_batched(entries, M: int, stream=None):
     """One launch over independent products sharing M.  `entries` from make_entries()."""
     st = load().qmm_run_batched(entries, len(entries), M, _stream_handle(stream))
     _check(st, "qmm_run_batched")
+
+
+def ffn_workspace_bytes(M: int, F: int) -> int:
+    return load().qmm_ffn_workspace_bytes(M, F)
+
+
+def run_ffn(Wgu, Wdown, F: int, K: int, X, Y, workspace, M: int | None = None, stream=None):
+    """One feed-forward block: Y = (silu(X Wg^T) * (X Wu^T) as bf16) Wdown^T, all on the GPU.
+    `workspace`: a device tensor of >= ffn_workspace_bytes(M, F) bytes (holds G and H)."""
+    if M is None:
+        M = X.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load().qmm_run_ffn(ctypes.c_void_p(Wgu.data_ptr()), ctypes.c_void_p(Wdown.data_ptr()), F, K,
+                            ctypes.c_void_p(X.data_ptr()), ctypes.c_void_p(Y.data_ptr()), M,
+                            ctypes.c_void_p(workspace.data_ptr()), nbytes, _stream_handle(stream))
+    _check(st, "qmm_run_ffn")
 
 
 def dequant(Wq, N: int, K: int, out, stream=None):

@@ -186,6 +186,28 @@ int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M);
 qmm_status qmm_run_noalloc(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
                            float* Y_dev, int M, cudaStream_t stream);
 
+/* One feed-forward block of the verify pass: the two matrices the configurations give per layer
+ * ("Single FFN layer decode": the fused gate/up matrix and the down matrix; the pages time the
+ * fused gate/up product as "gate+up", FlashRT issue #153, the tile-bench tables) run as one
+ * dependent chain on `stream`:
+ *     G[M x 2F] = X[M x K] * dequant(Wgu)^T          (fp32; columns 0..F-1 gate, F..2F-1 up)
+ *     H[M x F]  = bf16( silu(G[:, f]) * G[:, F + f] ), silu(g) = g / (1 + e^-g), in fp32,
+ *                 rounded once to bf16 (round to nearest even)
+ *     Y[M x K]  = H * dequant(Wdown)^T               (fp32)
+ * (the pages do not print the gating function between the two products; SiLU-gated is the
+ * plainest reading for the model family they run).
+ *   Wgu_dev: packed (2F) x K weights, gate rows 0..F-1 then up rows F..2F-1.
+ *   Wdown_dev: packed K x F weights.  F and K are multiples of 256.
+ *   X_dev: M x K bf16.  Y_dev: M x K fp32 (overwritten).
+ *   workspace_dev: caller-owned device memory of at least qmm_ffn_workspace_bytes(M, F) bytes,
+ *     16-byte aligned; it holds G and H (the library allocates nothing for the chain itself;
+ *     the two products behave as qmm_run).  Both products are checked as in qmm_run; then
+ *     QMM_ERR_ALIGN (workspace), QMM_ERR_BUFSIZE (workspace too small), QMM_ERR_NULL.
+ * Each product picks its kernel variant as qmm_run does. */
+size_t qmm_ffn_workspace_bytes(int M, int64_t F);
+qmm_status qmm_run_ffn(const void* Wgu_dev, const void* Wdown_dev, int64_t F, int64_t K, const uint16_t* X_dev,
+                       float* Y_dev, int M, void* workspace_dev, size_t workspace_bytes, cudaStream_t stream);
+
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the
  * last read.  Bit 0: a kernel stopped waiting for its own weight copies after a bounded number

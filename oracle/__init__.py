@@ -11,6 +11,11 @@ Functions (all on host numpy arrays):
   dequant(Wq, N, K)         -> fp32 weights, the single rounding of d*sc*q - dmin*m
   matmul(Wq, N, K, X, rows) -> (Y, S) in fp64: Y = sum_k w*x, S = sum_k |w*x|
   half_value, half_from_float, bf16_value: the number formats, from their definitions
+  bf16_round(v)             -> bf16 bits of fp64 values, round to nearest even (definition)
+  swiglu(G, F)              -> silu(G[:, :F]) * G[:, F:] in fp64, the step between the gate/up
+                               and down products of one feed-forward block (gate+up products
+                               are what FlashRT issue #153 times; the SiLU gating between them is
+                               the plainest reading: the pages do not print it)
 """
 from __future__ import annotations
 
@@ -138,3 +143,28 @@ def matmul(Wq: np.ndarray, N: int, K: int, X_bits: np.ndarray, rows=None, thread
 
 def max_threads() -> int:
     return _load().oracle_max_threads()
+
+
+def bf16_round(v) -> np.ndarray:
+    """bf16 bit patterns (uint16) of fp64 values, rounded to nearest even: 8 significant bits,
+    exponent range of fp32 (normal down to 2^-126, subnormal steps of 2^-133), overflow to
+    infinity, signs kept (also on zero)."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)                                     # v = m * 2^e, 0.5 <= |m| < 1
+    e = np.where(v == 0, -1000, e)
+    normal = e - 1 >= -126
+    r = np.where(normal, np.ldexp(np.rint(m * 256.0), e - 8),       # 8 significant bits
+                 np.ldexp(np.rint(np.ldexp(v, 133)), -133))          # subnormal grid 2^-133
+    r = np.where(np.abs(r) > 3.3895313892515355e38, np.copysign(np.inf, v), r)   # past max bf16
+    r = np.where(v == 0, v, r)
+    bits32 = r.astype(np.float32).view(np.uint32)          # r has <= 8 significant bits: exact
+    return (bits32 >> 16).astype(np.uint16)
+
+
+def swiglu(G: np.ndarray, F: int) -> np.ndarray:
+    """silu(G[:, f]) * G[:, F + f] for f < F, in fp64, silu(g) = g / (1 + e^-g)."""
+    G = np.asarray(G, dtype=np.float64)
+    assert G.shape[1] == 2 * F
+    g, u = G[:, :F], G[:, F:]
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u

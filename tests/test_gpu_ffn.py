@@ -1,0 +1,85 @@
+"""GPU parity of the feed-forward chain (qmm_run_ffn): gate/up product -> SiLU-gated bf16
+activations -> down product, through the C ABI, against the oracle step by step.
+
+The chain is checked where each result is defined:
+  G (fp32, the gate/up product)  within 1e-4 * sum|w x| of the oracle, per element;
+  H (bf16)                       within one bf16 step of the oracle's fp64 SwiGLU of the GPU's G
+                                 (the GPU rounds an fp32 value, the oracle an fp64 one);
+  Y (fp32, the down product)     within 1e-4 * sum|w x| of the oracle fed the GPU's H.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_quantized_skinny_gb300 import build_lib, inputs
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    build_lib.build()
+    from bit_quantized_skinny_gb300 import qmm as q
+    q.load()
+    return q
+
+
+def _dev_bytes(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _dev_x(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16).copy()).cuda().view(torch.bfloat16)
+
+
+def _within(Y, Yref, S, what):
+    err = np.abs(Y.astype(np.float64) - Yref)
+    bad = err > TOL * S
+    assert not bad.any(), f"{what}: {bad.sum()} elements out of bound, max err {err.max()}"
+    assert np.all(np.isfinite(Y))
+
+
+def _bf16_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("F,K,Ms", [(512, 256, [1, 3, 8]), (768, 512, [16, 32]), (1024, 1024, [2, 9])])
+def test_ffn_chain_step_by_step(qmm, oracle_lib, F, K, Ms):
+    Wgu = oracle_lib.pack(inputs.weights_f32(2 * F, K, 700 + F))
+    Wdn = oracle_lib.pack(inputs.weights_f32(K, F, 800 + F))
+    Wgu_d, Wdn_d = _dev_bytes(Wgu), _dev_bytes(Wdn)
+    for M in Ms:
+        X = inputs.activations_bf16_bits(M, K, 900 + M)
+        Y = torch.full((M, K), 7.0, dtype=torch.float32, device="cuda")
+        ws = torch.zeros(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
+        qmm.run_ffn(Wgu_d, Wdn_d, F, K, _dev_x(X), Y, ws, M=M)
+        torch.cuda.synchronize()
+        assert qmm.device_status() == 0
+        wsh = ws.cpu().numpy()
+        g_bytes = (M * 2 * F * 4 + 15) // 16 * 16
+        G = wsh[:M * 2 * F * 4].view(np.float32).reshape(M, 2 * F)
+        H = wsh[g_bytes:g_bytes + M * F * 2].view(np.uint16).reshape(M, F)
+        Gref, SG = oracle_lib.matmul(Wgu, 2 * F, K, X)
+        _within(G, Gref, SG, f"gate/up M={M}")
+        href = oracle_lib.swiglu(G.astype(np.float64), F)
+        hg = _bf16_to_f64(H)
+        step = np.ldexp(1.0, np.frexp(np.abs(href))[1] - 8)       # one bf16 step at |href|
+        assert np.all(np.abs(hg - href) <= step), f"H off by more than one bf16 step at M={M}"
+        assert np.mean(H == oracle_lib.bf16_round(href)) > 0.99   # nearly all round identically
+        Yref, SY = oracle_lib.matmul(Wdn, K, F, H)
+        _within(Y.cpu().numpy(), Yref, SY, f"down M={M}")
+
+
+def test_ffn_argument_errors(qmm):
+    F, K, M = 256, 256, 2
+    W = torch.zeros(2 * F * (K // 256) * 144, dtype=torch.uint8, device="cuda")
+    X = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros((M, K), device="cuda")
+    small = torch.zeros(qmm.ffn_workspace_bytes(M, F) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.run_ffn(W, W, F, K, X, Y, small, M=M)
+    assert ei.value.status == 5   # QMM_ERR_BUFSIZE
+    assert qmm.ffn_workspace_bytes(M, 100) == 0   # F not a multiple of 256

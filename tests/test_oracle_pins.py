@@ -359,3 +359,38 @@ def test_pages_bandwidth_unit():
             assert abs(gbps - printed) <= 0.1, (name, gbps, printed)
         else:
             assert abs(100 * gbps / 273 - printed) <= 0.06, (name, gbps, printed)
+
+
+# ------------------------------------------------------------------ feed-forward step --------
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    """The oracle's bf16 rounding (from the format's definition) equals torch's fp32 -> bf16
+    conversion (round to nearest even) on random, tie and edge values."""
+    import torch
+    rng = np.random.default_rng(5)
+    f = np.concatenate([rng.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+                        (rng.standard_normal(2000) * 1e-38).astype(np.float32),   # subnormal range
+                        np.array([0.0, -0.0, 1.0, -1.0, 3.3895314e38, 1e-45, 65504.0], np.float32)])
+    # exact ties: values with 9 significant bits whose last bit is 1
+    ties = (np.arange(1, 512, 2, dtype=np.float32) + np.float32(256.0)) * np.float32(2.0 ** -8)
+    f = np.concatenate([f, ties, -ties])
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_mod().bf16_round(f.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_swiglu_matches_torch_silu_in_fp64():
+    import torch
+    rng = np.random.default_rng(6)
+    F = 64
+    G = rng.standard_normal((3, 2 * F)) * 4.0
+    G[0, :4] = [0.0, -40.0, 40.0, -800.0]
+    ref = (torch.nn.functional.silu(torch.from_numpy(G[:, :F])) * torch.from_numpy(G[:, F:])).numpy()
+    got = oracle_mod().swiglu(G, F)
+    assert np.allclose(got, ref, rtol=1e-15, atol=0.0)
+    assert got[0, 0] == 0.0 and abs(got[0, 3]) < 1e-300   # silu(0) = 0, silu(-800) underflows to 0
+
+
+def oracle_mod():
+    import oracle
+    return oracle
