@@ -11,6 +11,7 @@ larger than L2 (129 MB), so no flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--M 8] [--impl ours|reference]
   python bench.py --single gate_up|down|q|k|lm_head|all [--Ms 1,2,...] [--variant fma|tc|auto|both]
   python bench.py --ffn [--Ms 1,2,...]     (one feed-forward block per call: gate/up, gate, down)
+  python bench.py --indexed [--Ms 1,2,...] (indexed-expert product over 16 experts)
 
 `--single` times one matrix product per launch instead (weights cycled over copies totalling
 more than 4x the L2 size), for the switch-point sweep between the two kernel families and as
@@ -458,6 +459,44 @@ def run_ffn(args):
                       "l2": f"weights cycled over copies >= 4x L2 ({l2 >> 20} MB)", "per_M": res}), flush=True)
 
 
+def run_indexed(args):
+    """The indexed-expert product (qmm_run_indexed) over 16 synthetic experts of 4096 x 5120
+    (seeded, the same weight distribution as the other workloads), M rows spread over the experts
+    round robin (M >= 16: every expert in use).  GB/s counts the packed weights of the experts in
+    use (each read once per call); expert sets cycled over copies totalling more than 4x L2.
+    Prints one JSON line."""
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, inputs, qmm, workloads
+
+    build_lib.build()
+    qmm.load()
+    torch.cuda.set_device(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    N, K, E = 4096, 5120, 16
+    base, _ = workloads.packed_weights(N, K, inputs.seed_for(6, 0), device="cuda")
+    experts = [base] + [base.clone() for _ in range(E - 1)]   # content does not change the timing
+    ebytes = base.numel()
+    copies = max(1, -(-4 * l2 // (ebytes * E)))
+    sets = [experts] + [[w.clone() for w in experts] for _ in range(copies - 1)]
+    stream = torch.cuda.current_stream()
+    res = {}
+    for M in args.Ms:
+        ids = [i % E for i in range(M)]
+        used = len(set(ids))
+        X, _ = workloads.activations(M, K, inputs.seed_for(6, 50 + M), device="cuda")
+        Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        ws = torch.empty(qmm.indexed_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+        fn = lambda: [qmm.run_indexed(ex, N, K, ids, X, Y, ws) for ex in sets]
+        ms = time_steps(fn, max(2, args.steps // 5), 3, stream, lambda: None) / len(sets)
+        res[str(M)] = {"experts_used": used, "us": round(ms * 1e3, 2),
+                       "gbps": round(weight_gbps(used * ebytes, ms), 1)}
+        if qmm.device_status() != 0:
+            raise RuntimeError("kernel reported a device-side error")
+    print(json.dumps({"metric": "weight-read GB/s of the indexed-expert product (experts in use)", "unit": UNIT,
+                      "experts": E, "N": N, "K": K, "expert_bytes": ebytes, "copies": copies,
+                      "l2": f"expert sets cycled over copies >= 4x L2 ({l2 >> 20} MB)", "per_M": res}), flush=True)
+
+
 def run_reference(args, rank: int):
     """The oracle (plain fp64 C, host cores) on a bounded sample of the same workload."""
     if rank != 0:
@@ -527,6 +566,7 @@ def main(argv=None):
     ap.add_argument("--Ms", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 3, 4, 7, 8, 9, 12, 16])
     ap.add_argument("--variant", choices=["fma", "tc", "auto", "both"], default="both")
     ap.add_argument("--ffn", action="store_true", help="time one feed-forward block per call instead")
+    ap.add_argument("--indexed", action="store_true", help="time the indexed-expert product instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -544,6 +584,10 @@ def main(argv=None):
     if args.ffn:
         if rank == 0:
             run_ffn(args)
+        return
+    if args.indexed:
+        if rank == 0:
+            run_indexed(args)
         return
     dist_ok = False
     if world > 1:

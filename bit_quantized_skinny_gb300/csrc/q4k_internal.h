@@ -34,6 +34,16 @@ size_t noalloc_scratch_needed(int M, int64_t K);
 // G[M x 2F] fp32 (gate columns 0..F-1, up columns F..2F-1), H = bf16(silu(gate) * up).
 cudaError_t launch_swiglu(const float* G, int64_t F, int M, uint16_t* H, cudaStream_t stream);
 
+// Row maps of the indexed-expert product: for each of the M activation rows, the row it goes to
+// (gather) or comes from (scatter) in the gathered blocks.
+struct RowMap {
+  int row[32];
+};
+cudaError_t launch_gather_rows(const RowMap& map, int M, const uint16_t* X, int64_t K, uint16_t* Xg,
+                               cudaStream_t stream);
+cudaError_t launch_scatter_rows(const RowMap& map, int M, const float* Yg, int64_t N, float* Y,
+                                cudaStream_t stream);
+
 // Device dequantization test hook.
 cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 

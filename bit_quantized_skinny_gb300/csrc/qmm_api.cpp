@@ -176,6 +176,67 @@ qmm_status qmm_run_ffn(const void* Wgu_dev, const void* Wdown_dev, int64_t F, in
   return run_jobs(&down, 1, M, QMM_VARIANT_AUTO, stream);
 }
 
+// Indexed-expert product.  Workspace: the gathered activation rows (M rows, then M rows of
+// zeros that the last expert's block may read past its own rows) and the gathered results
+// (used experts x rows of the largest expert; at most (M+1)^2/4 blocks of rows).
+size_t indexed_x_bytes(int M, int64_t K) { return ((size_t)2 * M * (size_t)K * sizeof(uint16_t) + 15) & ~(size_t)15; }
+size_t indexed_y_rows(int M) { return (size_t)(M + 1) * (M + 1) / 4 + 1; }
+
+size_t qmm_indexed_workspace_bytes(int M, int64_t N, int64_t K) {
+  if (M < 1 || M > QMM_MAX_M || check_shape(N, K) != QMM_OK) return 0;
+  return indexed_x_bytes(M, K) + indexed_y_rows(M) * (size_t)N * sizeof(float);
+}
+
+qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64_t N, int64_t K,
+                           const int32_t* ids_host, const uint16_t* X_dev, float* Y_dev, int M,
+                           void* workspace_dev, size_t workspace_bytes, cudaStream_t stream) {
+  if (!experts_host || !ids_host || !workspace_dev) return QMM_ERR_NULL;
+  if (n_experts < 1 || n_experts > QMM_MAX_BATCH) return QMM_ERR_COUNT;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  for (int e = 0; e < n_experts; ++e) {
+    qmm_status s = check_job(experts_host[e], N, K, X_dev, Y_dev);
+    if (s != QMM_OK) return s;
+  }
+  if (!aligned(workspace_dev, 16)) return QMM_ERR_ALIGN;
+  if (workspace_bytes < qmm_indexed_workspace_bytes(M, N, K)) return QMM_ERR_BUFSIZE;
+  int count[QMM_MAX_BATCH] = {};
+  for (int i = 0; i < M; ++i) {
+    if (ids_host[i] < 0 || ids_host[i] >= n_experts) return QMM_ERR_SHAPE;
+    ++count[ids_host[i]];
+  }
+  // experts in use, in order of expert index; their rows gathered in order of i
+  int slot[QMM_MAX_BATCH], first[QMM_MAX_BATCH];
+  int used = 0, rows = 0, mmax = 0;
+  for (int e = 0; e < n_experts; ++e) {
+    if (!count[e]) continue;
+    slot[e] = used++;
+    first[e] = rows;
+    rows += count[e];
+    mmax = count[e] > mmax ? count[e] : mmax;
+  }
+  uint16_t* Xg = static_cast<uint16_t*>(workspace_dev);
+  float* Yg = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace_dev) + indexed_x_bytes(M, K));
+  q4k::RowMap gather{}, scatter{};
+  int seen[QMM_MAX_BATCH] = {};
+  for (int i = 0; i < M; ++i) {
+    const int e = ids_host[i];
+    gather.row[i] = first[e] + seen[e];
+    scatter.row[i] = slot[e] * mmax + seen[e];
+    ++seen[e];
+  }
+  q4k::Job jobs[QMM_MAX_BATCH];
+  for (int e = 0; e < n_experts; ++e)
+    if (count[e])
+      jobs[slot[e]] = q4k::Job{experts_host[e], Xg + (size_t)first[e] * K, Yg + (size_t)slot[e] * mmax * N, N, K};
+  cudaError_t err = cudaMemsetAsync(Xg + (size_t)rows * K, 0, (size_t)mmax * K * sizeof(uint16_t), stream);
+  if (err == cudaSuccess) err = q4k::launch_gather_rows(gather, M, X_dev, K, Xg, stream);
+  if (err != cudaSuccess) return cuda_fail(err);
+  qmm_status s = run_jobs(jobs, used, mmax, QMM_VARIANT_AUTO, stream);
+  if (s != QMM_OK) return s;
+  err = q4k::launch_scatter_rows(scatter, M, Yg, N, Y_dev, stream);
+  return err == cudaSuccess ? QMM_OK : cuda_fail(err);
+}
+
 qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev, cudaStream_t stream) {
   if (!Wq_dev || !out_dev) return QMM_ERR_NULL;
   qmm_status s = check_shape(N, K);

@@ -30,7 +30,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANG
 EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
            "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
-           "qmm_ffn_workspace_bytes", "qmm_run_ffn"]
+           "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -84,6 +84,11 @@ def load(path: str | None = None):
     lib.qmm_ffn_workspace_bytes.restype = ctypes.c_size_t
     lib.qmm_run_ffn.argtypes = [vp, vp, i64, i64, vp, vp, i32, vp, ctypes.c_size_t, vp]
     lib.qmm_run_ffn.restype = i32
+    lib.qmm_indexed_workspace_bytes.argtypes = [i32, i64, i64]
+    lib.qmm_indexed_workspace_bytes.restype = ctypes.c_size_t
+    lib.qmm_run_indexed.argtypes = [ctypes.POINTER(vp), i32, i64, i64, ctypes.POINTER(ctypes.c_int32), vp, vp, i32,
+                                    vp, ctypes.c_size_t, vp]
+    lib.qmm_run_indexed.restype = i32
     lib.qmm_device_status.argtypes = [ctypes.POINTER(u32)]
     lib.qmm_device_status.restype = i32
     lib.qmm_strerror.argtypes = [i32]
@@ -180,6 +185,24 @@ def run_ffn(Wgu, Wdown, F: int, K: int, X, Y, workspace, M: int | None = None, s
                             ctypes.c_void_p(X.data_ptr()), ctypes.c_void_p(Y.data_ptr()), M,
                             ctypes.c_void_p(workspace.data_ptr()), nbytes, _stream_handle(stream))
     _check(st, "qmm_run_ffn")
+
+
+def indexed_workspace_bytes(M: int, N: int, K: int) -> int:
+    return load().qmm_indexed_workspace_bytes(M, N, K)
+
+
+def run_indexed(experts, N: int, K: int, ids, X, Y, workspace, stream=None):
+    """Y[i] = X[i] * dequant(experts[ids[i]])^T for every row i, on the GPU.  `experts`: device
+    tensors (packed N x K each); `ids`: host sequence of M expert indices; `workspace`: a device
+    tensor of >= indexed_workspace_bytes(M, N, K) bytes."""
+    M = len(ids)
+    ptrs = (ctypes.c_void_p * len(experts))(*[w.data_ptr() for w in experts])
+    idv = (ctypes.c_int32 * M)(*[int(v) for v in ids])
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load().qmm_run_indexed(ptrs, len(experts), N, K, idv, ctypes.c_void_p(X.data_ptr()),
+                                ctypes.c_void_p(Y.data_ptr()), M, ctypes.c_void_p(workspace.data_ptr()), nbytes,
+                                _stream_handle(stream))
+    _check(st, "qmm_run_indexed")
 
 
 def dequant(Wq, N: int, K: int, out, stream=None):

@@ -208,6 +208,24 @@ size_t qmm_ffn_workspace_bytes(int M, int64_t F);
 qmm_status qmm_run_ffn(const void* Wgu_dev, const void* Wdown_dev, int64_t F, int64_t K, const uint16_t* X_dev,
                        float* Y_dev, int M, void* workspace_dev, size_t workspace_bytes, cudaStream_t stream);
 
+/* Indexed-expert product (the matrix-product-by-id case that the pages' backend op tests cover
+ * next to the plain product: "sixi-asi 0.9", section "The patch", MUL_MAT and MUL_MAT_ID): row i
+ * of X is multiplied by the weight matrix of expert ids_host[i],
+ *     Y[i][n] = sum_k w_{ids[i]}[n][k] * x[i][k],   0 <= i < M,
+ * with the same dequantization and rounding as qmm_run (each expert's rows are one product of
+ * the batched launch; results as qmm_run_batched on those rows).
+ *   experts_host: n_experts device pointers (host array), each a packed N x K matrix.
+ *   ids_host: M expert indices (host array, read during the call), 0 <= ids[i] < n_experts.
+ *   X_dev: M x K bf16; Y_dev: M x N fp32 (overwritten).
+ *   workspace_dev: caller-owned device memory, >= qmm_indexed_workspace_bytes(M, N, K) bytes,
+ *     16-byte aligned (gathered rows and results; the library allocates nothing else here).
+ * Errors as qmm_run_batched, plus QMM_ERR_SHAPE (an id out of range), QMM_ERR_COUNT (n_experts
+ * outside [1, QMM_MAX_BATCH]), QMM_ERR_ALIGN / QMM_ERR_BUFSIZE (workspace). */
+size_t qmm_indexed_workspace_bytes(int M, int64_t N, int64_t K);
+qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64_t N, int64_t K,
+                           const int32_t* ids_host, const uint16_t* X_dev, float* Y_dev, int M,
+                           void* workspace_dev, size_t workspace_bytes, cudaStream_t stream);
+
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the
  * last read.  Bit 0: a kernel stopped waiting for its own weight copies after a bounded number
