@@ -12,6 +12,10 @@ Functions (all on host numpy arrays):
   matmul(Wq, N, K, X, rows) -> (Y, S) in fp64: Y = sum_k w*x, S = sum_k |w*x|
   half_value, half_from_float, bf16_value: the number formats, from their definitions
   bf16_round(v)             -> bf16 bits of fp64 values, round to nearest even (definition)
+  fmt_pack / fmt_dequant / fmt_matmul(fmt, ...): the same for the other weight formats of
+                               formats_oracle.c (Q5K, NVFP4, INT4 with one scale per 128 columns;
+                               fmt 0 is Q4K and goes to the functions above)
+  e4m3_value, e2m1_value, e4m3_from_float, e2m1_from_float: the 8- and 4-bit float formats
   swiglu(G, F)              -> silu(G[:, :F]) * G[:, F:] in fp64, the step between the gate/up
                                and down products of one feed-forward block (gate+up products
                                are what FlashRT issue #153 times; the SiLU gating between them is
@@ -28,6 +32,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "q4k_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "formats_oracle.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -35,12 +40,12 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile q4k_oracle.c with gcc (OpenMP, no FMA contraction, no fast-math)."""
+    """Compile the oracle's C files with gcc (OpenMP, no FMA contraction, no fast-math)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB_PATH) or any(os.path.getmtime(_LIB_PATH) < os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+               "-fPIC", "-shared", "-o", tmp] + _SRCS + ["-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -64,6 +69,22 @@ def _load():
             lib.oracle_matmul.restype = None
             lib.oracle_pack.argtypes = [vp, i64, i64, vp]
             lib.oracle_pack.restype = i32
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_value.restype = ctypes.c_double
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_e2m1_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_from_float.restype = ctypes.c_uint8
+            lib.oracle_fmt_packed_bytes.argtypes = [i32, i64, i64]
+            lib.oracle_fmt_packed_bytes.restype = i64
+            lib.oracle_fmt_dequant.argtypes = [i32, vp, i64, i64, vp, i64, vp]
+            lib.oracle_fmt_dequant.restype = None
+            lib.oracle_fmt_matmul.argtypes = [i32, vp, i64, i64, vp, i32, vp, i64, vp, vp, i32]
+            lib.oracle_fmt_matmul.restype = None
+            lib.oracle_fmt_pack.argtypes = [i32, vp, i64, i64, vp]
+            lib.oracle_fmt_pack.restype = i32
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = i32
             _lib = lib
@@ -168,3 +189,88 @@ def swiglu(G: np.ndarray, F: int) -> np.ndarray:
     g, u = G[:, :F], G[:, F:]
     with np.errstate(over="ignore"):
         return g / (1.0 + np.exp(-g)) * u
+
+
+# ---- the other weight formats (formats_oracle.c) -------------------------------------------
+FMT_Q4K, FMT_Q5K, FMT_NVFP4, FMT_INT4 = 0, 1, 2, 3
+FORMATS = {"q4k": FMT_Q4K, "q5k": FMT_Q5K, "nvfp4": FMT_NVFP4, "int4": FMT_INT4}
+
+
+def e4m3_value(c: int) -> float:
+    return _load().oracle_e4m3_value(c)
+
+
+def e2m1_value(c: int) -> float:
+    return _load().oracle_e2m1_value(c)
+
+
+def e4m3_from_float(x: float) -> int:
+    """E4M3 code of a non-negative value: nearest, ties to even, clamped to 448."""
+    return _load().oracle_e4m3_from_float(ctypes.c_float(x))
+
+
+def e2m1_from_float(x: float) -> int:
+    """E2M1 code of a value: nearest magnitude, ties to even, clamped to 6, sign kept."""
+    return _load().oracle_e2m1_from_float(ctypes.c_float(x))
+
+
+def fmt_packed_bytes(fmt: int, N: int, K: int) -> int:
+    if fmt == FMT_Q4K:
+        return packed_bytes(N, K)
+    return int(_load().oracle_fmt_packed_bytes(fmt, N, K))
+
+
+def fmt_pack(fmt: int, W: np.ndarray) -> np.ndarray:
+    if fmt == FMT_Q4K:
+        return pack(W)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    if K % 256 != 0 or K == 0 or N == 0:
+        raise ValueError("K must be a positive multiple of 256 and N >= 1")
+    out = np.zeros(fmt_packed_bytes(fmt, N, K), dtype=np.uint8)
+    rc = _load().oracle_fmt_pack(fmt, _ptr(W), N, K, _ptr(out))
+    if rc != 0:
+        raise OraclePackError(f"oracle_fmt_pack failed with status {rc}")
+    return out
+
+
+def fmt_dequant(fmt: int, Wq: np.ndarray, N: int, K: int, rows=None) -> np.ndarray:
+    """fp32 weights of rows `rows` (None: all N rows) of a packed matrix."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    assert Wq.size == fmt_packed_bytes(fmt, N, K)
+    if fmt == FMT_Q4K:
+        full = dequant(Wq, N, K)
+        return full if rows is None else full[np.asarray(rows)]
+    if rows is None:
+        nrows, rp = N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        nrows, rp = rows.size, _ptr(rows)
+    out = np.empty((nrows, K), dtype=np.float32)
+    if nrows:
+        _load().oracle_fmt_dequant(fmt, _ptr(Wq), N, K, rp, nrows, _ptr(out))
+    return out
+
+
+def fmt_matmul(fmt: int, Wq: np.ndarray, N: int, K: int, X_bits: np.ndarray, rows=None, threads: int = 0):
+    """Y, S (float64, M x len(rows)) of the product in format `fmt`, as matmul() for Q4K."""
+    if fmt == FMT_Q4K:
+        return matmul(Wq, N, K, X_bits, rows, threads)
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    assert Wq.size == fmt_packed_bytes(fmt, N, K)
+    X_bits = np.ascontiguousarray(X_bits, dtype=np.uint16)
+    if X_bits.ndim == 1:
+        X_bits = X_bits[None, :]
+    M = X_bits.shape[0]
+    assert X_bits.shape[1] == K
+    if rows is None:
+        nrows, rp = N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        assert rows.ndim == 1 and (rows.size == 0 or (rows.min() >= 0 and rows.max() < N))
+        nrows, rp = rows.size, _ptr(rows)
+    Y = np.empty((M, nrows), dtype=np.float64)
+    S = np.empty((M, nrows), dtype=np.float64)
+    if nrows:
+        _load().oracle_fmt_matmul(fmt, _ptr(Wq), N, K, _ptr(X_bits), M, rp, nrows, _ptr(Y), _ptr(S), threads)
+    return Y, S
