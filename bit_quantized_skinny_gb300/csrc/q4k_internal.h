@@ -5,13 +5,20 @@
 
 namespace q4k {
 
-// One product handed to a kernel: Y[M x N] = X[M x K] * dequant(W)^T.
+// Weight formats (the qmm_format codes of the C ABI).
+enum WeightFormat : int { kFmtQ4K = 0, kFmtQ5K = 1, kFmtNVFP4 = 2, kFmtINT4 = 3 };
+
+// One product handed to a kernel: Y[M x N] = X[M x K] * dequant(W)^T.  fmt is the weight
+// format; aux points into the packed buffer at what the format keeps outside its row blocks
+// (NVFP4: the fp32 tensor scale; INT4: the scale plane; otherwise unused).
 struct Job {
   const void* W;
   const uint16_t* X;
   float* Y;
   int64_t N;
   int64_t K;
+  int fmt = kFmtQ4K;
+  const void* aux = nullptr;
 };
 
 // Launch the CUDA-core (fma) kernel over `count` jobs sharing M, in one launch.
@@ -44,14 +51,19 @@ cudaError_t launch_gather_rows(const RowMap& map, int M, const uint16_t* X, int6
 cudaError_t launch_scatter_rows(const RowMap& map, int M, const float* Yg, int64_t N, float* Y,
                                 cudaStream_t stream);
 
-// Device dequantization test hook.
+// Device dequantization test hooks (Q4K; the other formats).
 cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
+cudaError_t launch_dequant_fmt(int fmt, const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 
 // Device status words of the kernel files: read and clear (synchronous; 0 = no error).
 cudaError_t read_and_clear_fma_status(unsigned* out);
 cudaError_t read_and_clear_tc_status(unsigned* out);
 
-// Host packer (qmm_pack.cpp).  Returns 0, or 6 on non-finite input / fp16 overflow.
+// Host packers (qmm_pack.cpp).  Return 0, or 6 on non-finite input / fp16 overflow.
 int pack_q4k(const float* W, int64_t N, int64_t K, uint8_t* out, int threads);
+int pack_fmt(int fmt, const float* W, int64_t N, int64_t K, uint8_t* out, int threads);
+// Bytes of a packed N x K matrix in format fmt, and the offset of its aux part (0: none).
+int64_t fmt_packed_bytes(int fmt, int64_t N, int64_t K);
+int64_t fmt_aux_offset(int fmt, int64_t N, int64_t K);
 
 }  // namespace q4k

@@ -69,6 +69,7 @@
 #include <cuda_fp16.h>
 
 #include "q4k_device.cuh"
+#include "q4k_formats.cuh"
 #include "q4k_internal.h"
 #include "q4k_tcgen05.cuh"
 
@@ -87,22 +88,34 @@ constexpr int kMaxGroups = 3;
 // thread 128 registers (a sub-partition holds 16384).
 __host__ __device__ constexpr int groups(int mpad) { return mpad <= 16 ? 3 : 2; }
 __host__ __device__ constexpr int threads(int mpad) { return 32 * (groups(mpad) * kGroupWarps + 2); }
-constexpr int kWStageBytes = kTileRows * kBlockBytes;    // 18432: one super-block of a tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
 constexpr int kMaxPrep = 512;      // distinct activations per preparation launch
+constexpr int kSmemLimit = 232448; // shared memory per CTA (227 KB)
+
+// Bytes of one row's 256 weights in the streamed weight plane (one TMA box column), per format:
+// Q4K and NVFP4 144 (NVFP4: 16 E4M3 scales + 128 bytes of codes), Q5K 176, INT4 128 (its
+// scales live in a separate plane).  The dmin term (an extra MMA and a second accumulator
+// column block) belongs to the k-quants only.
+__host__ __device__ constexpr int blk_bytes(int f) { return f == kFmtQ5K ? 176 : (f == kFmtINT4 ? 128 : 144); }
+__host__ __device__ constexpr bool has_min(int f) { return f == kFmtQ4K || f == kFmtQ5K; }
+__host__ __device__ constexpr int w_stage_bytes(int f) { return kTileRows * blk_bytes(f); }
 
 __host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
 // A stage holds one super-block of a tile (the weight rows) and the prepared activation block
 // of the same super-block: both arrive on one barrier, issued the same distance ahead.
-// (rounded up to 128 bytes: a TMA tile copy writes to a 128-byte aligned address)
-__host__ __device__ constexpr int stage_bytes(int mpad) { return (kWStageBytes + bblock_bytes(mpad) + 127) / 128 * 128; }
-__host__ __device__ constexpr int stages(int mpad) { return mpad <= 16 ? 8 : 5; }
+// (rounded up to 128 bytes: a TMA tile copy writes to a 128-byte aligned address; INT4 tiles
+// are copied with the 128-byte swizzle, whose destination is 1024-byte aligned)
+__host__ __device__ constexpr int stage_bytes(int mpad, int f) {
+  return f == kFmtINT4 ? (w_stage_bytes(f) + bblock_bytes(mpad) + 1023) / 1024 * 1024
+                       : (w_stage_bytes(f) + bblock_bytes(mpad) + 127) / 128 * 128;
+}
 constexpr int kMaxStages = 8;
-// TMEM columns.  Each group owns one A slot (one super-block: 64 columns of sc*q pairs per K
+// TMEM columns.  Each group owns one A slot (one super-block: 64 columns of fp16 pairs per K
 // half and 8 columns of (m_j) pairs for the dmin MMA, 136 in all) and one accumulator (Mpad
-// columns of the product and Mpad of the dmin term, at the top of the 512 columns):
+// columns of the product and Mpad of the dmin term -- or, for INT4, of the second K half --
+// at the top of the 512 columns):
 //   Mpad 16: A slots 0..407, accumulators 416..511
 //   Mpad 32: A slots 0..271, accumulators 384..511
 constexpr uint32_t kACols = 136;
@@ -130,20 +143,34 @@ enum : int {
   kNumBars = kBarDrain + 1
 };
 
-template <int MPAD>
+// Mpad 32: each group's running sum of chunk sums (32 tokens x 128 rows of fp32) lives in
+// shared memory, not in registers.
+__host__ __device__ constexpr int ytot_bytes(int mpad) { return mpad == 32 ? groups(mpad) * 32 * kTileRows * 4 : 0; }
+// Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest.
+__host__ __device__ constexpr int stages(int mpad, int f) {
+  return (mpad <= 16 ? 8 : 5) < (kSmemLimit - ytot_bytes(mpad) - kNumBars * 8 - 32) / stage_bytes(mpad, f)
+             ? (mpad <= 16 ? 8 : 5)
+             : (kSmemLimit - ytot_bytes(mpad) - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+}
+
+template <int MPAD, int FMT>
 struct TcSmem {
   static constexpr int kW = 0;
-  // Mpad 32: each group's running sum of chunk sums (32 tokens x 128 rows of fp32) lives here,
-  // not in registers
-  static constexpr int kYtot = kW + stages(MPAD) * stage_bytes(MPAD);
-  static constexpr int kBars = kYtot + (MPAD == 32 ? groups(MPAD) * 32 * kTileRows * 4 : 0);
+  static constexpr int kYtot = kW + stages(MPAD, FMT) * stage_bytes(MPAD, FMT);
+  static constexpr int kBars = kYtot + ytot_bytes(MPAD);
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
-static_assert(TcSmem<16>::kTotal <= 232448 && TcSmem<32>::kTotal <= 232448, "shared memory");
+static_assert(TcSmem<16, kFmtQ4K>::kTotal <= kSmemLimit && TcSmem<32, kFmtQ4K>::kTotal <= kSmemLimit &&
+              TcSmem<16, kFmtQ5K>::kTotal <= kSmemLimit && TcSmem<32, kFmtQ5K>::kTotal <= kSmemLimit &&
+              TcSmem<16, kFmtINT4>::kTotal <= kSmemLimit && TcSmem<32, kFmtINT4>::kTotal <= kSmemLimit,
+              "shared memory");
+static_assert(stages(16, kFmtQ4K) == 8 && stages(32, kFmtQ4K) == 5 && stages(16, kFmtQ5K) >= 4 &&
+              stages(32, kFmtQ5K) >= 3 && stages(16, kFmtINT4) >= 4 && stages(32, kFmtINT4) >= 3,
+              "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
-static_assert(stage_bytes(16) % 128 == 0 && stage_bytes(32) % 128 == 0 && kWStageBytes % 128 == 0, "stage alignment");
-static_assert(stages(16) <= kMaxStages && stages(32) <= kMaxStages, "stage barriers");
+static_assert(stage_bytes(16, kFmtQ4K) % 128 == 0 && stage_bytes(32, kFmtQ5K) % 128 == 0 &&
+              stage_bytes(16, kFmtINT4) % 1024 == 0 && w_stage_bytes(kFmtQ5K) % 128 == 0, "stage alignment");
 
 struct TcEntry {
   float* Y;
@@ -169,6 +196,10 @@ struct TcParams {
   int M;
   int tasks_total;
   int pad_;
+  // the formats other than Q4K run one product per launch: what that product keeps outside its
+  // row blocks (NVFP4: the fp32 tensor scale; INT4: the N x K/128 binary16 scale plane).  Kept
+  // out of TcEntry: the Q4K kernel measured ~1.5% slower with a different entry layout.
+  const void* aux;
 };
 
 struct PrepEntry {
@@ -193,8 +224,10 @@ __device__ __forceinline__ __half2 bits2h(uint32_t v) { return *reinterpret_cast
 
 // ------------------------------------------------------------------------------------------
 // Activation preparation.  Block = 8*MPAD threads; thread (i = t/8, j = t%8) handles token i,
-// sub-block j (32 activations) of one super-block.
-template <int MPAD, int NX>
+// sub-block j (32 activations) of one super-block.  Each 8-activation word is stored as fp16
+// pairs in the order of the weight decode: (x_c, x_c+4), c = 0..3, or with NAT (NVFP4) the
+// natural (x_2c, x_2c+1).
+template <int MPAD, int NX, bool NAT>
 __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_constant__ PrepParams<NX> P) {
   // the product kernel that follows may start its prologue now (programmatic dependent launch);
   // it waits for this grid's completion before it reads what this grid writes
@@ -260,7 +293,8 @@ __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_consta
     }
     uint32_t packed[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) packed[c] = h2bits(__floats2half2_rn(xv[c], xv[c + 4]));
+    for (int c = 0; c < 4; ++c)
+      packed[c] = NAT ? h2bits(__floats2half2_rn(xv[2 * c], xv[2 * c + 1])) : h2bits(__floats2half2_rn(xv[c], xv[c + 4]));
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       const __half2 hh = bits2h(packed[p & 3]);
@@ -368,22 +402,150 @@ __device__ __forceinline__ uint32_t su_of(const int (&n)[NG], int g, int i) {
   return s;
 }
 
-// MPAD: MMA width (token columns of B and of the accumulators, 16 or 32).  MT: the token columns
-// the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M hold zeros.
-template <int MPAD, int MT, int MAXE>
+// Weight decode of one K half (128 weights of a row) of each format into the A slot of TMEM.
+// Inputs: the row's block in the stage at `rb`, its first 16 bytes `hd`, the half h; the A
+// columns of the half at `aaddr`.  The quant words are read from shared memory before the
+// caller releases the stage (the `in` structure), then decoded and stored with tcgen05.st.
+template <int FMT>
+struct HalfIn {
+  uint4 qv[4];   // quants of the half: 16 bytes per 32 weights
+  uint4 hb;      // Q5K: the high-bit words of the half's four sub-blocks
+};
+
+// INT4 tiles are copied with the 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+// c ^ (r % 8) of the row (spreads the rows' reads over all shared-memory banks).
+template <int FMT>
+__device__ __forceinline__ void load_half(HalfIn<FMT>& in, uint32_t rb, int h, int r) {
+  if constexpr (FMT == kFmtINT4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 16u * (uint32_t)((4 * h + k) ^ (r & 7)));
+  } else if constexpr (FMT == kFmtQ5K) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 48 + 64 * h + 16 * k);
+    in.hb = lds128(rb + 16 + 16 * h);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
+  }
+}
+
+// fp16 constants of the decodes, made once per thread (outside the super-block loop)
+struct DecodeConsts {
+  __half2 k1024, kn1024, k1o16, kn64, kn1032, kn72;
+  __device__ __forceinline__ DecodeConsts()
+      : k1024(bits2h(0x64006400u)), kn1024(__float2half2_rn(-1024.f)), k1o16(__float2half2_rn(0.0625f)),
+        kn64(__float2half2_rn(-64.f)), kn1032(__float2half2_rn(-1032.f)), kn72(__float2half2_rn(-72.f)) {}
+};
+
+template <int FMT>
+__device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& hd, int h, uint32_t aaddr,
+                                            const DecodeConsts& C) {
+  if constexpr (FMT == kFmtQ4K || FMT == kFmtQ5K) {
+    const __half2 k1024 = C.k1024, kn1024 = C.kn1024, k1o16 = C.k1o16, kn64 = C.kn64;
+    // the 12-bit (sc, m) groups of sub-blocks 4h .. 4h+3
+    const uint64_t F = h ? ((uint64_t)hd.w << 32 | hd.z) : ((uint64_t)hd.z << 32 | hd.y);
+    const int fbase = h ? 16 : 0;
+    __half2 sc2[4], scm[4], sc16[4], sc64[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t gr = (uint32_t)(F >> (fbase + 12 * jj)) & 0xFFFu;
+      const uint32_t scb = ((gr & 63u) | 0x6400u) * 0x10001u;      // (1024+sc, 1024+sc)
+      sc2[jj] = __hsub2(bits2h(scb), k1024);                       // (sc, sc) exact
+      scm[jj] = __hmul2(sc2[jj], kn1024);                           // -1024 sc
+      sc16[jj] = __hmul2(sc2[jj], k1o16);                           // sc / 16
+      sc64[jj] = __hmul2(sc2[jj], kn64);                            // -64 sc
+    }
+    // A = sc*q as fp16 pairs, 16 columns per sub-block
+    const uint32_t hwords[4] = {in.hb.x, in.hb.y, in.hb.z, in.hb.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = in.qv[k];
+      const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+      uint32_t cols[16];
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) {
+        const uint32_t wv = words[ww];
+        uint32_t p[4];
+        if constexpr (FMT == kFmtQ5K) {
+          if (ww == 0) q5k_magic<0>(wv, hwords[k], p);
+          if (ww == 1) q5k_magic<1>(wv, hwords[k], p);
+          if (ww == 2) q5k_magic<2>(wv, hwords[k], p);
+          if (ww == 3) q5k_magic<3>(wv, hwords[k], p);
+        } else {
+          const uint32_t b8 = wv >> 8;
+          asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p[0]) : "r"(wv));
+          asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p[1]) : "r"(wv));
+          asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p[2]) : "r"(b8));
+          asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p[3]) : "r"(b8));
+        }
+        cols[4 * ww + 0] = h2bits(__hfma2(bits2h(p[0]), sc2[k], scm[k]));   // (q0, q4) * sc
+        cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p[1]), sc16[k], sc64[k]));  // (q1, q5) * sc
+        cols[4 * ww + 2] = h2bits(__hfma2(bits2h(p[2]), sc2[k], scm[k]));   // (q2, q6) * sc
+        cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p[3]), sc16[k], sc64[k]));  // (q3, q7) * sc
+      }
+      tc::st_x16(aaddr + 16 * k, cols);
+    }
+  } else if constexpr (FMT == kFmtINT4) {
+    // A = q (the integer itself); the scale of each K half is applied in the epilogue
+    const __half2 kn1032 = C.kn1032, k1o16 = C.k1o16, kn72 = C.kn72;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = in.qv[k];
+      const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+      uint32_t cols[16];
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) {
+        uint32_t p[4];
+        int4_magic(words[ww], p);
+        cols[4 * ww + 0] = h2bits(__hadd2(bits2h(p[0]), kn1032));          // (q0, q4)
+        cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p[1]), k1o16, kn72));     // (q1, q5)
+        cols[4 * ww + 2] = h2bits(__hadd2(bits2h(p[2]), kn1032));          // (q2, q6)
+        cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p[3]), k1o16, kn72));     // (q3, q7)
+      }
+      tc::st_x16(aaddr + 16 * k, cols);
+    }
+  } else {   // NVFP4: A = s_b * v, exact (at most 6 significant bits, at most 6 * 448)
+    // the E4M3 scales of blocks 8h .. 8h+7 as fp16 pairs
+    const uint32_t sw0 = h ? hd.z : hd.x, sw1 = h ? hd.w : hd.y;
+    const uint32_t sp[4] = {e4m3x2_pair(sw0), e4m3x2_pair(sw0 >> 16), e4m3x2_pair(sw1), e4m3x2_pair(sw1 >> 16)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = in.qv[k];
+      const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+      // weights 32k .. 32k+15 use scale 2k of the half, 32k+16 .. 32k+31 scale 2k+1
+      const __half2 s_lo = __low2half2(bits2h(sp[k])), s_hi = __high2half2(bits2h(sp[k]));
+      uint32_t cols[16];
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) {
+        uint32_t p[4];
+        e2m1x8_pairs(words[ww], p);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cols[4 * ww + c] = h2bits(__hmul2(bits2h(p[c]), ww < 2 ? s_lo : s_hi));
+      }
+      tc::st_x16(aaddr + 16 * k, cols);
+    }
+  }
+}
+
+// FMT: weight format.  MPAD: MMA width (token columns of B and of the accumulators, 16 or 32).
+// MT: the token columns the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M
+// hold zeros.
+template <int FMT, int MPAD, int MT, int MAXE>
 __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
-  using L = TcSmem<MPAD>;
+  using L = TcSmem<MPAD, FMT>;
   constexpr int NG = groups(MPAD);
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
   constexpr int kMmaWarp = kProdWarp + 1;       // MMA issue; owns TMEM
   constexpr int kBB = bblock_bytes(MPAD);
-  constexpr int kS = stages(MPAD);
-  constexpr int kSB = stage_bytes(MPAD);
+  constexpr int kS = stages(MPAD, FMT);
+  constexpr int kSB = stage_bytes(MPAD, FMT);
+  constexpr int kBlk = blk_bytes(FMT);
+  constexpr int kWSB = w_stage_bytes(FMT);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t sW = smem_addr(smem + L::kW);   // stage k: weights at sW + k*kSB, activations 18432 further
+  const uint32_t sW = smem_addr(smem + L::kW);   // stage k: weights at sW + k*kSB, activations kWSB further
   const uint32_t bars = smem_addr(smem + L::kBars);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
@@ -460,9 +622,9 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
             owner = (owner & ~(3u << (2 * ws))) | ((uint32_t)g << (2 * ws));
             const uint32_t st = sW + ws * kSB;
             const int e = cur[g].e, sb = cur[g].sb;
-            mbar_arrive_expect_tx(gfull(g, ws), kWStageBytes + kBB);
-            tma_load_2d(st, &P.maps[e], sb * kBlockBytes, cur[g].tile * kTileRows, gfull(g, ws), pol);
-            bulk_g2s(st + kWStageBytes, P.e[e].B + (int64_t)sb * kBB, kBB, gfull(g, ws), 0ull);
+            mbar_arrive_expect_tx(gfull(g, ws), kWSB + kBB);
+            tma_load_2d(st, &P.maps[e], sb * kBlk, cur[g].tile * kTileRows, gfull(g, ws), pol);
+            bulk_g2s(st + kWSB, P.e[e].B + (int64_t)sb * kBB, kBB, gfull(g, ws), 0ull);
             cur[g].advance(P);
             ++su;
           }
@@ -497,7 +659,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           if (ok && i < n[g]) {
             gbits ^= bit;
             tc::fence_after_sync();
-            const uint64_t bdesc = tc::smem_desc_kmajor(sW + ws * kSB + kWStageBytes, 128, 4096);   // + 16 per MMA: 256 bytes
+            const uint64_t bdesc = tc::smem_desc_kmajor(sW + ws * kSB + kWSB, 128, 4096);   // + 16 per MMA: 256 bytes
             tc::mma_f16_ts_x8(tmem + acc1_col(MPAD, g), tmem + a_col(g), bdesc, 16, idesc, 0);
             ok = wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u);
           }
@@ -506,10 +668,16 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
             const uint32_t abase = tmem + a_col(g);
             const uint32_t d1 = tmem + acc1_col(MPAD, g);
             const uint32_t d2 = tmem + acc2_col(MPAD, g);
-            const uint32_t bslot = sW + ws * kSB + kWStageBytes;
+            const uint32_t bslot = sW + ws * kSB + kWSB;
             const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);
-            tc::mma_f16_ts_x8(d1, abase + 64, bdesc + 8 * 16, 16, idesc, 1);
-            tc::mma_f16_ts(d2, abase + 128, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
+            if constexpr (FMT == kFmtINT4) {
+              // the second K half has its own scale: its own accumulator
+              tc::mma_f16_ts_x8(d2, abase + 64, bdesc + 8 * 16, 16, idesc, 0);
+            } else {
+              tc::mma_f16_ts_x8(d1, abase + 64, bdesc + 8 * 16, 16, idesc, 1);
+            }
+            if constexpr (has_min(FMT))
+              tc::mma_f16_ts(d2, abase + 128, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
             tc::commit(bar(kBarGDone + g));
             tc::commit(bar(kBarWEmpty + ws));
             ++su;
@@ -523,14 +691,12 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
+    // ------------------------------------------------------------------ dequant + epilogue
     const int grp = warp >> 2;       // dequant group: the CTA's local tasks j % NG == grp
     const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
     const int r = 32 * q + lane;     // row inside the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    const __half2 k1024 = bits2h(0x64006400u);
-    const __half2 kn1024 = __float2half2_rn(-1024.f);
-    const __half2 k1o16 = __float2half2_rn(0.0625f);
-    const __half2 kn64 = __float2half2_rn(-64.f);
+    const DecodeConsts dc;
     auto wait_w = [&](uint32_t k, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(k, parity)); };
 
     float y[MT];   // the current chunk's sum, tokens 0 .. MT-1 of this thread's row
@@ -560,6 +726,16 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     uint4 hd_n = make_uint4(0, 0, 0, 0);
     float sigma_n = 0.f;
     for (int i = 0; cur.t >= 0; ++i) {
+      // INT4: the scales of this row's two K halves, from the scale plane (read early: they are
+      // needed only by the epilogue)
+      uint32_t int4_scales = 0;
+      if constexpr (FMT == kFmtINT4) {
+        const TcEntry& E0 = P.e[cur.e];
+        const int row0 = cur.tile * kTileRows + r;
+        if (row0 < E0.N)
+          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux) +
+                                                                (int64_t)row0 * (E0.K >> 7)) + cur.sb);
+      }
       uint32_t ws;
       uint4 hd;
       float sigma;
@@ -572,60 +748,24 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
         if (!wait_w(gfull(grp, ws), (sbits >> ws) & 1u)) break;
         sbits ^= 1u << ws;
         // this row's header and 2^s of the activation block from the stage
-        hd = lds128(sW + ws * kSB + r * kBlockBytes);
-        sigma = lds_f32(sW + ws * kSB + kWStageBytes + MPAD * 544);
+        hd = FMT == kFmtINT4 ? make_uint4(0, 0, 0, 0) : lds128(sW + ws * kSB + r * kBlk);
+        sigma = lds_f32(sW + ws * kSB + kWSB + MPAD * 544);
       }
       // ---- the rest of this row's super-block (quants one K half at a time) from the stage;
       // this warp's part of the stage is released once all are read
-      const uint32_t rb = sW + ws * kSB + r * kBlockBytes;
+      const uint32_t rb = sW + ws * kSB + r * kBlk;
 
       // (the A slot is free: this group waited for its previous MMAs below)
 
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint4 qv[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
+        HalfIn<FMT> in;
+        load_half<FMT>(in, rb, h, r);
         if (h == 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         }
-        // the 12-bit (sc, m) groups of sub-blocks 4h .. 4h+3
-        const uint64_t F = h ? ((uint64_t)hd.w << 32 | hd.z) : ((uint64_t)hd.z << 32 | hd.y);
-        const int fbase = h ? 16 : 0;
-        __half2 sc2[4], scm[4], sc16[4], sc64[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t gr = (uint32_t)(F >> (fbase + 12 * jj)) & 0xFFFu;
-          const uint32_t scb = ((gr & 63u) | 0x6400u) * 0x10001u;      // (1024+sc, 1024+sc)
-          sc2[jj] = __hsub2(bits2h(scb), k1024);                       // (sc, sc) exact
-          scm[jj] = __hmul2(sc2[jj], kn1024);                           // -1024 sc
-          sc16[jj] = __hmul2(sc2[jj], k1o16);                           // sc / 16
-          sc64[jj] = __hmul2(sc2[jj], kn64);                            // -64 sc
-        }
-        // A = sc*q as fp16 pairs, 16 columns per sub-block
-        const uint32_t aaddr = aslot + 64u * h;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = qv[k];
-          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-          uint32_t cols[16];
-#pragma unroll
-          for (int ww = 0; ww < 4; ++ww) {
-            const uint32_t wv = words[ww];
-            const uint32_t b8 = wv >> 8;
-            uint32_t p0, p1, p2, p3;
-            asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p0) : "r"(wv));
-            asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p1) : "r"(wv));
-            asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p2) : "r"(b8));
-            asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p3) : "r"(b8));
-            cols[4 * ww + 0] = h2bits(__hfma2(bits2h(p0), sc2[k], scm[k]));   // (q0, q4) * sc
-            cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p1), sc16[k], sc64[k]));  // (q1, q5) * sc
-            cols[4 * ww + 2] = h2bits(__hfma2(bits2h(p2), sc2[k], scm[k]));   // (q2, q6) * sc
-            cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p3), sc16[k], sc64[k]));  // (q3, q7) * sc
-          }
-          tc::st_x16(aaddr + 16 * k, cols);
-        }
+        decode_half<FMT>(in, hd, h, aslot + 64u * h, dc);
         if (h == 0) {   // the first K half goes to the MMA warp now
           tc::wait_st();
           tc::fence_before_sync();
@@ -633,8 +773,9 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp));
         }
       }
-      {
+      if constexpr (has_min(FMT)) {
         // A_ext: (m_0..m_7) at k = 0..7 and again at k = 8..15
+        const __half2 k1024 = dc.k1024;
         const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 (bits 0..47)
         const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 (bits 16..63)
         uint32_t mm[8];
@@ -658,32 +799,48 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           ws_n = su_of<NG>(n, grp, i + 1) % kS;
           if (!wait_w(gfull(grp, ws_n), (sbits >> ws_n) & 1u)) break;
           sbits ^= 1u << ws_n;
-          hd_n = lds128(sW + ws_n * kSB + r * kBlockBytes);
-          sigma_n = lds_f32(sW + ws_n * kSB + kWStageBytes + MPAD * 544);
+          hd_n = FMT == kFmtINT4 ? make_uint4(0, 0, 0, 0) : lds128(sW + ws_n * kSB + r * kBlk);
+          sigma_n = lds_f32(sW + ws_n * kSB + kWSB + MPAD * 544);
         }
       }
 
       // ---- the accumulator of this super-block into y (MT token columns)
       if (!wait_w(bar(kBarGDone + grp), (uint32_t)i & 1u)) break;
       tc::fence_after_sync();
-      const float2 dd = __half22float2(bits2h(hd.x));   // (D, Dm) of this row
-      const float sx = dd.x * sigma, sy = dd.y * sigma * 64.f;
+      // the factors of the two accumulator blocks:
+      //   k-quants  y += (D 2^s) acc - (Dm 2^s 64) acc_ext
+      //   NVFP4     y += (g 2^s) acc
+      //   INT4      y += (s_0 2^s) acc_half0 + (s_1 2^s) acc_half1
+      float sx, sy;
+      if constexpr (has_min(FMT)) {
+        const float2 dd = __half22float2(bits2h(hd.x));   // (D, Dm) of this row
+        sx = dd.x * sigma;
+        sy = -(dd.y * sigma * 64.f);
+      } else if constexpr (FMT == kFmtNVFP4) {
+        sx = __ldg(static_cast<const float*>(P.aux)) * sigma;
+        sy = 0.f;
+      } else {
+        const float2 ss = __half22float2(bits2h(int4_scales));
+        sx = ss.x * sigma;
+        sy = ss.y * sigma;
+      }
+      constexpr bool kTwo = FMT != kFmtNVFP4;   // a second accumulator block to read
       constexpr int kW = MT == 16 ? 16 : 8;   // token columns per TMEM read round
 #pragma unroll
       for (int c0 = 0; c0 < MT; c0 += kW) {
         float a1[kW], a2[kW];
         if constexpr (kW == 8) {
           tc::ld_x8(acc1 + c0, a1);
-          tc::ld_x8(acc2 + c0, a2);
+          if constexpr (kTwo) tc::ld_x8(acc2 + c0, a2);
         } else {
           tc::ld_x16(acc1 + c0, a1);
-          tc::ld_x16(acc2 + c0, a2);
+          if constexpr (kTwo) tc::ld_x16(acc2 + c0, a2);
         }
         tc::wait_ld();
 #pragma unroll
         for (int k = 0; k < kW; ++k) {
           y[c0 + k] = fmaf(sx, a1[k], y[c0 + k]);
-          y[c0 + k] = fmaf(-sy, a2[k], y[c0 + k]);
+          if constexpr (kTwo) y[c0 + k] = fmaf(sy, a2[k], y[c0 + k]);
         }
       }
 
@@ -747,6 +904,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+
 // ------------------------------------------------------------------------------------------
 // Per-(device, stream) workspace for the prepared activations.  Grown on demand with
 // cudaMalloc (the first call on a stream, or a call needing more room, allocates; cudaFree of a
@@ -802,25 +960,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Map of a packed Q4K matrix as a 2D byte array: inner dimension the K/256*144 bytes of a row,
-// outer dimension the N rows; the box is one super-block (144 bytes) of 128 rows.
-cudaError_t weight_map(const void* W, int64_t N, int64_t K, CUtensorMap* out) {
+// Map of a packed matrix's weight plane as a 2D byte array: inner dimension the bytes of a row
+// (K/256 blocks of blk_bytes(fmt)), outer dimension the N rows; the box is one 256-weight block
+// of 128 rows.  INT4 boxes (128 bytes) are copied with the 128-byte swizzle.
+cudaError_t weight_map(const void* W, int64_t N, int64_t K, int fmt, CUtensorMap* out) {
   static std::mutex mu;
-  static std::map<std::tuple<const void*, int64_t, int64_t>, CUtensorMap> cache;
+  static std::map<std::tuple<const void*, int64_t, int64_t, int>, CUtensorMap> cache;
   std::lock_guard<std::mutex> g(mu);
-  const auto key = std::make_tuple(W, N, K);
+  const auto key = std::make_tuple(W, N, K, fmt);
   auto it = cache.find(key);
   if (it != cache.end()) { *out = it->second; return cudaSuccess; }
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t rowbytes = (cuuint64_t)(K / 256) * kBlockBytes;
+  const cuuint64_t rowbytes = (cuuint64_t)(K / 256) * blk_bytes(fmt);
   const cuuint64_t dims[2] = {rowbytes, (cuuint64_t)N};
   const cuuint64_t strides[1] = {rowbytes};
-  const cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)kTileRows};
+  const cuuint32_t box[2] = {(cuuint32_t)blk_bytes(fmt), (cuuint32_t)kTileRows};
   const cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
   const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        fmt == kFmtINT4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   if (cache.size() >= 4096) cache.clear();
@@ -829,14 +989,15 @@ cudaError_t weight_map(const void* W, int64_t N, int64_t K, CUtensorMap* out) {
   return cudaSuccess;
 }
 
-template <int MPAD, int MT, int MAXE>
+template <int FMT, int MPAD, int MT, int MAXE>
 cudaError_t set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(q4k_tc_kernel<MPAD, MT, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<MPAD>::kTotal);
+  err = cudaFuncSetAttribute(q4k_tc_kernel<FMT, MPAD, MT, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TcSmem<MPAD, FMT>::kTotal);
   if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return err;
 }
@@ -894,7 +1055,7 @@ SplitSpace split_space(int64_t N, int64_t K, const Split& s) {
 // The main kernel over jobs[0 .. count) (count <= MAXE), whose prepared activations start at
 // bsrc[k], with K splits sp[k] and split workspace part[k] / ctr[k].  Parameters are built in a
 // static block under the caller's lock.
-template <int MPAD, int MAXE>
+template <int FMT, int MPAD, int MAXE>
 cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split* sp, float* const* part,
                         unsigned* const* ctr, int count, int M, cudaStream_t stream) {
   static TcParams<MAXE> par;
@@ -902,7 +1063,7 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   par.M = M;
   int tasks = 0;
   for (int k = 0; k < count; ++k) {
-    cudaError_t err = weight_map(jobs[k].W, jobs[k].N, jobs[k].K, &par.maps[k]);
+    cudaError_t err = weight_map(jobs[k].W, jobs[k].N, jobs[k].K, FMT, &par.maps[k]);
     if (err != cudaSuccess) return err;
     const int tiles = (int)((jobs[k].N + kTileRows - 1) / kTileRows);
     par.e[k] = TcEntry{jobs[k].Y, bsrc[k], part[k], ctr[k], (int)jobs[k].N, (int)jobs[k].K,
@@ -910,12 +1071,13 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
     tasks += tiles * sp[k].splits;
   }
   par.tasks_total = tasks;
+  par.aux = jobs[0].aux;
   // Programmatic dependent launch: the kernel may start while the preparation kernel before it
   // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)std::min(tasks, num_sms()));
   cfg.blockDim = dim3(threads(MPAD));
-  cfg.dynamicSmemBytes = TcSmem<MPAD>::kTotal;
+  cfg.dynamicSmemBytes = TcSmem<MPAD, FMT>::kTotal;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -924,17 +1086,17 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   cfg.numAttrs = 1;
   if constexpr (MPAD == 16) {
     if (M <= 8) {
-      cudaError_t err = set_smem_attr<MPAD, 8, MAXE>();
+      cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE>();
       if (err != cudaSuccess) return err;
-      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<MPAD, 8, MAXE>, par);
+      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE>, par);
     }
   }
-  cudaError_t err = set_smem_attr<MPAD, MPAD, MAXE>();
+  cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE>();
   if (err != cudaSuccess) return err;
-  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<MPAD, MPAD, MAXE>, par);
+  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE>, par);
 }
 
-template <int MPAD, int NX>
+template <int MPAD, int NX, bool NAT>
 cudaError_t launch_prep_n(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
                           unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
   static PrepParams<NX> prep;   // built on the host, passed by value at launch
@@ -948,22 +1110,26 @@ cudaError_t launch_prep_n(const std::vector<std::pair<const uint16_t*, int64_t>>
     blocks += (int)(xs[u].second / 256);
   }
   prep.blocks_total = blocks;
-  q4k_xprep_kernel<MPAD, NX><<<blocks, 8 * MPAD, 0, stream>>>(prep);
+  q4k_xprep_kernel<MPAD, NX, NAT><<<blocks, 8 * MPAD, 0, stream>>>(prep);
   return cudaGetLastError();
 }
 
 // The parameter block is copied at every launch: size it to the distinct activations.
-template <int MPAD>
+template <int MPAD, bool NAT>
 cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
                         unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
-  if (xs.size() <= 1) return launch_prep_n<MPAD, 1>(xs, outs, zero, zero_words, M, stream);
-  if (xs.size() <= 16) return launch_prep_n<MPAD, 16>(xs, outs, zero, zero_words, M, stream);
-  return launch_prep_n<MPAD, kMaxPrep>(xs, outs, zero, zero_words, M, stream);
+  if (xs.size() <= 1) return launch_prep_n<MPAD, 1, NAT>(xs, outs, zero, zero_words, M, stream);
+  if constexpr (NAT) {
+    return cudaErrorNotSupported;   // single products only
+  } else {
+    if (xs.size() <= 16) return launch_prep_n<MPAD, 16, NAT>(xs, outs, zero, zero_words, M, stream);
+    return launch_prep_n<MPAD, kMaxPrep, NAT>(xs, outs, zero, zero_words, M, stream);
+  }
 }
 
 // Shared by the workspace and the no-allocation paths: prepare the distinct activations into
 // `prep_base` (laid out by the caller), zero the split counters, and run the main kernel(s).
-template <int MPAD>
+template <int FMT, int MPAD>
 cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
                    const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
                    const std::vector<int>& xidx, const std::vector<Split>& sp, uint8_t* split_base,
@@ -984,18 +1150,22 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
   }
   static std::mutex mu;
   std::lock_guard<std::mutex> g(mu);
-  cudaError_t err = launch_prep<MPAD>(xs, outs, counters, zero_words, M, stream);
+  cudaError_t err = launch_prep<MPAD, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream);
   if (err != cudaSuccess) return err;
-  if (count == 1) return launch_main<MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M, stream);
-  for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
-    err = launch_main<MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, sp.data() + k0, part.data() + k0,
-                                        ctr.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
-    if (err != cudaSuccess) return err;
+  if (count == 1) return launch_main<FMT, MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M, stream);
+  if constexpr (FMT != kFmtQ4K) {
+    return cudaErrorNotSupported;   // the other formats run single products
+  } else {
+    for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
+      err = launch_main<FMT, MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, sp.data() + k0, part.data() + k0,
+                                               ctr.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
+      if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
   }
-  return cudaSuccess;
 }
 
-template <int MPAD>
+template <int FMT, int MPAD>
 cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) {
   static_assert(sizeof(TcParams<kMaxEBatch>) < 32000 && sizeof(PrepParams<kMaxPrep>) < 32000, "kernel parameters too large");
   constexpr int kBB = bblock_bytes(MPAD);
@@ -1033,7 +1203,7 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
   uint8_t* ws = static_cast<uint8_t*>(wsp);
   std::vector<uint8_t*> outs(xs.size());
   for (size_t u = 0; u < xs.size(); ++u) outs[u] = ws + xoff[u];
-  return run_tc<MPAD>(jobs, count, M, stream, xs, outs, xidx, sp, ws + split_off, zero_words);
+  return run_tc<FMT, MPAD>(jobs, count, M, stream, xs, outs, xidx, sp, ws + split_off, zero_words);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1050,7 +1220,7 @@ cudaError_t launch_tc_noalloc_t(const Job& job, int M, cudaStream_t stream, uint
   const std::vector<uint8_t*> outs{scratch};
   const std::vector<int> xidx{0};
   const std::vector<Split> sp{Split{1, (int)(job.K / 256)}};
-  return run_tc<MPAD>(&job, 1, M, stream, xs, outs, xidx, sp, scratch, 0);
+  return run_tc<kFmtQ4K, MPAD>(&job, 1, M, stream, xs, outs, xidx, sp, scratch, 0);
 }
 
 }  // namespace
@@ -1120,7 +1290,18 @@ cudaError_t launch_tc_noalloc(const Job& job, int M, cudaStream_t stream) {
 
 cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream) {
   if (count < 1 || count > kMaxPrep) return cudaErrorInvalidValue;
-  return (M <= 16) ? launch_tc_t<16>(jobs, count, M, stream) : launch_tc_t<32>(jobs, count, M, stream);
+  const int fmt = jobs[0].fmt;
+  for (int k = 1; k < count; ++k)
+    if (jobs[k].fmt != fmt) return cudaErrorInvalidValue;   // one format per launch
+  if (fmt != kFmtQ4K && count != 1) return cudaErrorNotSupported;
+  const bool narrow = M <= 16;
+  switch (fmt) {
+    case kFmtQ4K: return narrow ? launch_tc_t<kFmtQ4K, 16>(jobs, count, M, stream) : launch_tc_t<kFmtQ4K, 32>(jobs, count, M, stream);
+    case kFmtQ5K: return narrow ? launch_tc_t<kFmtQ5K, 16>(jobs, count, M, stream) : launch_tc_t<kFmtQ5K, 32>(jobs, count, M, stream);
+    case kFmtNVFP4: return narrow ? launch_tc_t<kFmtNVFP4, 16>(jobs, count, M, stream) : launch_tc_t<kFmtNVFP4, 32>(jobs, count, M, stream);
+    case kFmtINT4: return narrow ? launch_tc_t<kFmtINT4, 16>(jobs, count, M, stream) : launch_tc_t<kFmtINT4, 32>(jobs, count, M, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace q4k

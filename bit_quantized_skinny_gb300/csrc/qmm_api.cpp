@@ -33,6 +33,8 @@ qmm_status check_shape(int64_t N, int64_t K) {
   return QMM_OK;
 }
 
+bool valid_format(int fmt) { return fmt >= QMM_FMT_Q4K && fmt <= QMM_FMT_INT4; }
+
 qmm_status check_job(const void* W, int64_t N, int64_t K, const uint16_t* X, const float* Y) {
   if (!W || !X || !Y) return QMM_ERR_NULL;
   qmm_status s = check_shape(N, K);
@@ -246,6 +248,47 @@ qmm_status qmm_dequant(const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
   return e == cudaSuccess ? QMM_OK : cuda_fail(e);
 }
 
+size_t qmm_fmt_packed_bytes(int fmt, int64_t N, int64_t K) {
+  if (check_shape(N, K) != QMM_OK) return 0;
+  const int64_t b = q4k::fmt_packed_bytes(fmt, N, K);
+  return b < 0 ? 0 : (size_t)b;
+}
+
+qmm_status qmm_fmt_pack(int fmt, const float* W_host, int64_t N, int64_t K, void* out_host, size_t out_bytes,
+                        int threads) {
+  if (!valid_format(fmt)) return QMM_ERR_FORMAT;
+  if (!W_host || !out_host) return QMM_ERR_NULL;
+  qmm_status s = check_shape(N, K);
+  if (s != QMM_OK) return s;
+  if (out_bytes < qmm_fmt_packed_bytes(fmt, N, K)) return QMM_ERR_BUFSIZE;
+  const int rc = q4k::pack_fmt(fmt, W_host, N, K, static_cast<uint8_t*>(out_host), threads);
+  return rc == 0 ? QMM_OK : QMM_ERR_NONFINITE;
+}
+
+qmm_status qmm_fmt_run(int fmt, const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev, float* Y_dev,
+                       int M, cudaStream_t stream) {
+  if (!valid_format(fmt)) return QMM_ERR_FORMAT;
+  if (fmt == QMM_FMT_Q4K) return qmm_run(Wq_dev, N, K, X_dev, Y_dev, M, stream);
+  qmm_status s = check_job(Wq_dev, N, K, X_dev, Y_dev);
+  if (s != QMM_OK) return s;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  q4k::Job job{Wq_dev, X_dev, Y_dev, N, K};
+  job.fmt = fmt;
+  job.aux = static_cast<const uint8_t*>(Wq_dev) + q4k::fmt_aux_offset(fmt, N, K);
+  cudaError_t e = q4k::launch_tc(&job, 1, M, stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
+qmm_status qmm_fmt_dequant(int fmt, const void* Wq_dev, int64_t N, int64_t K, float* out_dev, cudaStream_t stream) {
+  if (!valid_format(fmt)) return QMM_ERR_FORMAT;
+  if (!Wq_dev || !out_dev) return QMM_ERR_NULL;
+  qmm_status s = check_shape(N, K);
+  if (s != QMM_OK) return s;
+  if (!aligned(Wq_dev, 16) || !aligned(out_dev, 16)) return QMM_ERR_ALIGN;
+  cudaError_t e = q4k::launch_dequant_fmt(fmt, Wq_dev, N, K, out_dev, stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
 int qmm_select_variant(int M, int64_t N, int64_t K) { return select_variant(M, N, K); }
 
 int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M) {
@@ -281,6 +324,7 @@ const char* qmm_strerror(qmm_status status) {
     case QMM_ERR_COUNT: return "batched entry count must be in [1, QMM_MAX_BATCH]";
     case QMM_ERR_VARIANT: return "the requested kernel variant cannot run this shape";
     case QMM_ERR_SCRATCH: return "qmm_run_noalloc: the problem needs more than QMM_NOALLOC_SCRATCH_BYTES of scratch";
+    case QMM_ERR_FORMAT: return "unknown weight format code";
   }
   return "unknown status";
 }

@@ -99,6 +99,187 @@ bool pack_superblock(const float* w, uint8_t* out) {
   return true;
 }
 
+// ---- the other formats -------------------------------------------------------------------
+
+// Q5K super-block (176 bytes): the Q4K header and scale fields, 31 quant levels; the low nibble
+// of weight t at bits 4t of bytes 48.., its high bit in the 32-bit word of its sub-block j at
+// bit 4i + c (t = 32j + 8c + i).
+bool pack_q5k_superblock(const float* w, uint8_t* out) {
+  float step_raw[8], offset_raw[8];
+  for (int j = 0; j < 8; ++j) {
+    const float* s = w + 32 * j;
+    float mn = 0.0f, mx = s[0];
+    for (int t = 0; t < 32; ++t) {
+      mn = (s[t] < mn) ? s[t] : mn;
+      mx = (s[t] > mx) ? s[t] : mx;
+    }
+    step_raw[j] = (mx - mn) / 31.0f;
+    offset_raw[j] = 0.0f - mn;
+  }
+  float step_max = 0.0f, offset_max = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    step_max = std::max(step_max, step_raw[j]);
+    offset_max = std::max(offset_max, offset_raw[j]);
+  }
+  uint16_t d_bits = 0, dmin_bits = 0;
+  bool ovf_d = false, ovf_m = false;
+  const float D = to_half_and_back(step_max / 63.0f, &d_bits, &ovf_d);
+  const float Dm = to_half_and_back(offset_max / 63.0f, &dmin_bits, &ovf_m);
+  if (ovf_d || ovf_m) return false;
+  std::memset(out, 0, 176);
+  out[0] = (uint8_t)(d_bits & 0xFF);
+  out[1] = (uint8_t)(d_bits >> 8);
+  out[2] = (uint8_t)(dmin_bits & 0xFF);
+  out[3] = (uint8_t)(dmin_bits >> 8);
+  uint64_t f_lo = 0, f_hi = 0;
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t sc = (D > 0.0f) ? level(step_raw[j] / D, 63.0f) : 0u;
+    const uint32_t mn = (Dm > 0.0f) ? level(offset_raw[j] / Dm, 63.0f) : 0u;
+    const uint64_t g = (uint64_t)(sc | (mn << 6));
+    const int bit = 12 * j;
+    if (bit + 12 <= 64) {
+      f_lo |= g << bit;
+    } else if (bit >= 64) {
+      f_hi |= g << (bit - 64);
+    } else {
+      f_lo |= g << bit;
+      f_hi |= g >> (64 - bit);
+    }
+    const float step = D * static_cast<float>(sc);
+    const float off = Dm * static_cast<float>(mn);
+    uint32_t hi_word = 0;
+    for (int u = 0; u < 32; ++u) {
+      const int t = 32 * j + u;
+      const uint32_t q = step > 0.0f ? level((w[t] + off) / step, 31.0f) : 0u;
+      out[48 + t / 2] |= (uint8_t)((q & 15u) << (4 * (t & 1)));
+      hi_word |= (q >> 4) << (4 * (u & 7) + (u >> 3));
+    }
+    for (int b = 0; b < 4; ++b) out[16 + 4 * j + b] = (uint8_t)(hi_word >> (8 * b));
+  }
+  for (int b = 0; b < 8; ++b) out[4 + b] = (uint8_t)(f_lo >> (8 * b));
+  for (int b = 0; b < 4; ++b) out[12 + b] = (uint8_t)(f_hi >> (8 * b));
+  return true;
+}
+
+// E4M3 (bias 7, 3 fraction bits, largest finite 448) of a non-negative finite value: round to
+// nearest even on the format's grid, clamped to 448.
+uint8_t e4m3_code(float x) {
+  if (!(x > 0.0f)) return 0;
+  if (x >= 448.0f) return 0x7E;
+  int e = 0;
+  std::frexp(x, &e);                       // x = m 2^e, m in [0.5, 1)
+  const int E = e - 1;                     // floor(log2 x)
+  const int qe = E < -6 ? -9 : E - 3;      // grid spacing: 2^-9 below 2^-6, else 2^(E-3)
+  const float r = std::ldexp(std::rint(std::ldexp(x, -qe)), qe);
+  if (r >= 448.0f) return 0x7E;
+  if (r < 0.015625f) return (uint8_t)std::ldexp(r, 9);   // subnormal: r / 2^-9
+  int e2 = 0;
+  std::frexp(r, &e2);
+  const int E2 = e2 - 1;
+  const int f = (int)(std::ldexp(r, 3 - E2)) - 8;
+  return (uint8_t)(((E2 + 7) << 3) | f);
+}
+
+float e4m3_float(uint8_t c) {
+  const int e = (c >> 3) & 15, f = c & 7;
+  const float v = e == 0 ? std::ldexp((float)f, -9) : std::ldexp((float)(8 + f), e - 10);
+  return (c & 0x80) ? -v : v;
+}
+
+// E2M1 (bias 1, 1 fraction bit, largest 6) of a finite value: nearest even magnitude, clamped
+// to 6, the sign bit of x kept.
+uint8_t e2m1_code(float x) {
+  const float a = std::fabs(x);
+  uint8_t c = 7;
+  if (a < 6.0f) {
+    int e = 0;
+    std::frexp(a, &e);
+    const int E = a > 0.0f ? e - 1 : -1;
+    const int qe = E < 0 ? -1 : E - 1;     // spacing 0.5 below 1, else 2^(E-1)
+    const float r = std::ldexp(std::rint(std::ldexp(a, -qe)), qe);
+    if (r < 1.0f) {
+      c = (uint8_t)(r * 2.0f);
+    } else {
+      int e2 = 0;
+      std::frexp(r, &e2);
+      const int E2 = e2 - 1;
+      c = (uint8_t)(((E2 + 1) << 1) | ((int)std::ldexp(r, 1 - E2) - 2));
+    }
+  }
+  return std::signbit(x) ? (uint8_t)(c | 8u) : c;
+}
+
+// NVFP4 block (144 bytes): 16 E4M3 scales, then the E2M1 codes of the 256 weights (low nibble
+// first), against the tensor scale g.
+void pack_nvfp4_superblock(const float* w, float g, uint8_t* out) {
+  std::memset(out, 0, 144);
+  for (int b = 0; b < 16; ++b) {
+    float a = 0.0f;
+    for (int t = 16 * b; t < 16 * b + 16; ++t) a = std::max(a, std::fabs(w[t]));
+    const float r = (a / 6.0f) / g;
+    const uint8_t s = e4m3_code(r);
+    out[b] = s;
+    const float S = e4m3_float(s) * g;
+    for (int t = 16 * b; t < 16 * b + 16; ++t) {
+      const uint8_t c = S > 0.0f ? e2m1_code(w[t] / S) : 0;
+      out[16 + t / 2] |= (uint8_t)(c << (4 * (t & 1)));
+    }
+  }
+}
+
+// INT4 row: K/2 bytes of two's-complement quants (low nibble first) and K/128 binary16 scales.
+bool pack_int4_row(const float* w, int64_t K, uint8_t* q, uint8_t* scales) {
+  for (int64_t g = 0; g < K / 128; ++g) {
+    const float* s = w + 128 * g;
+    float a = 0.0f;
+    for (int t = 0; t < 128; ++t) a = std::max(a, std::fabs(s[t]));
+    uint16_t bits = 0;
+    bool ovf = false;
+    const float S = to_half_and_back(a / 7.0f, &bits, &ovf);
+    if (ovf) return false;
+    scales[2 * g] = (uint8_t)(bits & 0xFF);
+    scales[2 * g + 1] = (uint8_t)(bits >> 8);
+    for (int t = 0; t < 128; t += 2) {
+      int v[2] = {0, 0};
+      for (int u = 0; u < 2; ++u) {
+        if (S > 0.0f) {
+          const float r = std::rint(s[t + u] / S);
+          v[u] = (int)(r < -8.0f ? -8.0f : (r > 7.0f ? 7.0f : r));
+        }
+      }
+      q[64 * g + t / 2] = (uint8_t)((v[0] & 15) | ((v[1] & 15) << 4));
+    }
+  }
+  return true;
+}
+
+// Rows [0, N) split over up to `threads` threads; fn(n) packs row n and returns false on error.
+template <class Fn>
+int for_rows(int64_t N, int threads, Fn fn) {
+  int nthr = threads > 0 ? threads : (int)std::thread::hardware_concurrency();
+  if (nthr < 1) nthr = 1;
+  nthr = (int)std::min<int64_t>(nthr, N);
+  std::vector<int> status(nthr, 0);
+  auto work = [&](int tid) {
+    const int64_t r0 = N * tid / nthr, r1 = N * (tid + 1) / nthr;
+    for (int64_t n = r0; n < r1; ++n)
+      if (!fn(n)) {
+        status[tid] = 6;
+        return;
+      }
+  };
+  if (nthr == 1) {
+    work(0);
+  } else {
+    std::vector<std::thread> pool;
+    for (int t = 0; t < nthr; ++t) pool.emplace_back(work, t);
+    for (auto& th : pool) th.join();
+  }
+  for (int st : status)
+    if (st) return st;
+  return 0;
+}
+
 }  // namespace
 
 int pack_q4k(const float* W, int64_t N, int64_t K, uint8_t* out, int threads) {
@@ -129,6 +310,58 @@ int pack_q4k(const float* W, int64_t N, int64_t K, uint8_t* out, int threads) {
   for (int s : status)
     if (s) return s;
   return 0;
+}
+
+int64_t fmt_packed_bytes(int fmt, int64_t N, int64_t K) {
+  switch (fmt) {
+    case kFmtQ4K: return N * (K / 256) * 144;
+    case kFmtQ5K: return N * (K / 256) * 176;
+    case kFmtNVFP4: return N * (K / 256) * 144 + 16;
+    case kFmtINT4: return N * (K / 2) + N * (K / 128) * 2;
+    default: return -1;
+  }
+}
+
+int64_t fmt_aux_offset(int fmt, int64_t N, int64_t K) {
+  if (fmt == kFmtNVFP4) return N * (K / 256) * 144;
+  if (fmt == kFmtINT4) return N * (K / 2);
+  return 0;
+}
+
+int pack_fmt(int fmt, const float* W, int64_t N, int64_t K, uint8_t* out, int threads) {
+  if (fmt == kFmtQ4K) return pack_q4k(W, N, K, out, threads);
+  const int64_t nb = K / 256;
+  for (int64_t e = 0; e < N * K; ++e)
+    if (!std::isfinite(W[e])) return 6;
+  if (fmt == kFmtQ5K)
+    return for_rows(N, threads, [&](int64_t n) {
+      for (int64_t b = 0; b < nb; ++b)
+        if (!pack_q5k_superblock(W + n * K + b * 256, out + (n * nb + b) * 176)) return false;
+      return true;
+    });
+  if (fmt == kFmtNVFP4) {
+    float amax = 0.0f;
+    for (int64_t e = 0; e < N * K; ++e) amax = std::max(amax, std::fabs(W[e]));
+    float g = amax / 2688.0f;   // 6 x 448: the largest E2M1 value times the largest E4M3 value
+    if (!(g > 0.0f)) g = 1.0f;
+    const int rc = for_rows(N, threads, [&](int64_t n) {
+      for (int64_t b = 0; b < nb; ++b) pack_nvfp4_superblock(W + n * K + b * 256, g, out + (n * nb + b) * 144);
+      return true;
+    });
+    uint8_t* tr = out + fmt_aux_offset(fmt, N, K);
+    std::memset(tr, 0, 16);
+    uint32_t gb = 0;
+    std::memcpy(&gb, &g, 4);
+    for (int b = 0; b < 4; ++b) tr[b] = (uint8_t)(gb >> (8 * b));
+    return rc;
+  }
+  if (fmt == kFmtINT4) {
+    uint8_t* scales = out + fmt_aux_offset(fmt, N, K);
+    return for_rows(N, threads, [&](int64_t n) {
+      return pack_int4_row(W + n * K, K, out + n * (K / 2), scales + n * (K / 128) * 2);
+    });
+  }
+  return 2;
 }
 
 }  // namespace q4k

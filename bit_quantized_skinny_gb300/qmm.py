@@ -24,13 +24,17 @@ VARIANT_NAMES = {VARIANT_FMA: "fma", VARIANT_TC: "tc"}
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANGE",
           4: "QMM_ERR_ALIGN", 5: "QMM_ERR_BUFSIZE", 6: "QMM_ERR_NONFINITE", 7: "QMM_ERR_CUDA",
-          8: "QMM_ERR_COUNT", 9: "QMM_ERR_VARIANT", 10: "QMM_ERR_SCRATCH"}
+          8: "QMM_ERR_COUNT", 9: "QMM_ERR_VARIANT", 10: "QMM_ERR_SCRATCH", 11: "QMM_ERR_FORMAT"}
+
+FMT_Q4K, FMT_Q5K, FMT_NVFP4, FMT_INT4 = 0, 1, 2, 3
+FORMATS = {"q4k": FMT_Q4K, "q5k": FMT_Q5K, "nvfp4": FMT_NVFP4, "int4": FMT_INT4}
 
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
            "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
-           "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed"]
+           "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed",
+           "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -89,6 +93,14 @@ def load(path: str | None = None):
     lib.qmm_run_indexed.argtypes = [ctypes.POINTER(vp), i32, i64, i64, ctypes.POINTER(ctypes.c_int32), vp, vp, i32,
                                     vp, ctypes.c_size_t, vp]
     lib.qmm_run_indexed.restype = i32
+    lib.qmm_fmt_packed_bytes.argtypes = [i32, i64, i64]
+    lib.qmm_fmt_packed_bytes.restype = ctypes.c_size_t
+    lib.qmm_fmt_pack.argtypes = [i32, vp, i64, i64, vp, ctypes.c_size_t, i32]
+    lib.qmm_fmt_pack.restype = i32
+    lib.qmm_fmt_run.argtypes = [i32, vp, i64, i64, vp, vp, i32, vp]
+    lib.qmm_fmt_run.restype = i32
+    lib.qmm_fmt_dequant.argtypes = [i32, vp, i64, i64, vp, vp]
+    lib.qmm_fmt_dequant.restype = i32
     lib.qmm_device_status.argtypes = [ctypes.POINTER(u32)]
     lib.qmm_device_status.restype = i32
     lib.qmm_strerror.argtypes = [i32]
@@ -208,6 +220,37 @@ def run_indexed(experts, N: int, K: int, ids, X, Y, workspace, stream=None):
 def dequant(Wq, N: int, K: int, out, stream=None):
     _check(load().qmm_dequant(ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(out.data_ptr()),
                               _stream_handle(stream)), "qmm_dequant")
+
+
+def fmt_packed_bytes(fmt: int, N: int, K: int) -> int:
+    return load().qmm_fmt_packed_bytes(fmt, N, K)
+
+
+def fmt_pack(fmt: int, W: np.ndarray, threads: int = 0) -> np.ndarray:
+    """Pack an N x K fp32 host array into weight format `fmt` (host, multi-threaded)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    nbytes = fmt_packed_bytes(fmt, N, K)
+    if nbytes == 0:
+        raise QmmError(2, "qmm_fmt_pack")
+    out = np.empty(nbytes, dtype=np.uint8)
+    _check(load().qmm_fmt_pack(fmt, W.ctypes.data_as(ctypes.c_void_p), N, K, out.ctypes.data_as(ctypes.c_void_p),
+                               out.nbytes, threads), "qmm_fmt_pack")
+    return out
+
+
+def fmt_run(fmt: int, Wq, N: int, K: int, X, Y, M: int | None = None, stream=None):
+    """Y[M x N] = X[M x K] * dequant(Wq)^T for weights in format `fmt`, on the GPU."""
+    if M is None:
+        M = X.shape[0]
+    st = load().qmm_fmt_run(fmt, ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()),
+                            ctypes.c_void_p(Y.data_ptr()), M, _stream_handle(stream))
+    _check(st, "qmm_fmt_run")
+
+
+def fmt_dequant(fmt: int, Wq, N: int, K: int, out, stream=None):
+    _check(load().qmm_fmt_dequant(fmt, ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(out.data_ptr()),
+                                  _stream_handle(stream)), "qmm_fmt_dequant")
 
 
 def select_variant(M: int, N: int, K: int) -> int:

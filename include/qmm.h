@@ -95,7 +95,8 @@ typedef enum {
   QMM_ERR_CUDA = 7,       /* a CUDA runtime call or kernel launch failed                   */
   QMM_ERR_COUNT = 8,      /* qmm_run_batched: count outside [1, QMM_MAX_BATCH]              */
   QMM_ERR_VARIANT = 9,    /* an explicitly requested kernel variant cannot run this shape  */
-  QMM_ERR_SCRATCH = 10    /* qmm_run_noalloc: problem larger than its fixed device buffer  */
+  QMM_ERR_SCRATCH = 10,   /* qmm_run_noalloc: problem larger than its fixed device buffer  */
+  QMM_ERR_FORMAT = 11     /* qmm_fmt_*: unknown weight format code                         */
 } qmm_status;
 
 /* Bytes of the packed form of an N x K weight matrix: N * (K/256) * 144.
@@ -225,6 +226,71 @@ size_t qmm_indexed_workspace_bytes(int M, int64_t N, int64_t K);
 qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64_t N, int64_t K,
                            const int32_t* ids_host, const uint16_t* X_dev, float* Y_dev, int M,
                            void* workspace_dev, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Other weight formats.  The pages run Q4_K_M files, which mix k-quant widths ("sixi-asi 0.9",
+ * section "Numbers"), and weigh two other 4-bit layouts: NVFP4 W4A16 weights on Blackwell
+ * tensor cores (FlashRT issue #153: the NVFP4 W4A16 GEMM is most of the decode time; "sixi-asi
+ * 0.9", section "What I got wrong in 0.8": block-scaled FP4 reached through tcgen05) and plain
+ * 4-bit integers with one scale per 128 columns ("sixi-asi 0.11", section "What did not work").
+ * None prints a byte layout; these are this library's.  Every weight below is one IEEE
+ * rounding of an exact number, and qmm_fmt_dequant returns it bit for bit.
+ *
+ *   QMM_FMT_Q4K   the Q4K format above.
+ *   QMM_FMT_Q5K   176 bytes per super-block of 256 weights of a row (rows one after another):
+ *                 bytes [0, 16) as in Q4K (d, dmin, the 96-bit F of (sc_j, m_j));
+ *                 bytes [16, 48) eight 32-bit little-endian words, word j the high bits of
+ *                 sub-block j: weight t = 32j + 8c + i (c = 0..3, i = 0..7) has its high bit
+ *                 at bit 4i + c (the layout the decode reads in one shift per pair);
+ *                 bytes [48, 176) the low 4 bits of weight t at bits [4t, 4t+4), as Q4K.
+ *                 q_t = low + 16 high (0..31); weight = RN32(d*sc_j*q_t - dmin*m_j).
+ *   QMM_FMT_NVFP4 144 bytes per 256 weights: bytes [0, 16) sixteen E4M3 scales (sign, 4
+ *                 exponent bits with bias 7, 3 fraction bits; largest 448), s_b for weights
+ *                 16b .. 16b+15; bytes [16, 144) the E2M1 codes (sign, 2 exponent bits with
+ *                 bias 1, 1 fraction bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6) of weight t at bits
+ *                 [4t, 4t+4).  After all N rows: a 16-byte trailer, the binary32 tensor scale
+ *                 g then 12 zero bytes.  weight = RN32(g * s_b * v_t).
+ *   QMM_FMT_INT4  a quant plane of N rows of K/2 bytes (weight k of a row: the two's-complement
+ *                 4-bit integer at bits [4k, 4k+4) of the row), then at byte N*K/2 a scale
+ *                 plane of N x K/128 binary16 scales, row-major; weight = s * q (exact).
+ *
+ * Packers (plain rules; binary32 arithmetic, one rounding per operation):
+ *   Q5K   the Q4K rule with 31 levels: scale_j = (hi_j - lo_j)/31, q clamped to [0, 31].
+ *   NVFP4 g = max|w| / 2688 (6 * 448; 1 if that is not positive); per 16 weights
+ *         s = E4M3(max|w| / 6 / g), round to nearest even, clamped to 448; S = s * g;
+ *         v = E2M1(w / S), nearest even, clamped to 6, sign kept (S = 0: v = +0).
+ *   INT4  per 128 weights s = binary16(max|w| / 7); q = S > 0 ? clamp(rint(w / S), -8, 7) : 0
+ *         (S = the value of s).
+ *
+ * The products run on the tensor cores (one launch per call; the CUDA-core kernel is Q4K's);
+ * the other conventions are those of qmm_run.  Shapes: as for Q4K (K % 256 == 0). */
+typedef enum {
+  QMM_FMT_Q4K = 0,
+  QMM_FMT_Q5K = 1,
+  QMM_FMT_NVFP4 = 2,
+  QMM_FMT_INT4 = 3
+} qmm_format;
+
+/* Bytes of the packed form of an N x K matrix in format fmt (0 for an invalid shape or
+ * format): Q4K N*(K/256)*144, Q5K N*(K/256)*176, NVFP4 N*(K/256)*144 + 16,
+ * INT4 N*K/2 + N*(K/128)*2. */
+size_t qmm_fmt_packed_bytes(int fmt, int64_t N, int64_t K);
+
+/* Pack W_host (N x K row-major fp32, host) into format fmt, as qmm_pack does for Q4K.
+ * Errors: QMM_ERR_FORMAT, QMM_ERR_NULL, QMM_ERR_SHAPE, QMM_ERR_BUFSIZE, QMM_ERR_NONFINITE. */
+qmm_status qmm_fmt_pack(int fmt, const float* W_host, int64_t N, int64_t K, void* out_host,
+                        size_t out_bytes, int threads);
+
+/* Y_dev[M x N] = X_dev[M x K] * dequant(Wq_dev)^T for weights packed in format fmt
+ * (qmm_fmt_packed_bytes(fmt, N, K) bytes on the device, 16-byte aligned).  QMM_FMT_Q4K is
+ * qmm_run.  Errors as qmm_run, and QMM_ERR_FORMAT. */
+qmm_status qmm_fmt_run(int fmt, const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
+                       float* Y_dev, int M, cudaStream_t stream);
+
+/* Test hook: out_dev[N x K] = the dequantized weights of format fmt, computed on the device
+ * with the decode steps of the product kernel.  Bit-exact to the definitions above. */
+qmm_status qmm_fmt_dequant(int fmt, const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
+                           cudaStream_t stream);
 
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the

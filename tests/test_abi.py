@@ -95,3 +95,71 @@ def test_pack_errors(qmm):
     small = np.zeros(10, np.uint8)
     assert lib.qmm_pack(W.ctypes.data_as(ctypes.c_void_p), 2, 256,
                         small.ctypes.data_as(ctypes.c_void_p), small.nbytes, 1) == 5
+
+
+# ---------------------------------------------------------------- other weight formats ----
+
+FMTS = ["q5k", "nvfp4", "int4"]
+
+
+def test_fmt_packed_bytes(qmm):
+    assert qmm.fmt_packed_bytes(qmm.FMT_Q4K, 34816, 5120) == 100_270_080
+    assert qmm.fmt_packed_bytes(qmm.FMT_Q5K, 34816, 5120) == 34816 * 20 * 176
+    assert qmm.fmt_packed_bytes(qmm.FMT_NVFP4, 34816, 5120) == 100_270_080 + 16
+    assert qmm.fmt_packed_bytes(qmm.FMT_INT4, 34816, 5120) == 34816 * 2560 + 34816 * 40 * 2
+    assert qmm.fmt_packed_bytes(9, 4, 256) == 0
+    assert qmm.fmt_packed_bytes(qmm.FMT_INT4, 4, 255) == 0
+
+
+@pytest.mark.parametrize("fmt_name", FMTS)
+@pytest.mark.parametrize("shape", [(37, 2304), (5, 256), (64, 5120)])
+def test_fmt_pack_equals_oracle_pack(qmm, oracle_lib, fmt_name, shape):
+    N, K = shape
+    fmt = qmm.FORMATS[fmt_name]
+    W = inputs.weights_f32(N, K, 200 + N)
+    ref = oracle_lib.fmt_pack(oracle_lib.FORMATS[fmt_name], W)
+    assert np.array_equal(qmm.fmt_pack(fmt, W), ref)
+    assert np.array_equal(qmm.fmt_pack(fmt, W, threads=3), ref)
+
+
+@pytest.mark.parametrize("fmt_name", FMTS)
+def test_fmt_pack_equals_oracle_on_awkward_values(qmm, oracle_lib, fmt_name):
+    rng = np.random.default_rng(19)
+    W = (rng.standard_normal((24, 768)) * np.exp(rng.uniform(-12, 6, (24, 1)))).astype(np.float32)
+    W[0, :256] = 0.0
+    W[1, :256] = -0.0
+    W[2, :256] = 3.0
+    W[3, :256] = -3.0
+    W[4, 0:32] = np.linspace(-1, 1, 32, dtype=np.float32)
+    W[5, :] = np.float32(1e-30)
+    W[6, :] = np.float32(-7e-6)
+    W[7, :] = np.float32(6e4)
+    for sub in (W, W[:1] * 0):    # also an all-zero matrix (NVFP4 tensor scale 1)
+        ref = oracle_lib.fmt_pack(oracle_lib.FORMATS[fmt_name], sub)
+        assert np.array_equal(qmm.fmt_pack(qmm.FORMATS[fmt_name], sub), ref)
+
+
+def test_fmt_argument_errors_need_no_gpu(qmm):
+    lib = qmm.load()
+    p = ctypes.c_void_p(16)
+    assert lib.qmm_fmt_run(7, p, 4, 256, p, p, 1, None) == 11
+    assert lib.qmm_fmt_run(-1, p, 4, 256, p, p, 1, None) == 11
+    assert lib.qmm_fmt_run(qmm.FMT_NVFP4, None, 4, 256, p, p, 1, None) == 1
+    assert lib.qmm_fmt_run(qmm.FMT_INT4, p, 4, 255, p, p, 1, None) == 2
+    assert lib.qmm_fmt_run(qmm.FMT_Q5K, p, 4, 256, p, p, 33, None) == 3
+    assert lib.qmm_fmt_run(qmm.FMT_Q5K, ctypes.c_void_p(24), 4, 256, p, p, 1, None) == 4
+    assert lib.qmm_fmt_dequant(4, p, 4, 256, p, None) == 11
+    assert lib.qmm_fmt_dequant(qmm.FMT_INT4, p, 4, 100, p, None) == 2
+    W = np.zeros((2, 256), np.float32)
+    W[0, 1] = np.inf
+    for fmt in (qmm.FMT_Q5K, qmm.FMT_NVFP4, qmm.FMT_INT4):
+        with pytest.raises(qmm.QmmError) as e:
+            qmm.fmt_pack(fmt, W)
+        assert e.value.status == 6
+    small = np.zeros(10, np.uint8)
+    W[0, 1] = 0
+    assert lib.qmm_fmt_pack(qmm.FMT_INT4, W.ctypes.data_as(ctypes.c_void_p), 2, 256,
+                            small.ctypes.data_as(ctypes.c_void_p), small.nbytes, 1) == 5
+    assert lib.qmm_fmt_pack(5, W.ctypes.data_as(ctypes.c_void_p), 2, 256,
+                            small.ctypes.data_as(ctypes.c_void_p), small.nbytes, 1) == 11
+    assert lib.qmm_strerror(11) == b"unknown weight format code"
