@@ -497,6 +497,54 @@ def run_indexed(args):
                       "l2": f"expert sets cycled over copies >= 4x L2 ({l2 >> 20} MB)", "per_M": res}), flush=True)
 
 
+def run_formats(args):
+    """The other weight formats (Q5K, NVFP4 W4A16, INT4 with one scale per 128 columns) next
+    to Q4K on the same tensor-core kernel: one product per launch, per format x shape x M,
+    weights cycled over copies totalling more than 4x L2.  GB/s counts each format's packed
+    bytes (its weight stream: what the launch must read).  Prints one JSON line."""
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, inputs, qmm, workloads
+
+    build_lib.build()
+    qmm.load()
+    torch.cuda.set_device(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    peak, _ = hbm_peak()
+    names = ["gate_up", "down", "q", "lm_head"] if args.formats == "all" else args.formats.split(",")
+    stream = torch.cuda.current_stream()
+    results = {}
+    fmts = qmm.FORMATS if not args.fmt else {k: qmm.FORMATS[k] for k in args.fmt.split(",")}
+    for fname, fmt in fmts.items():
+        per_shape = {}
+        for name in names:
+            N, K = SINGLE_SHAPES[name]
+            Wd = workloads.packed_weights_fmt(fmt, N, K, inputs.seed_for(3, list(SINGLE_SHAPES).index(name)))
+            copies = max(1, -(-4 * l2 // Wd.numel()))
+            ws = [Wd] + [Wd.clone() for _ in range(copies - 1)]
+            res = {}
+            for M in args.Ms:
+                X, _ = workloads.activations(M, K, inputs.seed_for(3, 50 + M), device="cuda")
+                Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+                if fmt == qmm.FMT_Q4K:   # the same tensor-core kernel as the other formats
+                    fn = lambda: [qmm.run(w, N, K, X, Y, M=M, variant=qmm.VARIANT_TC) for w in ws]
+                else:
+                    fn = lambda: [qmm.fmt_run(fmt, w, N, K, X, Y, M=M) for w in ws]
+                ms = time_steps(fn, max(2, args.steps // 5), 3, stream, lambda: None) / len(ws)
+                gbps = weight_gbps(Wd.numel(), ms)
+                res[str(M)] = {"us": round(ms * 1e3, 2), "gbps": round(gbps, 1),
+                               "frac_of_measured_hbm": round(gbps / peak, 3)}
+                if qmm.device_status() != 0:
+                    raise RuntimeError("kernel reported a device-side error")
+            per_shape[name] = {"N": N, "K": K, "weight_bytes": Wd.numel(),
+                               "bits_per_weight": round(8 * Wd.numel() / (N * K), 4), "per_M": res}
+            del ws, Wd
+            torch.cuda.empty_cache()
+        results[fname] = per_shape
+    print(json.dumps({"metric": "weight-read GB/s per single product, by weight format", "unit": UNIT,
+                      "peak_gbps": peak, "l2": f"weights cycled over copies >= 4x L2 ({l2 >> 20} MB)",
+                      "formats": results}), flush=True)
+
+
 def run_reference(args, rank: int):
     """The oracle (plain fp64 C, host cores) on a bounded sample of the same workload."""
     if rank != 0:
@@ -567,6 +615,9 @@ def main(argv=None):
     ap.add_argument("--variant", choices=["fma", "tc", "auto", "both"], default="both")
     ap.add_argument("--ffn", action="store_true", help="time one feed-forward block per call instead")
     ap.add_argument("--indexed", action="store_true", help="time the indexed-expert product instead")
+    ap.add_argument("--fmt", default=None, help="with --formats: only these formats (comma list)")
+    ap.add_argument("--formats", default=None,
+                    help="time the weight formats on these shapes instead (comma list of gate_up,down,q,k,lm_head or 'all')")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -588,6 +639,10 @@ def main(argv=None):
     if args.indexed:
         if rank == 0:
             run_indexed(args)
+        return
+    if args.formats:
+        if rank == 0:
+            run_formats(args)
         return
     dist_ok = False
     if world > 1:

@@ -143,30 +143,35 @@ enum : int {
   kNumBars = kBarDrain + 1
 };
 
-// Mpad 32: each group's running sum of chunk sums (32 tokens x 128 rows of fp32) lives in
-// shared memory, not in registers.
-__host__ __device__ constexpr int ytot_bytes(int mpad) { return mpad == 32 ? groups(mpad) * 32 * kTileRows * 4 : 0; }
-// Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest.
-__host__ __device__ constexpr int stages(int mpad, int f) {
-  return (mpad <= 16 ? 8 : 5) < (kSmemLimit - ytot_bytes(mpad) - kNumBars * 8 - 32) / stage_bytes(mpad, f)
-             ? (mpad <= 16 ? 8 : 5)
-             : (kSmemLimit - ytot_bytes(mpad) - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+// With 16 or 32 token columns each group's running sum of chunk sums (MT tokens x 128 rows of
+// fp32) lives in shared memory, not in registers (there it spilled); it is touched once per
+// chunk of 4 super-blocks.
+__host__ __device__ constexpr int ytot_bytes(int mpad, int mt) { return mt >= 16 ? groups(mpad) * mt * kTileRows * 4 : 0; }
+// Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens).
+__host__ __device__ constexpr int stages_fit(int mpad, int f, int mt) {
+  return (kSmemLimit - ytot_bytes(mpad, mt) - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+}
+__host__ __device__ constexpr int stages(int mpad, int f, int mt) {
+  return stages_fit(mpad, f, mt) < (mpad <= 16 ? 8 : 5) ? stages_fit(mpad, f, mt) : (mpad <= 16 ? 8 : 5);
 }
 
-template <int MPAD, int FMT>
+template <int MPAD, int FMT, int MT>
 struct TcSmem {
   static constexpr int kW = 0;
-  static constexpr int kYtot = kW + stages(MPAD, FMT) * stage_bytes(MPAD, FMT);
-  static constexpr int kBars = kYtot + ytot_bytes(MPAD);
+  static constexpr int kYtot = kW + stages(MPAD, FMT, MT) * stage_bytes(MPAD, FMT);
+  static constexpr int kBars = kYtot + ytot_bytes(MPAD, MT);
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
-static_assert(TcSmem<16, kFmtQ4K>::kTotal <= kSmemLimit && TcSmem<32, kFmtQ4K>::kTotal <= kSmemLimit &&
-              TcSmem<16, kFmtQ5K>::kTotal <= kSmemLimit && TcSmem<32, kFmtQ5K>::kTotal <= kSmemLimit &&
-              TcSmem<16, kFmtINT4>::kTotal <= kSmemLimit && TcSmem<32, kFmtINT4>::kTotal <= kSmemLimit,
+template <int FMT>
+constexpr bool smem_fits() {
+  return TcSmem<16, FMT, 8>::kTotal <= kSmemLimit && TcSmem<16, FMT, 16>::kTotal <= kSmemLimit &&
+         TcSmem<32, FMT, 32>::kTotal <= kSmemLimit;
+}
+static_assert(smem_fits<kFmtQ4K>() && smem_fits<kFmtQ5K>() && smem_fits<kFmtNVFP4>() && smem_fits<kFmtINT4>(),
               "shared memory");
-static_assert(stages(16, kFmtQ4K) == 8 && stages(32, kFmtQ4K) == 5 && stages(16, kFmtQ5K) >= 4 &&
-              stages(32, kFmtQ5K) >= 3 && stages(16, kFmtINT4) >= 4 && stages(32, kFmtINT4) >= 3,
+static_assert(stages(16, kFmtQ4K, 8) == 8 && stages(16, kFmtQ4K, 16) == 7 && stages(32, kFmtQ4K, 32) == 5 &&
+              stages(16, kFmtQ5K, 16) >= 4 && stages(32, kFmtQ5K, 32) >= 3 && stages(32, kFmtINT4, 32) >= 3,
               "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
 static_assert(stage_bytes(16, kFmtQ4K) % 128 == 0 && stage_bytes(32, kFmtQ5K) % 128 == 0 &&
@@ -413,12 +418,15 @@ struct HalfIn {
 };
 
 // INT4 tiles are copied with the 128-byte swizzle: 16-byte chunk c of row r sits at chunk
-// c ^ (r % 8) of the row (spreads the rows' reads over all shared-memory banks).
+// c ^ (r % 8) of the row (spreads the rows' reads over all shared-memory banks).  The stage is
+// 1024-byte aligned and a row is 128 bytes, so r % 8 is bits 7..9 of the row's address rb:
+// chunk c is at (rb ^ ((rb >> 3) & 0x70)) ^ 16c.
 template <int FMT>
-__device__ __forceinline__ void load_half(HalfIn<FMT>& in, uint32_t rb, int h, int r) {
+__device__ __forceinline__ void load_half(HalfIn<FMT>& in, uint32_t rb, int h) {
   if constexpr (FMT == kFmtINT4) {
+    const uint32_t rbs = rb ^ ((rb >> 3) & 0x70u);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 16u * (uint32_t)((4 * h + k) ^ (r & 7)));
+    for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rbs ^ (uint32_t)(16 * (4 * h + k)));
   } else if constexpr (FMT == kFmtQ5K) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 48 + 64 * h + 16 * k);
@@ -534,12 +542,12 @@ template <int FMT, int MPAD, int MT, int MAXE>
 __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
-  using L = TcSmem<MPAD, FMT>;
+  using L = TcSmem<MPAD, FMT, MT>;
   constexpr int NG = groups(MPAD);
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
   constexpr int kMmaWarp = kProdWarp + 1;       // MMA issue; owns TMEM
   constexpr int kBB = bblock_bytes(MPAD);
-  constexpr int kS = stages(MPAD, FMT);
+  constexpr int kS = stages(MPAD, FMT, MT);
   constexpr int kSB = stage_bytes(MPAD, FMT);
   constexpr int kBlk = blk_bytes(FMT);
   constexpr int kWSB = w_stage_bytes(FMT);
@@ -704,7 +712,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     for (int k = 0; k < MT; ++k) y[k] = 0.f;
     // the task's running sum of chunk sums: registers, or shared memory (token k at [k * 128])
     // for 32 tokens
-    constexpr bool kYtotSmem = MT == 32;
+    constexpr bool kYtotSmem = MT >= 16;
     float ytot_r[kYtotSmem ? 1 : MT];
     float* ytot_s = reinterpret_cast<float*>(smem + L::kYtot) + (size_t)grp * MT * kTileRows + r;
 #pragma unroll
@@ -726,16 +734,6 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     uint4 hd_n = make_uint4(0, 0, 0, 0);
     float sigma_n = 0.f;
     for (int i = 0; cur.t >= 0; ++i) {
-      // INT4: the scales of this row's two K halves, from the scale plane (read early: they are
-      // needed only by the epilogue)
-      uint32_t int4_scales = 0;
-      if constexpr (FMT == kFmtINT4) {
-        const TcEntry& E0 = P.e[cur.e];
-        const int row0 = cur.tile * kTileRows + r;
-        if (row0 < E0.N)
-          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux) +
-                                                                (int64_t)row0 * (E0.K >> 7)) + cur.sb);
-      }
       uint32_t ws;
       uint4 hd;
       float sigma;
@@ -760,7 +758,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         HalfIn<FMT> in;
-        load_half<FMT>(in, rb, h, r);
+        load_half<FMT>(in, rb, h);
         if (h == 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
@@ -772,6 +770,16 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp));
         }
+      }
+      // INT4: the scales of this row's two K halves, from the scale plane (read now, used by
+      // the epilogue once the MMAs are done)
+      uint32_t int4_scales = 0;
+      if constexpr (FMT == kFmtINT4) {
+        const TcEntry& E0 = P.e[cur.e];
+        const int row0 = cur.tile * kTileRows + r;
+        if (row0 < E0.N)
+          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux) +
+                                                                (int64_t)row0 * (E0.K >> 7)) + cur.sb);
       }
       if constexpr (has_min(FMT)) {
         // A_ext: (m_0..m_7) at k = 0..7 and again at k = 8..15
@@ -997,7 +1005,7 @@ cudaError_t set_smem_attr() {
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   err = cudaFuncSetAttribute(q4k_tc_kernel<FMT, MPAD, MT, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcSmem<MPAD, FMT>::kTotal);
+                             TcSmem<MPAD, FMT, MT>::kTotal);
   if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return err;
 }
@@ -1077,7 +1085,6 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)std::min(tasks, num_sms()));
   cfg.blockDim = dim3(threads(MPAD));
-  cfg.dynamicSmemBytes = TcSmem<MPAD, FMT>::kTotal;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1088,11 +1095,13 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
     if (M <= 8) {
       cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE>();
       if (err != cudaSuccess) return err;
+      cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
       return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE>, par);
     }
   }
   cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE>();
   if (err != cudaSuccess) return err;
+  cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
   return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE>, par);
 }
 

@@ -41,6 +41,34 @@ def packed_weights(N: int, K: int, seed: int, device=None, keep_host: bool = Fal
     return dev, host
 
 
+def packed_weights_fmt(fmt: int, N: int, K: int, seed: int, device="cuda"):
+    """A device buffer of an N x K matrix in weight format `fmt` for timing: the first
+    min(N, ROWS_PER_CHUNK) rows of W(N, K, seed) packed with the library's packer, their bytes
+    repeated down to row N (the kernels have no data-dependent paths, so the content does not
+    change the timing).  INT4 repeats its quant plane and its scale plane; NVFP4 keeps the first
+    chunk's tensor scale."""
+    import torch
+    from . import qmm
+
+    rows = min(N, inputs.ROWS_PER_CHUNK)
+    _, w = next(inputs.weight_chunks(N, K, seed))
+    chunk = torch.from_numpy(qmm.fmt_pack(fmt, w[:rows])).to(device)
+    out = torch.empty(qmm.fmt_packed_bytes(fmt, N, K), dtype=torch.uint8, device=device)
+    if fmt == qmm.FMT_INT4:
+        planes = [(K // 2, 0, 0), (K // 64, N * (K // 2), rows * (K // 2))]   # (row bytes, out offset, chunk offset)
+    else:
+        rb = (K // 256) * (176 if fmt == qmm.FMT_Q5K else 144)
+        planes = [(rb, 0, 0)]
+    for row_bytes, off, coff in planes:
+        src = chunk[coff:coff + rows * row_bytes]
+        for r0 in range(0, N, rows):
+            n = min(rows, N - r0)
+            out[off + r0 * row_bytes:off + (r0 + n) * row_bytes].copy_(src[:n * row_bytes])
+    if fmt == qmm.FMT_NVFP4:
+        out[-16:].copy_(chunk[-16:])
+    return out
+
+
 def activations(M: int, K: int, seed: int, device=None):
     """(torch bf16 tensor on `device`, host uint16 bits) of M x K activations."""
     import torch
