@@ -13,7 +13,7 @@ Functions (all on host numpy arrays):
   half_value, half_from_float, bf16_value: the number formats, from their definitions
   bf16_round(v)             -> bf16 bits of fp64 values, round to nearest even (definition)
   fmt_pack / fmt_dequant / fmt_matmul(fmt, ...): the same for the other weight formats of
-                               formats_oracle.c (Q5K, NVFP4, INT4 with one scale per 128 columns;
+                               formats_oracle.c (Q5K, Q6K, NVFP4, INT4 with one scale per 128 columns;
                                fmt 0 is Q4K and goes to the functions above)
   e4m3_value, e2m1_value, e4m3_from_float, e2m1_from_float: the 8- and 4-bit float formats
   swiglu(G, F)              -> silu(G[:, :F]) * G[:, F:] in fp64, the step between the gate/up
@@ -192,8 +192,8 @@ def swiglu(G: np.ndarray, F: int) -> np.ndarray:
 
 
 # ---- the other weight formats (formats_oracle.c) -------------------------------------------
-FMT_Q4K, FMT_Q5K, FMT_NVFP4, FMT_INT4 = 0, 1, 2, 3
-FORMATS = {"q4k": FMT_Q4K, "q5k": FMT_Q5K, "nvfp4": FMT_NVFP4, "int4": FMT_INT4}
+FMT_Q4K, FMT_Q5K, FMT_NVFP4, FMT_INT4, FMT_Q6K = 0, 1, 2, 3, 4
+FORMATS = {"q4k": FMT_Q4K, "q5k": FMT_Q5K, "nvfp4": FMT_NVFP4, "int4": FMT_INT4, "q6k": FMT_Q6K}
 
 
 def e4m3_value(c: int) -> float:

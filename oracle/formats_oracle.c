@@ -11,7 +11,7 @@
  * ("sixi-asi 0.11", section "What did not work").  None prints a byte layout; the layouts here are
  * the library's, and every weight value below is a single IEEE rounding of an exact number.
  *
- * Format codes: 1 Q5K, 2 NVFP4, 3 INT4 (0 is Q4K, in q4k_oracle.c).
+ * Format codes: 1 Q5K, 2 NVFP4, 3 INT4, 4 Q6K (0 is Q4K, in q4k_oracle.c).
  *
  * Q5K: 176 bytes per super-block of 256 weights of one row (rows one after another, blocks in
  * order of k):
@@ -31,6 +31,17 @@
  *   trailer      g, binary32 (the tensor scale), then 12 zero bytes
  *   weight = RN32(g * s_b * v_t); s_b * v_t is exact in binary32, so this is one rounding.
  *
+ * Q6K: 208 bytes per super-block of 256 weights of one row (rows one after another), then a
+ * plane of N x K/256 binary16 super-block scales d (row-major) at byte N*(K/256)*208:
+ *   bytes 0-15    u_j, sub-block j = weights 16j..16j+15: sc_j = (u_j & 127) - 64 (-64..63;
+ *                 bit 7 is not used)
+ *   bytes 16-143  1024-bit integer L: the low 4 bits of weight t are L bits [4t, 4t+4)
+ *   bytes 144-207 sixteen 32-bit little-endian words; word m holds the 2-bit high parts of
+ *                 weights 16m..16m+15: weight t = 16m + 8a + i (a = 0..1, i = 0..7) at bits
+ *                 8a + 16*(i >= 4) + 2*(i % 4)
+ *   q_t = low + 16 * high (0..63); weight = RN32(d*sc_j*(q_t - 32)), exact in binary32 (at most
+ *   11 + 6 + 6 significant bits).
+ *
  * INT4: a quant plane, then a scale plane:
  *   quant plane  N rows of K/2 bytes; weight k of a row: the two's-complement 4-bit integer
  *                q (-8..7) at bits [4k, 4k+4) of the row's little-endian integer
@@ -46,6 +57,9 @@
  *        clamped to 6 (S = 0: v_t = 0); the sign of w_t is kept, also when v_t rounds to 0.
  *   INT4 per 128 weights a = max |w|, s = binary16(a / 7) (error 6 on overflow), S = value(s),
  *        q = S > 0 ? clamp(rint(w / S), -8, 7) : 0.
+ *   Q6K  per 16 weights a_j = max |w|, scale_j = a_j / 31; d = binary16(max_j scale_j / 63)
+ *        (error 6 on overflow), D = value(d); sc_j = D > 0 ? clamp(rint(scale_j / D), 0, 63) : 0;
+ *        q_t = D*sc_j > 0 ? clamp(rint(w_t / (D*sc_j)), -32, 31) + 32 : 32.
  */
 #include <math.h>
 #include <stdint.h>
@@ -59,7 +73,7 @@ double oracle_half_value(uint16_t h);
 double oracle_bf16_value(uint16_t b);
 int oracle_half_from_float(float f, uint16_t* out);
 
-enum { FMT_Q5K = 1, FMT_NVFP4 = 2, FMT_INT4 = 3 };
+enum { FMT_Q5K = 1, FMT_NVFP4 = 2, FMT_INT4 = 3, FMT_Q6K = 4 };
 
 static unsigned bits_of(const uint8_t* p, int64_t pos, int n) {
   unsigned v = 0;
@@ -129,6 +143,7 @@ int64_t oracle_fmt_packed_bytes(int fmt, int64_t N, int64_t K) {
     case FMT_Q5K: return N * (K / 256) * 176;
     case FMT_NVFP4: return N * (K / 256) * 144 + 16;
     case FMT_INT4: return N * (K / 2) + N * (K / 128) * 2;
+    case FMT_Q6K: return N * (K / 256) * 208 + N * (K / 256) * 2;
     default: return -1;
   }
 }
@@ -164,6 +179,19 @@ static void dequant_row(int fmt, const uint8_t* Wq, int64_t N, int64_t K, int64_
         double v = oracle_e2m1_value((uint8_t)bits_of(blk + 16, 4 * t, 4));
         /* s*v has <= 6 significant bits, g 24: the product is exact in fp64 */
         w[b * 256 + t] = (float)(g * (s * v));
+      }
+    }
+  } else if (fmt == FMT_Q6K) {
+    const uint8_t* dp = Wq + N * nb * 208 + n * nb * 2;
+    for (int64_t b = 0; b < nb; b++) {
+      const uint8_t* blk = Wq + (n * nb + b) * 208;
+      double d = oracle_half_value((uint16_t)(dp[2 * b] | (dp[2 * b + 1] << 8)));
+      for (int t = 0; t < 256; t++) {
+        int j = t / 16, m = t / 16, a = (t % 16) / 8, i = t % 8;
+        int sc = (int)(blk[j] & 127) - 64;
+        unsigned hi = bits_of(blk + 144, 32 * m + 8 * a + 16 * (i >= 4) + 2 * (i % 4), 2);
+        int q = (int)(bits_of(blk + 16, 4 * t, 4) + 16 * hi);
+        w[b * 256 + t] = (float)(d * (double)sc * (double)(q - 32));
       }
     }
   } else {  /* FMT_INT4 */
@@ -281,6 +309,38 @@ static void pack_nvfp4_block(const float* w, float g, uint8_t* blk) {
   }
 }
 
+static int pack_q6k_block(const float* w, uint8_t* blk, uint8_t* dbits) {
+  float scale[16];
+  for (int j = 0; j < 16; j++) {
+    float a = 0.0f;
+    for (int t = 16 * j; t < 16 * j + 16; t++)
+      if (fabsf(w[t]) > a) a = fabsf(w[t]);
+    scale[j] = a / 31.0f;
+  }
+  float smax = 0.0f;
+  for (int j = 0; j < 16; j++)
+    if (scale[j] > smax) smax = scale[j];
+  uint16_t dh;
+  if (oracle_half_from_float(smax / 63.0f, &dh)) return 6;
+  float D = (float)oracle_half_value(dh);
+  dbits[0] = (uint8_t)(dh & 0xff);
+  dbits[1] = (uint8_t)(dh >> 8);
+  memset(blk, 0, 208);
+  for (int j = 0; j < 16; j++) {
+    unsigned sc = (D > 0.0f) ? (unsigned)clampf_(rintf(scale[j] / D), 0.0f, 63.0f) : 0u;
+    blk[j] = (uint8_t)(sc + 64);
+    float step = D * (float)sc;
+    for (int t = 16 * j; t < 16 * j + 16; t++) {
+      int q = 32;
+      if (step > 0.0f) q = (int)clampf_(rintf(w[t] / step), -32.0f, 31.0f) + 32;
+      int m = t / 16, a = (t % 16) / 8, i = t % 8;
+      put_bits(blk + 16, 4 * t, 4, (unsigned)q & 15u);
+      put_bits(blk + 144, 32 * m + 8 * a + 16 * (i >= 4) + 2 * (i % 4), 2, (unsigned)q >> 4);
+    }
+  }
+  return 0;
+}
+
 /* W: N x K row-major binary32.  Returns 0, 6 on a non-finite weight or a binary16 overflow,
  * 2 on an unknown format. */
 int oracle_fmt_pack(int fmt, const float* W, int64_t N, int64_t K, uint8_t* out) {
@@ -306,6 +366,15 @@ int oracle_fmt_pack(int fmt, const float* W, int64_t N, int64_t K, uint8_t* out)
     uint8_t* tr = out + N * nb * 144;
     memset(tr, 0, 16);
     memcpy(tr, &g, 4);   /* little-endian hosts */
+    return 0;
+  }
+  if (fmt == FMT_Q6K) {
+    uint8_t* dplane = out + N * nb * 208;
+    for (int64_t n = 0; n < N; n++)
+      for (int64_t b = 0; b < nb; b++) {
+        int rc = pack_q6k_block(W + n * K + b * 256, out + (n * nb + b) * 208, dplane + (n * nb + b) * 2);
+        if (rc) return rc;
+      }
     return 0;
   }
   if (fmt == FMT_INT4) {

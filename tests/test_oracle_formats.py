@@ -1,4 +1,4 @@
-"""Pins of the oracle of the other weight formats (Q5K, NVFP4, INT4 with one scale per 128
+"""Pins of the oracle of the other weight formats (Q5K, Q6K, NVFP4, INT4 with one scale per 128
 columns) to things other than itself (CPU only).
 
 * E4M3 values and rounding against torch's float8_e4m3fn (a library conversion); E2M1 values
@@ -88,6 +88,7 @@ def test_packed_bytes(oracle_lib):
     assert oracle_lib.fmt_packed_bytes(oracle_lib.FMT_Q5K, 3, 512) == 3 * 2 * 176
     assert oracle_lib.fmt_packed_bytes(oracle_lib.FMT_NVFP4, 3, 512) == 3 * 2 * 144 + 16
     assert oracle_lib.fmt_packed_bytes(oracle_lib.FMT_INT4, 3, 512) == 3 * 256 + 3 * 4 * 2
+    assert oracle_lib.fmt_packed_bytes(oracle_lib.FMT_Q6K, 3, 512) == 3 * 2 * 208 + 3 * 2 * 2
 
 
 # ---------------------------------------------------------------- layouts by hand ---------
@@ -139,6 +140,45 @@ def test_q5k_high_bit_positions(oracle_lib):
         ref = np.zeros(256, np.float32)
         ref[t] = 16.0
         assert np.array_equal(got, ref), t
+
+
+def q6k_matrix(u, q, d_bits):
+    """A 1 x 256 Q6K matrix (one block and its d) from its fields, following the written layout."""
+    L = 0
+    H = [0] * 16
+    for t in range(256):
+        m, a, i = t // 16, (t % 16) // 8, t % 8
+        L |= (q[t] & 15) << (4 * t)
+        H[m] |= ((q[t] >> 4) & 3) << (8 * a + 16 * (i >= 4) + 2 * (i % 4))
+    return bytes(u) + L.to_bytes(128, "little") + b"".join(h.to_bytes(4, "little") for h in H) + \
+        d_bits.to_bytes(2, "little")
+
+
+def test_q6k_handbuilt_block_closed_form(oracle_lib):
+    # d = 0.5, u_j = 64 + j + 1 (sc_j = j + 1), q_t = t mod 64: w_t = 0.5 (j + 1)((t mod 64) - 32)
+    blk = q6k_matrix([65 + j for j in range(16)], [t % 64 for t in range(256)], 0x3800)
+    got = oracle_lib.fmt_dequant(oracle_lib.FMT_Q6K, np.frombuffer(blk, np.uint8), 1, 256)[0]
+    ref = np.array([0.5 * (t // 16 + 1) * ((t % 64) - 32) for t in range(256)], np.float32)
+    assert np.array_equal(got, ref)
+
+
+def test_q6k_fields(oracle_lib):
+    # one weight at a time with both high bits set (q = 48: w = d sc 16); bit 7 of a scale byte
+    # is not used; u = 0 is sc = -64, u = 63 is sc = -1
+    for t in (0, 3, 4, 7, 8, 11, 12, 15, 16, 100, 255):
+        for qt, wt in ((48, 16.0), (16, -16.0), (31, -1.0)):   # high part 3, 1 and 1 with low 15
+            q = [32] * 256
+            q[t] = qt
+            blk = q6k_matrix([65] * 16, q, 0x3C00)
+            got = oracle_lib.fmt_dequant(oracle_lib.FMT_Q6K, np.frombuffer(blk, np.uint8), 1, 256)[0]
+            ref = np.zeros(256, np.float32)
+            ref[t] = wt
+            assert np.array_equal(got, ref), (t, qt)
+    q = [63] * 256
+    for u, sc in ((0, -64), (63, -1), (64 + 128, 0), (127 + 128, 63), (5 + 128, -59)):
+        blk = q6k_matrix([u] * 16, q, 0x3C00)
+        got = oracle_lib.fmt_dequant(oracle_lib.FMT_Q6K, np.frombuffer(blk, np.uint8), 1, 256)[0]
+        assert np.all(got == np.float32(sc * 31)), u
 
 
 def nvfp4_matrix(scales, codes, g):
@@ -206,6 +246,17 @@ def _exact_rows(fmt, raw, N, K, oracle_lib):
                     c = (Q >> (4 * t)) & 15
                     v = Fraction(E2M1_TABLE[c & 7]) * (-1 if c & 8 else 1)
                     row.append(g * s * v)
+        elif fmt == oracle_lib.FMT_Q6K:
+            for b in range(nb):
+                blk = raw[(n * nb + b) * 208:(n * nb + b + 1) * 208]
+                do = N * nb * 208 + (n * nb + b) * 2
+                d = half_fraction(int.from_bytes(raw[do:do + 2], "little"))
+                L = int.from_bytes(blk[16:144], "little")
+                H = [int.from_bytes(blk[144 + 4 * m:148 + 4 * m], "little") for m in range(16)]
+                for t in range(256):
+                    m, a, i = t // 16, (t % 16) // 8, t % 8
+                    q = ((L >> (4 * t)) & 15) + 16 * ((H[m] >> (8 * a + 16 * (i >= 4) + 2 * (i % 4))) & 3)
+                    row.append(d * ((blk[t // 16] & 127) - 64) * (q - 32))
         else:
             plane = int.from_bytes(raw[n * K // 2:(n + 1) * K // 2], "little")
             so = N * K // 2 + n * (K // 128) * 2
@@ -217,7 +268,7 @@ def _exact_rows(fmt, raw, N, K, oracle_lib):
     return rows
 
 
-@pytest.mark.parametrize("fmt_name", ["q5k", "nvfp4", "int4"])
+@pytest.mark.parametrize("fmt_name", ["q5k", "q6k", "nvfp4", "int4"])
 def test_dequant_bit_exact_vs_rationals(oracle_lib, fmt_name):
     fmt = oracle_lib.FORMATS[fmt_name]
     N, K = 6, 512
@@ -234,7 +285,7 @@ def test_dequant_bit_exact_vs_rationals(oracle_lib, fmt_name):
 
 # ---------------------------------------------------------------- the product ------------
 
-@pytest.mark.parametrize("fmt_name", ["q5k", "nvfp4", "int4"])
+@pytest.mark.parametrize("fmt_name", ["q5k", "q6k", "nvfp4", "int4"])
 def test_matmul_vs_exact_and_one_hot(oracle_lib, fmt_name):
     fmt = oracle_lib.FORMATS[fmt_name]
     N, K, M = 8, 768, 3
@@ -323,12 +374,36 @@ def test_int4_pack_bounds_and_scales(oracle_lib):
     assert np.all(err <= 0.5 * sc[:, :, None] + 0.5 * np.abs(amax - 7 * sc)[:, :, None] + 1e-12)
 
 
+def test_q6k_pack_bounds(oracle_lib):
+    N, K = 8, 1024
+    W = inputs.weights_f32(N, K, 24)
+    Wq = oracle_lib.fmt_pack(oracle_lib.FMT_Q6K, W)
+    w = oracle_lib.fmt_dequant(oracle_lib.FMT_Q6K, Wq, N, K)
+    raw = Wq.tobytes()
+    nb = K // 256
+    for n in range(N):
+        for b in range(nb):
+            blk = raw[(n * nb + b) * 208:][:208]
+            do = N * nb * 208 + (n * nb + b) * 2
+            d = float(half_fraction(int.from_bytes(raw[do:do + 2], "little")))
+            for j in range(16):
+                sc = (blk[j] & 127) - 64
+                seg = slice(b * 256 + 16 * j, b * 256 + 16 * j + 16)
+                a = np.abs(W[n, seg]).max()
+                # within half a step, plus the slack of the 6-bit sub-block scale
+                err = np.abs(W[n, seg].astype(np.float64) - w[n, seg])
+                assert 0 <= sc <= 63
+                assert err.max() <= 0.5 * d * sc + 0.04 * a + 1e-12
+    rms = float(np.sqrt(np.mean((w.astype(np.float64) - W) ** 2)))
+    assert rms < 5e-4
+
+
 def test_packers_reject_nonfinite(oracle_lib):
     W = np.zeros((2, 256), np.float32)
     W[1, 3] = np.inf
-    for fmt in (oracle_lib.FMT_Q5K, oracle_lib.FMT_NVFP4, oracle_lib.FMT_INT4):
+    for fmt in (oracle_lib.FMT_Q5K, oracle_lib.FMT_Q6K, oracle_lib.FMT_NVFP4, oracle_lib.FMT_INT4):
         with pytest.raises(oracle_lib.OraclePackError):
             oracle_lib.fmt_pack(fmt, W)
     Z = np.zeros((2, 256), np.float32)
-    for fmt in (oracle_lib.FMT_Q5K, oracle_lib.FMT_NVFP4, oracle_lib.FMT_INT4):
+    for fmt in (oracle_lib.FMT_Q5K, oracle_lib.FMT_Q6K, oracle_lib.FMT_NVFP4, oracle_lib.FMT_INT4):
         assert np.all(oracle_lib.fmt_dequant(fmt, oracle_lib.fmt_pack(fmt, Z), 2, 256) == 0)
