@@ -45,6 +45,7 @@ __device__ __forceinline__ float hi_f(uint32_t h2) { return __high2float(*reinte
 //   Q5K   fma(D*sc_j, q, -(Dm*m_j))   (the exact value, rounded once)
 //   NVFP4 g * (s_b * v)               (s_b * v exact; one rounding)
 //   INT4  s * q                       (exact)
+//   Q6K   (d * sc_j) * (q - 32)       (d * sc_j exact; one rounding, here none: 23 bits)
 template <int FMT>
 __global__ void __launch_bounds__(256) fmt_dequant_kernel(const uint8_t* __restrict__ W, int64_t N, int64_t K,
                                                           float* __restrict__ out) {
@@ -71,6 +72,30 @@ __global__ void __launch_bounds__(256) fmt_dequant_kernel(const uint8_t* __restr
                            hi_f(p[ww][2]) - 1024.f, (hi_f(p[ww][3]) - 1024.f) * 0.0625f};
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[8 * ww + i] = fmaf(sc.dsc, qv[i], -sc.dmm);
+    }
+  } else if constexpr (FMT == kFmtQ6K) {
+    // weights 32 part .. 32 part + 31 of a super-block: sub-blocks 2 part and 2 part + 1
+    const int64_t blk = s >> 3;
+    const int part = (int)(s & 7);
+    const uint8_t* b = W + blk * 208;
+    const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(W + N * (K / 256) * 208) + blk)));
+    const uint4 q = ldg_nc_v4(b + 16 + 16 * part);
+    const uint2 hh = __ldg(reinterpret_cast<const uint2*>(b + 144) + part);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t hwords[2] = {hh.x, hh.y};
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww) {
+      const int sub = 2 * part + (ww >> 1);
+      const float dsc = d * (float)((int)(b[sub] & 127) - 64);   // exact: 11 + 7 bits
+      uint32_t p[4];
+      if (ww & 1) q6k_magic<1>(words[ww], hwords[ww >> 1], p);
+      else q6k_magic<0>(words[ww], hwords[ww >> 1], p);
+      // (1024 + 16 q) / 16 - 96 = q - 32, exact
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        v[8 * ww + c] = dsc * (lo_f(p[c]) * 0.0625f - 96.f);
+        v[8 * ww + c + 4] = dsc * (hi_f(p[c]) * 0.0625f - 96.f);
+      }
     }
   } else if constexpr (FMT == kFmtNVFP4) {
     const float g = __ldg(reinterpret_cast<const float*>(W + N * (K / 256) * 144));
@@ -126,6 +151,7 @@ cudaError_t launch_dequant_fmt(int fmt, const void* W, int64_t N, int64_t K, flo
   if (fmt == kFmtQ5K) fmt_dequant_kernel<kFmtQ5K><<<(unsigned)blocks, 256, 0, stream>>>(w, N, K, out);
   else if (fmt == kFmtNVFP4) fmt_dequant_kernel<kFmtNVFP4><<<(unsigned)blocks, 256, 0, stream>>>(w, N, K, out);
   else if (fmt == kFmtINT4) fmt_dequant_kernel<kFmtINT4><<<(unsigned)blocks, 256, 0, stream>>>(w, N, K, out);
+  else if (fmt == kFmtQ6K) fmt_dequant_kernel<kFmtQ6K><<<(unsigned)blocks, 256, 0, stream>>>(w, N, K, out);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

@@ -34,6 +34,24 @@ __device__ __forceinline__ void q5k_magic(uint32_t w, uint32_t H, uint32_t (&p)[
   asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(p[3]) : "r"(b8), "r"(u3));
 }
 
+// Q6K: word w of low nibbles (weights 8a .. 8a+7 of a 16-weight sub-block, A = a) and the
+// sub-block's high-part word H (weight i of word a at bits 8a + 16 (i >= 4) + 2 (i % 4)).  The
+// 6-bit quants go to mantissa bits 4..9 (nibble at 4..7, high part at 8..9), so
+//   p[c] = (1024 + 16 q_c, 1024 + 16 q_{c+4}),  c = 0..3   (at most 1024 + 1008: exact).
+template <int A>
+__device__ __forceinline__ void q6k_magic(uint32_t w, uint32_t H, uint32_t (&p)[4]) {
+  const uint32_t h = H >> (8 * A);
+  uint32_t u0, u1, u2, u3;
+  asm("lop3.b32 %0, %1, 0x03000300, 0x64006400, 0xEA;" : "=r"(u0) : "r"(h << 8));   // high parts of 0, 4
+  asm("lop3.b32 %0, %1, 0x03000300, 0x64006400, 0xEA;" : "=r"(u1) : "r"(h << 6));   // of 1, 5
+  asm("lop3.b32 %0, %1, 0x03000300, 0x64006400, 0xEA;" : "=r"(u2) : "r"(h << 4));   // of 2, 6
+  asm("lop3.b32 %0, %1, 0x03000300, 0x64006400, 0xEA;" : "=r"(u3) : "r"(h << 2));   // of 3, 7
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(p[0]) : "r"(w << 4), "r"(u0));
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(p[1]) : "r"(w), "r"(u1));
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(p[2]) : "r"(w >> 4), "r"(u2));
+  asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(p[3]) : "r"(w >> 8), "r"(u3));
+}
+
 // INT4: word w of two's-complement 4-bit quants.  Flipping bit 3 of a field gives q + 8; one
 // 3-input logic op per pair takes the field, flips its top bit and ORs in the exponent of 1024
 // (lookup table 0x6A: b ? a ^ c : c, with b the field mask and c the magic plus the flipped bit).

@@ -6,11 +6,12 @@
 namespace q4k {
 
 // Weight formats (the qmm_format codes of the C ABI).
-enum WeightFormat : int { kFmtQ4K = 0, kFmtQ5K = 1, kFmtNVFP4 = 2, kFmtINT4 = 3 };
+enum WeightFormat : int { kFmtQ4K = 0, kFmtQ5K = 1, kFmtNVFP4 = 2, kFmtINT4 = 3, kFmtQ6K = 4 };
 
 // One product handed to a kernel: Y[M x N] = X[M x K] * dequant(W)^T.  fmt is the weight
 // format; aux points into the packed buffer at what the format keeps outside its row blocks
-// (NVFP4: the fp32 tensor scale; INT4: the scale plane; otherwise unused).
+// (NVFP4: the fp32 tensor scale; INT4: the scale plane; Q6K: the plane of super-block scales;
+// otherwise unused).
 struct Job {
   const void* W;
   const uint16_t* X;

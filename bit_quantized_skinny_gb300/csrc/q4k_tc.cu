@@ -95,10 +95,12 @@ constexpr int kMaxPrep = 512;      // distinct activations per preparation launc
 constexpr int kSmemLimit = 232448; // shared memory per CTA (227 KB)
 
 // Bytes of one row's 256 weights in the streamed weight plane (one TMA box column), per format:
-// Q4K and NVFP4 144 (NVFP4: 16 E4M3 scales + 128 bytes of codes), Q5K 176, INT4 128 (its
-// scales live in a separate plane).  The dmin term (an extra MMA and a second accumulator
-// column block) belongs to the k-quants only.
-__host__ __device__ constexpr int blk_bytes(int f) { return f == kFmtQ5K ? 176 : (f == kFmtINT4 ? 128 : 144); }
+// Q4K and NVFP4 144 (NVFP4: 16 E4M3 scales + 128 bytes of codes), Q5K 176, Q6K 208, INT4 128
+// (INT4's scales and Q6K's super-block scales live in separate planes).  The dmin term (an extra
+// MMA and a second accumulator column block) belongs to Q4K and Q5K only.
+__host__ __device__ constexpr int blk_bytes(int f) {
+  return f == kFmtQ5K ? 176 : (f == kFmtQ6K ? 208 : (f == kFmtINT4 ? 128 : 144));
+}
 __host__ __device__ constexpr bool has_min(int f) { return f == kFmtQ4K || f == kFmtQ5K; }
 __host__ __device__ constexpr int w_stage_bytes(int f) { return kTileRows * blk_bytes(f); }
 
@@ -168,11 +170,11 @@ constexpr bool smem_fits() {
   return TcSmem<16, FMT, 8>::kTotal <= kSmemLimit && TcSmem<16, FMT, 16>::kTotal <= kSmemLimit &&
          TcSmem<32, FMT, 32>::kTotal <= kSmemLimit;
 }
-static_assert(smem_fits<kFmtQ4K>() && smem_fits<kFmtQ5K>() && smem_fits<kFmtNVFP4>() && smem_fits<kFmtINT4>(),
-              "shared memory");
+static_assert(smem_fits<kFmtQ4K>() && smem_fits<kFmtQ5K>() && smem_fits<kFmtNVFP4>() && smem_fits<kFmtINT4>() &&
+              smem_fits<kFmtQ6K>(), "shared memory");
 static_assert(stages(16, kFmtQ4K, 8) == 8 && stages(16, kFmtQ4K, 16) == 7 && stages(32, kFmtQ4K, 32) == 5 &&
-              stages(16, kFmtQ5K, 16) >= 4 && stages(32, kFmtQ5K, 32) >= 3 && stages(32, kFmtINT4, 32) >= 3,
-              "stage counts");
+              stages(16, kFmtQ5K, 16) >= 4 && stages(32, kFmtQ5K, 32) >= 3 && stages(32, kFmtINT4, 32) >= 3 &&
+              stages(16, kFmtQ6K, 16) >= 4 && stages(32, kFmtQ6K, 32) >= 3, "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
 static_assert(stage_bytes(16, kFmtQ4K) % 128 == 0 && stage_bytes(32, kFmtQ5K) % 128 == 0 &&
               stage_bytes(16, kFmtINT4) % 1024 == 0 && w_stage_bytes(kFmtQ5K) % 128 == 0, "stage alignment");
@@ -415,6 +417,7 @@ template <int FMT>
 struct HalfIn {
   uint4 qv[4];   // quants of the half: 16 bytes per 32 weights
   uint4 hb;      // Q5K: the high-bit words of the half's four sub-blocks
+  uint4 hv[2];   // Q6K: the high-part words of the half's eight sub-blocks
 };
 
 // INT4 tiles are copied with the 128-byte swizzle: 16-byte chunk c of row r sits at chunk
@@ -431,6 +434,11 @@ __device__ __forceinline__ void load_half(HalfIn<FMT>& in, uint32_t rb, int h) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 48 + 64 * h + 16 * k);
     in.hb = lds128(rb + 16 + 16 * h);
+  } else if constexpr (FMT == kFmtQ6K) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
+    in.hv[0] = lds128(rb + 144 + 32 * h);
+    in.hv[1] = lds128(rb + 144 + 32 * h + 16);
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) in.qv[k] = lds128(rb + 16 + 64 * h + 16 * k);
@@ -490,6 +498,39 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
         cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p[1]), sc16[k], sc64[k]));  // (q1, q5) * sc
         cols[4 * ww + 2] = h2bits(__hfma2(bits2h(p[2]), sc2[k], scm[k]));   // (q2, q6) * sc
         cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p[3]), sc16[k], sc64[k]));  // (q3, q7) * sc
+      }
+      tc::st_x16(aaddr + 16 * k, cols);
+    }
+  } else if constexpr (FMT == kFmtQ6K) {
+    // A = sc_j * (q - 32), |A| <= 64 * 32: exact in fp16.  The 6-bit quant is placed at mantissa
+    // bits 4..9 (1024 + 16 q), then one HFMA2 with (sc/16, -96 sc) per pair.
+    // scale bytes u of the half's sub-blocks 2k, 2k+1 (bytes 8h + 2k, 8h + 2k + 1 of the header)
+    const uint32_t sw[2] = {h ? hd.z : hd.x, h ? hd.w : hd.y};
+    const uint32_t hwords[8] = {in.hv[0].x, in.hv[0].y, in.hv[0].z, in.hv[0].w,
+                                in.hv[1].x, in.hv[1].y, in.hv[1].z, in.hv[1].w};
+    const __half2 k1o16 = C.k1o16;
+    const __half2 kn68 = __float2half2_rn(-68.f), kn1536 = __float2half2_rn(-1536.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t ub;   // u of sub-block 2k in bits 0..7, of 2k+1 in bits 16..23
+      asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(ub) : "r"(sw[k >> 1] >> (16 * (k & 1))));
+      uint32_t um;
+      asm("lop3.b32 %0, %1, 0x007F007F, 0x64006400, 0xEA;" : "=r"(um) : "r"(ub));      // 1024 + (u & 127)
+      const __half2 s16 = __hfma2(bits2h(um), k1o16, kn68);   // ((1024 + u)/16 - 68 = sc/16, exact)
+      const __half2 c96 = __hmul2(s16, kn1536);               // -96 sc
+      const __half2 s16_a = __low2half2(s16), s16_b = __high2half2(s16);
+      const __half2 c96_a = __low2half2(c96), c96_b = __high2half2(c96);
+      const uint4 v = in.qv[k];
+      const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+      uint32_t cols[16];
+#pragma unroll
+      for (int ww = 0; ww < 4; ++ww) {
+        uint32_t p[4];
+        if (ww & 1) q6k_magic<1>(words[ww], hwords[2 * k + (ww >> 1)], p);
+        else q6k_magic<0>(words[ww], hwords[2 * k + (ww >> 1)], p);
+        const __half2 sa = ww < 2 ? s16_a : s16_b, ca = ww < 2 ? c96_a : c96_b;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cols[4 * ww + c] = h2bits(__hfma2(bits2h(p[c]), sa, ca));   // (q_c, q_c+4)
       }
       tc::st_x16(aaddr + 16 * k, cols);
     }
@@ -773,6 +814,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
       }
       // INT4: the scales of this row's two K halves, from the scale plane (read now, used by
       // the epilogue once the MMAs are done)
+      // Q6K: the row's super-block scale d, from its plane
       uint32_t int4_scales = 0;
       if constexpr (FMT == kFmtINT4) {
         const TcEntry& E0 = P.e[cur.e];
@@ -780,6 +822,11 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
         if (row0 < E0.N)
           int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux) +
                                                                 (int64_t)row0 * (E0.K >> 7)) + cur.sb);
+      } else if constexpr (FMT == kFmtQ6K) {
+        const TcEntry& E0 = P.e[cur.e];
+        const int row0 = cur.tile * kTileRows + r;
+        if (row0 < E0.N)
+          int4_scales = __ldg(static_cast<const unsigned short*>(P.aux) + (int64_t)row0 * (E0.K >> 8) + cur.sb);
       }
       if constexpr (has_min(FMT)) {
         // A_ext: (m_0..m_7) at k = 0..7 and again at k = 8..15
@@ -819,6 +866,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
       //   k-quants  y += (D 2^s) acc - (Dm 2^s 64) acc_ext
       //   NVFP4     y += (g 2^s) acc
       //   INT4      y += (s_0 2^s) acc_half0 + (s_1 2^s) acc_half1
+      //   Q6K       y += (d 2^s) acc
       float sx, sy;
       if constexpr (has_min(FMT)) {
         const float2 dd = __half22float2(bits2h(hd.x));   // (D, Dm) of this row
@@ -827,12 +875,15 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
       } else if constexpr (FMT == kFmtNVFP4) {
         sx = __ldg(static_cast<const float*>(P.aux)) * sigma;
         sy = 0.f;
+      } else if constexpr (FMT == kFmtQ6K) {
+        sx = __half2float(__ushort_as_half((unsigned short)int4_scales)) * sigma;
+        sy = 0.f;
       } else {
         const float2 ss = __half22float2(bits2h(int4_scales));
         sx = ss.x * sigma;
         sy = ss.y * sigma;
       }
-      constexpr bool kTwo = FMT != kFmtNVFP4;   // a second accumulator block to read
+      constexpr bool kTwo = FMT != kFmtNVFP4 && FMT != kFmtQ6K;   // a second accumulator block to read
       constexpr int kW = MT == 16 ? 16 : 8;   // token columns per TMEM read round
 #pragma unroll
       for (int c0 = 0; c0 < MT; c0 += kW) {
@@ -1309,6 +1360,7 @@ cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream) {
     case kFmtQ5K: return narrow ? launch_tc_t<kFmtQ5K, 16>(jobs, count, M, stream) : launch_tc_t<kFmtQ5K, 32>(jobs, count, M, stream);
     case kFmtNVFP4: return narrow ? launch_tc_t<kFmtNVFP4, 16>(jobs, count, M, stream) : launch_tc_t<kFmtNVFP4, 32>(jobs, count, M, stream);
     case kFmtINT4: return narrow ? launch_tc_t<kFmtINT4, 16>(jobs, count, M, stream) : launch_tc_t<kFmtINT4, 32>(jobs, count, M, stream);
+    case kFmtQ6K: return narrow ? launch_tc_t<kFmtQ6K, 16>(jobs, count, M, stream) : launch_tc_t<kFmtQ6K, 32>(jobs, count, M, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -33,7 +33,7 @@ qmm_status check_shape(int64_t N, int64_t K) {
   return QMM_OK;
 }
 
-bool valid_format(int fmt) { return fmt >= QMM_FMT_Q4K && fmt <= QMM_FMT_INT4; }
+bool valid_format(int fmt) { return fmt >= QMM_FMT_Q4K && fmt <= QMM_FMT_Q6K; }
 
 qmm_status check_job(const void* W, int64_t N, int64_t K, const uint16_t* X, const float* Y) {
   if (!W || !X || !Y) return QMM_ERR_NULL;

@@ -253,6 +253,46 @@ bool pack_int4_row(const float* w, int64_t K, uint8_t* q, uint8_t* scales) {
   return true;
 }
 
+// Q6K super-block (208 bytes, its binary16 d written to dbits): 16 scale bytes u = sc + 64, the
+// low nibbles of the 256 quants, then per 16 weights one 32-bit word of their 2-bit high parts
+// (weight 8a + i of the sub-block at bit 8a + 16 (i >= 4) + 2 (i % 4)).
+bool pack_q6k_superblock(const float* w, uint8_t* out, uint8_t* dbits) {
+  float scale[16];
+  float smax = 0.0f;
+  for (int j = 0; j < 16; ++j) {
+    float a = 0.0f;
+    for (int t = 16 * j; t < 16 * j + 16; ++t) a = std::max(a, std::fabs(w[t]));
+    scale[j] = a / 31.0f;
+    smax = std::max(smax, scale[j]);
+  }
+  uint16_t d_bits = 0;
+  bool ovf = false;
+  const float D = to_half_and_back(smax / 63.0f, &d_bits, &ovf);
+  if (ovf) return false;
+  dbits[0] = (uint8_t)(d_bits & 0xFF);
+  dbits[1] = (uint8_t)(d_bits >> 8);
+  std::memset(out, 0, 208);
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t sc = D > 0.0f ? level(scale[j] / D, 63.0f) : 0u;
+    out[j] = (uint8_t)(sc + 64);
+    const float step = D * static_cast<float>(sc);
+    uint32_t hw = 0;
+    for (int u = 0; u < 16; ++u) {
+      const int t = 16 * j + u;
+      int q = 32;
+      if (step > 0.0f) {
+        const float r = std::rint(w[t] / step);
+        q = (int)(r < -32.0f ? -32.0f : (r > 31.0f ? 31.0f : r)) + 32;
+      }
+      out[16 + t / 2] |= (uint8_t)((q & 15) << (4 * (t & 1)));
+      const int a = u >> 3, i = u & 7;
+      hw |= (uint32_t)(q >> 4) << (8 * a + 16 * (i >> 2) + 2 * (i & 3));
+    }
+    for (int b = 0; b < 4; ++b) out[144 + 4 * j + b] = (uint8_t)(hw >> (8 * b));
+  }
+  return true;
+}
+
 // Rows [0, N) split over up to `threads` threads; fn(n) packs row n and returns false on error.
 template <class Fn>
 int for_rows(int64_t N, int threads, Fn fn) {
@@ -318,6 +358,7 @@ int64_t fmt_packed_bytes(int fmt, int64_t N, int64_t K) {
     case kFmtQ5K: return N * (K / 256) * 176;
     case kFmtNVFP4: return N * (K / 256) * 144 + 16;
     case kFmtINT4: return N * (K / 2) + N * (K / 128) * 2;
+    case kFmtQ6K: return N * (K / 256) * 208 + N * (K / 256) * 2;
     default: return -1;
   }
 }
@@ -325,6 +366,7 @@ int64_t fmt_packed_bytes(int fmt, int64_t N, int64_t K) {
 int64_t fmt_aux_offset(int fmt, int64_t N, int64_t K) {
   if (fmt == kFmtNVFP4) return N * (K / 256) * 144;
   if (fmt == kFmtINT4) return N * (K / 2);
+  if (fmt == kFmtQ6K) return N * (K / 256) * 208;
   return 0;
 }
 
@@ -354,6 +396,15 @@ int pack_fmt(int fmt, const float* W, int64_t N, int64_t K, uint8_t* out, int th
     std::memcpy(&gb, &g, 4);
     for (int b = 0; b < 4; ++b) tr[b] = (uint8_t)(gb >> (8 * b));
     return rc;
+  }
+  if (fmt == kFmtQ6K) {
+    uint8_t* dplane = out + fmt_aux_offset(fmt, N, K);
+    return for_rows(N, threads, [&](int64_t n) {
+      for (int64_t b = 0; b < nb; ++b)
+        if (!pack_q6k_superblock(W + n * K + b * 256, out + (n * nb + b) * 208, dplane + (n * nb + b) * 2))
+          return false;
+      return true;
+    });
   }
   if (fmt == kFmtINT4) {
     uint8_t* scales = out + fmt_aux_offset(fmt, N, K);

@@ -26,8 +26,8 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_NULL", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_M_RANG
           4: "QMM_ERR_ALIGN", 5: "QMM_ERR_BUFSIZE", 6: "QMM_ERR_NONFINITE", 7: "QMM_ERR_CUDA",
           8: "QMM_ERR_COUNT", 9: "QMM_ERR_VARIANT", 10: "QMM_ERR_SCRATCH", 11: "QMM_ERR_FORMAT"}
 
-FMT_Q4K, FMT_Q5K, FMT_NVFP4, FMT_INT4 = 0, 1, 2, 3
-FORMATS = {"q4k": FMT_Q4K, "q5k": FMT_Q5K, "nvfp4": FMT_NVFP4, "int4": FMT_INT4}
+FMT_Q4K, FMT_Q5K, FMT_NVFP4, FMT_INT4, FMT_Q6K = 0, 1, 2, 3, 4
+FORMATS = {"q4k": FMT_Q4K, "q5k": FMT_Q5K, "q6k": FMT_Q6K, "nvfp4": FMT_NVFP4, "int4": FMT_INT4}
 
 # Every symbol include/qmm.h declares.
 EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_dequant",

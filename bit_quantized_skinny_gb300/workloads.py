@@ -45,8 +45,8 @@ def packed_weights_fmt(fmt: int, N: int, K: int, seed: int, device="cuda"):
     """A device buffer of an N x K matrix in weight format `fmt` for timing: the first
     min(N, ROWS_PER_CHUNK) rows of W(N, K, seed) packed with the library's packer, their bytes
     repeated down to row N (the kernels have no data-dependent paths, so the content does not
-    change the timing).  INT4 repeats its quant plane and its scale plane; NVFP4 keeps the first
-    chunk's tensor scale."""
+    change the timing).  INT4 and Q6K repeat both of their planes; NVFP4 keeps the first chunk's
+    tensor scale."""
     import torch
     from . import qmm
 
@@ -56,6 +56,9 @@ def packed_weights_fmt(fmt: int, N: int, K: int, seed: int, device="cuda"):
     out = torch.empty(qmm.fmt_packed_bytes(fmt, N, K), dtype=torch.uint8, device=device)
     if fmt == qmm.FMT_INT4:
         planes = [(K // 2, 0, 0), (K // 64, N * (K // 2), rows * (K // 2))]   # (row bytes, out offset, chunk offset)
+    elif fmt == qmm.FMT_Q6K:
+        rb = (K // 256) * 208
+        planes = [(rb, 0, 0), ((K // 256) * 2, N * rb, rows * rb)]
     else:
         rb = (K // 256) * (176 if fmt == qmm.FMT_Q5K else 144)
         planes = [(rb, 0, 0)]

@@ -250,6 +250,15 @@ qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64
  *                 bias 1, 1 fraction bit: 0, 0.5, 1, 1.5, 2, 3, 4, 6) of weight t at bits
  *                 [4t, 4t+4).  After all N rows: a 16-byte trailer, the binary32 tensor scale
  *                 g then 12 zero bytes.  weight = RN32(g * s_b * v_t).
+ *   QMM_FMT_Q6K   208 bytes per super-block of 256 weights of a row (rows one after another),
+ *                 then at byte N*(K/256)*208 a plane of N x K/256 binary16 super-block scales d:
+ *                 bytes [0, 16) u_j for sub-blocks j of 16 weights, sc_j = (u_j & 127) - 64
+ *                 (a 7-bit signed scale; bit 7 unused); bytes [16, 144) the low 4 bits of weight
+ *                 t at bits [4t, 4t+4); bytes [144, 208) sixteen 32-bit little-endian words, word
+ *                 m the 2-bit high parts of weights 16m .. 16m+15: weight 16m + 8a + i (a = 0..1,
+ *                 i = 0..7) at bits 8a + 16 (i >= 4) + 2 (i % 4).  q_t = low + 16 high (0..63);
+ *                 weight = RN32(d*sc_j*(q_t - 32)) (exact: at most 23 significant bits).  The
+ *                 7-bit scales keep sc*(q - 32) within 2048, exact in fp16 on the tensor cores.
  *   QMM_FMT_INT4  a quant plane of N rows of K/2 bytes (weight k of a row: the two's-complement
  *                 4-bit integer at bits [4k, 4k+4) of the row), then at byte N*K/2 a scale
  *                 plane of N x K/128 binary16 scales, row-major; weight = s * q (exact).
@@ -261,6 +270,9 @@ qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64
  *         v = E2M1(w / S), nearest even, clamped to 6, sign kept (S = 0: v = +0).
  *   INT4  per 128 weights s = binary16(max|w| / 7); q = S > 0 ? clamp(rint(w / S), -8, 7) : 0
  *         (S = the value of s).
+ *   Q6K   per 16 weights scale_j = max|w| / 31; d = binary16(max_j scale_j / 63); sc_j =
+ *         D > 0 ? clamp(rint(scale_j / D), 0, 63) : 0; q = D*sc_j > 0 ? clamp(rint(w / (D*sc_j)),
+ *         -32, 31) + 32 : 32 (D = the value of d).
  *
  * The products run on the tensor cores (one launch per call; the CUDA-core kernel is Q4K's);
  * the other conventions are those of qmm_run.  Shapes: as for Q4K (K % 256 == 0). */
@@ -268,12 +280,13 @@ typedef enum {
   QMM_FMT_Q4K = 0,
   QMM_FMT_Q5K = 1,
   QMM_FMT_NVFP4 = 2,
-  QMM_FMT_INT4 = 3
+  QMM_FMT_INT4 = 3,
+  QMM_FMT_Q6K = 4
 } qmm_format;
 
 /* Bytes of the packed form of an N x K matrix in format fmt (0 for an invalid shape or
  * format): Q4K N*(K/256)*144, Q5K N*(K/256)*176, NVFP4 N*(K/256)*144 + 16,
- * INT4 N*K/2 + N*(K/128)*2. */
+ * INT4 N*K/2 + N*(K/128)*2, Q6K N*(K/256)*210. */
 size_t qmm_fmt_packed_bytes(int fmt, int64_t N, int64_t K);
 
 /* Pack W_host (N x K row-major fp32, host) into format fmt, as qmm_pack does for Q4K.

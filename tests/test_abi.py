@@ -99,7 +99,7 @@ def test_pack_errors(qmm):
 
 # ---------------------------------------------------------------- other weight formats ----
 
-FMTS = ["q5k", "nvfp4", "int4"]
+FMTS = ["q5k", "q6k", "nvfp4", "int4"]
 
 
 def test_fmt_packed_bytes(qmm):
@@ -107,6 +107,7 @@ def test_fmt_packed_bytes(qmm):
     assert qmm.fmt_packed_bytes(qmm.FMT_Q5K, 34816, 5120) == 34816 * 20 * 176
     assert qmm.fmt_packed_bytes(qmm.FMT_NVFP4, 34816, 5120) == 100_270_080 + 16
     assert qmm.fmt_packed_bytes(qmm.FMT_INT4, 34816, 5120) == 34816 * 2560 + 34816 * 40 * 2
+    assert qmm.fmt_packed_bytes(qmm.FMT_Q6K, 34816, 5120) == 34816 * 20 * 210
     assert qmm.fmt_packed_bytes(9, 4, 256) == 0
     assert qmm.fmt_packed_bytes(qmm.FMT_INT4, 4, 255) == 0
 
@@ -148,11 +149,11 @@ def test_fmt_argument_errors_need_no_gpu(qmm):
     assert lib.qmm_fmt_run(qmm.FMT_INT4, p, 4, 255, p, p, 1, None) == 2
     assert lib.qmm_fmt_run(qmm.FMT_Q5K, p, 4, 256, p, p, 33, None) == 3
     assert lib.qmm_fmt_run(qmm.FMT_Q5K, ctypes.c_void_p(24), 4, 256, p, p, 1, None) == 4
-    assert lib.qmm_fmt_dequant(4, p, 4, 256, p, None) == 11
+    assert lib.qmm_fmt_dequant(9, p, 4, 256, p, None) == 11
     assert lib.qmm_fmt_dequant(qmm.FMT_INT4, p, 4, 100, p, None) == 2
     W = np.zeros((2, 256), np.float32)
     W[0, 1] = np.inf
-    for fmt in (qmm.FMT_Q5K, qmm.FMT_NVFP4, qmm.FMT_INT4):
+    for fmt in (qmm.FMT_Q5K, qmm.FMT_Q6K, qmm.FMT_NVFP4, qmm.FMT_INT4):
         with pytest.raises(qmm.QmmError) as e:
             qmm.fmt_pack(fmt, W)
         assert e.value.status == 6

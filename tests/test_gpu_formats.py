@@ -1,4 +1,4 @@
-"""GPU parity of the other weight formats (Q5K, NVFP4, INT4 with one scale per 128 columns):
+"""GPU parity of the other weight formats (Q5K, Q6K, NVFP4, INT4 with one scale per 128 columns):
 the CUDA path through the C ABI (qmm_fmt_run, qmm_fmt_dequant) against the oracle.
 
 Acceptance as for Q4K: dequantized weights bit-exact; every output element within
@@ -12,7 +12,7 @@ from bit_quantized_skinny_gb300 import build_lib, inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
-FMTS = ["q5k", "nvfp4", "int4"]
+FMTS = ["q5k", "q6k", "nvfp4", "int4"]
 
 
 @pytest.fixture(scope="module")
@@ -100,6 +100,9 @@ def test_dequant_random_bytes_bit_exact(qmm, oracle_lib, fmt_name):
         nan = (blocks[:, :16] & 0x7F) == 0x7F
         blocks[:, :16][nan] &= 0xFE
         raw[N * (K // 256) * 144:] = np.frombuffer(np.float32(0.75).tobytes() + bytes(12), np.uint8)
+    elif fmt_name == "q6k":
+        dp = raw[N * (K // 256) * 208:]
+        dp[1::2] &= 0xFB                             # even exponent field: finite d
     else:
         sc = raw[N * K // 2:]
         sc[1::2] &= 0xFB                             # even exponent field: finite scales
