@@ -550,6 +550,53 @@ def run_formats(args):
                       "formats": results}), flush=True)
 
 
+def run_pass_formats(args):
+    """The 64-layer pass (384 matrices) with its weights in each format, and a mixed pass
+    (Q6K for the v and down projections, Q4K for the others: the pattern of the pages' Q4_K_M
+    files, which mix k-quant widths), each as one qmm_fmt_run_batched call (one launch group per
+    format present).  GB/s counts the packed bytes the pass reads.  Prints one JSON line."""
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, inputs, qmm, workloads
+
+    build_lib.build()
+    qmm.load()
+    torch.cuda.set_device(0)
+    peak, _ = hbm_peak()
+    stream = torch.cuda.current_stream()
+    plans = {name: (lambda shape, f=fmt: f) for name, fmt in qmm.FORMATS.items()}
+    plans["mix_q4k_q6k"] = lambda shape: qmm.FMT_Q6K if shape in ("v", "down") else qmm.FMT_Q4K
+    names = list(plans) if args.pass_formats == "all" else args.pass_formats.split(",")
+    res = {}
+    for pname in names:
+        plan = plans[pname]
+        for M in args.Ms:
+            xs = {K: workloads.activations(M, K, inputs.seed_for(4, 100 + K % 97), device="cuda")[0]
+                  for K in sorted({K for _, _, K in workloads.LAYER_SHAPES})}
+            bases = {name: workloads.packed_weights_fmt(plan(name), N, K, inputs.seed_for(4, i))
+                     for i, (name, N, K) in enumerate(workloads.LAYER_SHAPES)}
+            items, keep = [], []
+            for layer in range(LAYERS):
+                for name, N, K in workloads.LAYER_SHAPES:
+                    w = bases[name] if layer == 0 else bases[name].clone()
+                    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+                    keep += [w, y]
+                    items.append((plan(name), w, xs[K], y, N, K))
+            entries = qmm.make_fmt_entries(items)
+            wbytes = sum(it[1].numel() for it in items)
+            fn = lambda: qmm.fmt_run_batched(entries, M)
+            ms = time_steps(fn, max(3, args.steps // 2), 3, stream, lambda: None)
+            g = weight_gbps(wbytes, ms)
+            res[f"{pname}/M{M}"] = {"ms": round(ms, 4), "weight_bytes": wbytes, "gbps": round(g, 1),
+                                    "frac_of_measured_hbm": round(g / peak, 4)}
+            if qmm.device_status() != 0:
+                raise RuntimeError("kernel reported a device-side error")
+            del items, keep, bases, entries
+            torch.cuda.empty_cache()
+    print(json.dumps({"metric": "weight-read GB/s of the 64-layer pass by weight format", "unit": UNIT,
+                      "peak_gbps": peak, "l2": "inputs larger than L2: every pass reads its weights from HBM",
+                      "passes": res}), flush=True)
+
+
 def run_reference(args, rank: int):
     """The oracle (plain fp64 C, host cores) on a bounded sample of the same workload."""
     if rank != 0:
@@ -621,6 +668,8 @@ def main(argv=None):
     ap.add_argument("--ffn", action="store_true", help="time one feed-forward block per call instead")
     ap.add_argument("--indexed", action="store_true", help="time the indexed-expert product instead")
     ap.add_argument("--fmt", default=None, help="with --formats: only these formats (comma list)")
+    ap.add_argument("--pass-formats", default=None,
+                    help="time the 64-layer pass in these weight formats instead (comma list, 'mix_q4k_q6k' or 'all')")
     ap.add_argument("--formats", default=None,
                     help="time the weight formats on these shapes instead (comma list of gate_up,down,q,k,lm_head or 'all')")
     args = ap.parse_args(argv)
@@ -648,6 +697,10 @@ def main(argv=None):
     if args.formats:
         if rank == 0:
             run_formats(args)
+        return
+    if args.pass_formats:
+        if rank == 0:
+            run_pass_formats(args)
         return
     dist_ok = False
     if world > 1:

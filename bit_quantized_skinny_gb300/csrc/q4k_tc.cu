@@ -194,8 +194,11 @@ struct TcEntry {
 };
 
 // Launch parameters: the weights of entry e are reached through maps[e], a 2D tensor map over
-// the packed rows (inner dimension: the row's bytes, outer: the N rows).
-template <int MAXE>
+// the packed rows (inner dimension: the row's bytes, outer: the N rows).  aux[e]: what entry e
+// keeps outside its row blocks (NVFP4: the fp32 tensor scale; INT4: the N x K/128 binary16 scale
+// plane; Q6K: the N x K/256 binary16 d plane); Q4K has none (one unused slot).  Kept out of
+// TcEntry: the Q4K kernel measured ~1.5 % slower with a different entry layout.
+template <int MAXE, int NAUX>
 struct TcParams {
   CUtensorMap maps[MAXE];
   TcEntry e[MAXE];
@@ -203,11 +206,9 @@ struct TcParams {
   int M;
   int tasks_total;
   int pad_;
-  // the formats other than Q4K run one product per launch: what that product keeps outside its
-  // row blocks (NVFP4: the fp32 tensor scale; INT4: the N x K/128 binary16 scale plane).  Kept
-  // out of TcEntry: the Q4K kernel measured ~1.5% slower with a different entry layout.
-  const void* aux;
+  const void* aux[NAUX];
 };
+__host__ __device__ constexpr int naux(int f, int maxe) { return f == kFmtQ4K ? 1 : maxe; }
 
 struct PrepEntry {
   const uint16_t* X;
@@ -357,10 +358,10 @@ __device__ __noinline__ void reduce_chunks(const float* part, int chunks, int M,
 }
 
 // Task t of the launch: its entry, tile and K split, and its super-block range.
-template <int MAXE>
+template <class PT>
 struct TaskView {
   int e, tile, split, sb0, sb1;
-  __device__ __forceinline__ TaskView(const TcParams<MAXE>& P, int t) {
+  __device__ __forceinline__ TaskView(const PT& P, int t) {
     int lo = 0, hi = P.count - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -378,18 +379,18 @@ struct TaskView {
 
 // Walk over the tasks of one dequant group: the CTA's local tasks j = g, g + NG, ... (task index
 // blockIdx.x + j * gridDim.x), each super-block of each task in order.
-template <int MAXE, int NG>
+template <class PT, int NG>
 struct GroupCursor {
   int j, t, e, tile, split, sb, end;
-  __device__ __forceinline__ void load(const TcParams<MAXE>& P) {
+  __device__ __forceinline__ void load(const PT& P) {
     t = (int)blockIdx.x + j * (int)gridDim.x;
     if (t >= P.tasks_total) { t = -1; return; }
-    const TaskView<MAXE> T(P, t);
+    const TaskView<PT> T(P, t);
     e = T.e; tile = T.tile; split = T.split; sb = T.sb0; end = T.sb1;
   }
-  __device__ __forceinline__ void start(const TcParams<MAXE>& P, int g) { j = g; load(P); }
+  __device__ __forceinline__ void start(const PT& P, int g) { j = g; load(P); }
   // after the current super-block: true if it was the last of its task
-  __device__ __forceinline__ bool advance(const TcParams<MAXE>& P) {
+  __device__ __forceinline__ bool advance(const PT& P) {
     if (++sb < end) return false;
     j += NG;
     load(P);
@@ -580,7 +581,8 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
 // MT: the token columns the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M
 // hold zeros.
 template <int FMT, int MPAD, int MT, int MAXE>
-__global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_constant__ TcParams<MAXE> P) {
+__global__ void __launch_bounds__(threads(MPAD), 1)
+    q4k_tc_kernel(const __grid_constant__ TcParams<MAXE, naux(FMT, MAXE)> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = TcSmem<MPAD, FMT, MT>;
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     fence_barrier_init();
   }
   if (warp == 0 && lane < NG) {   // super-blocks of each group
-    GroupCursor<MAXE, NG> cur;
+    GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur;
     cur.start(P, lane);
     int cnt = 0;
     while (cur.t >= 0) { cnt += cur.end - cur.sb; cur.j += NG; cur.load(P); }
@@ -654,7 +656,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the prepared activations are written
     if (elect_one()) {
       const uint64_t pol = policy_evict_first();
-      GroupCursor<MAXE, NG> cur[NG];
+      GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur[NG];
 #pragma unroll
       for (int g = 0; g < NG; ++g) cur[g].start(P, g);
       uint32_t su = 0;
@@ -765,7 +767,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
     const uint32_t acc2 = tl + acc2_col(MPAD, grp);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // split counters zeroed, activations written
     uint32_t sbits = 0;   // parity of this group's full barrier of each stage
-    GroupCursor<MAXE, NG> cur;
+    GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur;
     cur.start(P, grp);
     // With two groups (Mpad 32) the stage, header and 2^s of a group's next super-block are
     // fetched while the MMAs of the current one run (measured faster there; with three groups,
@@ -820,13 +822,13 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
         const TcEntry& E0 = P.e[cur.e];
         const int row0 = cur.tile * kTileRows + r;
         if (row0 < E0.N)
-          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux) +
+          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux[cur.e]) +
                                                                 (int64_t)row0 * (E0.K >> 7)) + cur.sb);
       } else if constexpr (FMT == kFmtQ6K) {
         const TcEntry& E0 = P.e[cur.e];
         const int row0 = cur.tile * kTileRows + r;
         if (row0 < E0.N)
-          int4_scales = __ldg(static_cast<const unsigned short*>(P.aux) + (int64_t)row0 * (E0.K >> 8) + cur.sb);
+          int4_scales = __ldg(static_cast<const unsigned short*>(P.aux[cur.e]) + (int64_t)row0 * (E0.K >> 8) + cur.sb);
       }
       if constexpr (has_min(FMT)) {
         // A_ext: (m_0..m_7) at k = 0..7 and again at k = 8..15
@@ -873,7 +875,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1) q4k_tc_kernel(const __grid_c
         sx = dd.x * sigma;
         sy = -(dd.y * sigma * 64.f);
       } else if constexpr (FMT == kFmtNVFP4) {
-        sx = __ldg(static_cast<const float*>(P.aux)) * sigma;
+        sx = __ldg(static_cast<const float*>(P.aux[cur.e])) * sigma;
         sy = 0.f;
       } else if constexpr (FMT == kFmtQ6K) {
         sx = __half2float(__ushort_as_half((unsigned short)int4_scales)) * sigma;
@@ -1117,7 +1119,7 @@ SplitSpace split_space(int64_t N, int64_t K, const Split& s) {
 template <int FMT, int MPAD, int MAXE>
 cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split* sp, float* const* part,
                         unsigned* const* ctr, int count, int M, cudaStream_t stream) {
-  static TcParams<MAXE> par;
+  static TcParams<MAXE, naux(FMT, MAXE)> par;
   par.count = count;
   par.M = M;
   int tasks = 0;
@@ -1130,7 +1132,7 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
     tasks += tiles * sp[k].splits;
   }
   par.tasks_total = tasks;
-  par.aux = jobs[0].aux;
+  for (int k = 0; k < naux(FMT, MAXE) && k < count; ++k) par.aux[k] = jobs[k].aux;
   // Programmatic dependent launch: the kernel may start while the preparation kernel before it
   // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
   cudaLaunchConfig_t cfg{};
@@ -1179,12 +1181,8 @@ template <int MPAD, bool NAT>
 cudaError_t launch_prep(const std::vector<std::pair<const uint16_t*, int64_t>>& xs, const std::vector<uint8_t*>& outs,
                         unsigned* zero, size_t zero_words, int M, cudaStream_t stream) {
   if (xs.size() <= 1) return launch_prep_n<MPAD, 1, NAT>(xs, outs, zero, zero_words, M, stream);
-  if constexpr (NAT) {
-    return cudaErrorNotSupported;   // single products only
-  } else {
-    if (xs.size() <= 16) return launch_prep_n<MPAD, 16, NAT>(xs, outs, zero, zero_words, M, stream);
-    return launch_prep_n<MPAD, kMaxPrep, NAT>(xs, outs, zero, zero_words, M, stream);
-  }
+  if (xs.size() <= 16) return launch_prep_n<MPAD, 16, NAT>(xs, outs, zero, zero_words, M, stream);
+  return launch_prep_n<MPAD, kMaxPrep, NAT>(xs, outs, zero, zero_words, M, stream);
 }
 
 // Shared by the workspace and the no-allocation paths: prepare the distinct activations into
@@ -1213,21 +1211,18 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
   cudaError_t err = launch_prep<MPAD, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream);
   if (err != cudaSuccess) return err;
   if (count == 1) return launch_main<FMT, MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M, stream);
-  if constexpr (FMT != kFmtQ4K) {
-    return cudaErrorNotSupported;   // the other formats run single products
-  } else {
-    for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
-      err = launch_main<FMT, MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, sp.data() + k0, part.data() + k0,
-                                               ctr.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
-      if (err != cudaSuccess) return err;
-    }
-    return cudaSuccess;
+  for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
+    err = launch_main<FMT, MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, sp.data() + k0, part.data() + k0,
+                                             ctr.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
+    if (err != cudaSuccess) return err;
   }
+  return cudaSuccess;
 }
 
 template <int FMT, int MPAD>
 cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) {
-  static_assert(sizeof(TcParams<kMaxEBatch>) < 32000 && sizeof(PrepParams<kMaxPrep>) < 32000, "kernel parameters too large");
+  static_assert(sizeof(TcParams<kMaxEBatch, 1>) < 32000 && sizeof(PrepParams<kMaxPrep>) < 32000 &&
+                sizeof(TcParams<kMaxEBatch, kMaxEBatch>) <= 32764, "kernel parameters too large");   // the launch limit
   constexpr int kBB = bblock_bytes(MPAD);
   // distinct activations (an X pointer with its K) get one prepared block run each
   std::vector<std::pair<const uint16_t*, int64_t>> xs;
@@ -1353,7 +1348,6 @@ cudaError_t launch_tc(const Job* jobs, int count, int M, cudaStream_t stream) {
   const int fmt = jobs[0].fmt;
   for (int k = 1; k < count; ++k)
     if (jobs[k].fmt != fmt) return cudaErrorInvalidValue;   // one format per launch
-  if (fmt != kFmtQ4K && count != 1) return cudaErrorNotSupported;
   const bool narrow = M <= 16;
   switch (fmt) {
     case kFmtQ4K: return narrow ? launch_tc_t<kFmtQ4K, 16>(jobs, count, M, stream) : launch_tc_t<kFmtQ4K, 32>(jobs, count, M, stream);

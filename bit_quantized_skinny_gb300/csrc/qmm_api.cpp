@@ -279,6 +279,39 @@ qmm_status qmm_fmt_run(int fmt, const void* Wq_dev, int64_t N, int64_t K, const 
   return e == cudaSuccess ? QMM_OK : cuda_fail(e);
 }
 
+qmm_status qmm_fmt_run_batched(const qmm_fmt_entry* entries_host, int count, int M, cudaStream_t stream) {
+  if (!entries_host) return QMM_ERR_NULL;
+  if (count < 1 || count > QMM_MAX_BATCH) return QMM_ERR_COUNT;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  for (int k = 0; k < count; ++k) {
+    const qmm_fmt_entry& e = entries_host[k];
+    if (!valid_format(e.fmt)) return QMM_ERR_FORMAT;
+    qmm_status s = check_job(e.Wq, e.N, e.K, e.X, e.Y);
+    if (s != QMM_OK) return s;
+  }
+  q4k::Job jobs[QMM_MAX_BATCH];
+  for (int fmt = QMM_FMT_Q4K; fmt <= QMM_FMT_Q6K; ++fmt) {
+    int n = 0;
+    for (int k = 0; k < count; ++k) {
+      const qmm_fmt_entry& e = entries_host[k];
+      if (e.fmt != fmt) continue;
+      jobs[n] = q4k::Job{e.Wq, e.X, e.Y, e.N, e.K};
+      jobs[n].fmt = fmt;
+      jobs[n].aux = static_cast<const uint8_t*>(e.Wq) + q4k::fmt_aux_offset(fmt, e.N, e.K);
+      ++n;
+    }
+    if (n == 0) continue;
+    if (fmt == QMM_FMT_Q4K) {
+      qmm_status s = run_jobs(jobs, n, M, QMM_VARIANT_AUTO, stream);
+      if (s != QMM_OK) return s;
+    } else {
+      cudaError_t e = q4k::launch_tc(jobs, n, M, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+  }
+  return QMM_OK;
+}
+
 qmm_status qmm_fmt_dequant(int fmt, const void* Wq_dev, int64_t N, int64_t K, float* out_dev, cudaStream_t stream) {
   if (!valid_format(fmt)) return QMM_ERR_FORMAT;
   if (!Wq_dev || !out_dev) return QMM_ERR_NULL;

@@ -34,7 +34,7 @@ EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_de
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
            "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
            "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed",
-           "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant"]
+           "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant", "qmm_fmt_run_batched"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -50,6 +50,11 @@ class QmmError(RuntimeError):
 
 class _Entry(ctypes.Structure):
     _fields_ = [("Wq", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class _FmtEntry(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("Wq", ctypes.c_void_p), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
@@ -99,6 +104,8 @@ def load(path: str | None = None):
     lib.qmm_fmt_pack.restype = i32
     lib.qmm_fmt_run.argtypes = [i32, vp, i64, i64, vp, vp, i32, vp]
     lib.qmm_fmt_run.restype = i32
+    lib.qmm_fmt_run_batched.argtypes = [ctypes.POINTER(_FmtEntry), i32, i32, vp]
+    lib.qmm_fmt_run_batched.restype = i32
     lib.qmm_fmt_dequant.argtypes = [i32, vp, i64, i64, vp, vp]
     lib.qmm_fmt_dequant.restype = i32
     lib.qmm_device_status.argtypes = [ctypes.POINTER(u32)]
@@ -246,6 +253,20 @@ def fmt_run(fmt: int, Wq, N: int, K: int, X, Y, M: int | None = None, stream=Non
     st = load().qmm_fmt_run(fmt, ctypes.c_void_p(Wq.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()),
                             ctypes.c_void_p(Y.data_ptr()), M, _stream_handle(stream))
     _check(st, "qmm_fmt_run")
+
+
+def make_fmt_entries(items):
+    """items: sequence of (fmt, Wq, X, Y, N, K) with torch tensors or raw int pointers."""
+    arr = (_FmtEntry * len(items))()
+    for k, (fmt, Wq, X, Y, N, K) in enumerate(items):
+        ptr = lambda t: t if isinstance(t, int) else t.data_ptr()
+        arr[k] = _FmtEntry(fmt, ptr(Wq), ptr(X), ptr(Y), N, K)
+    return arr
+
+
+def fmt_run_batched(entries, M: int, stream=None):
+    """Independent products sharing M, weights in any formats: one launch per format present."""
+    _check(load().qmm_fmt_run_batched(entries, len(entries), M, _stream_handle(stream)), "qmm_fmt_run_batched")
 
 
 def fmt_dequant(fmt: int, Wq, N: int, K: int, out, stream=None):

@@ -274,8 +274,8 @@ qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64
  *         D > 0 ? clamp(rint(scale_j / D), 0, 63) : 0; q = D*sc_j > 0 ? clamp(rint(w / (D*sc_j)),
  *         -32, 31) + 32 : 32 (D = the value of d).
  *
- * The products run on the tensor cores (one launch per call; the CUDA-core kernel is Q4K's);
- * the other conventions are those of qmm_run.  Shapes: as for Q4K (K % 256 == 0). */
+ * The products run on the tensor cores (the CUDA-core kernel is Q4K's); the other conventions
+ * are those of qmm_run.  Shapes: as for Q4K (K % 256 == 0). */
 typedef enum {
   QMM_FMT_Q4K = 0,
   QMM_FMT_Q5K = 1,
@@ -299,6 +299,24 @@ qmm_status qmm_fmt_pack(int fmt, const float* W_host, int64_t N, int64_t K, void
  * qmm_run.  Errors as qmm_run, and QMM_ERR_FORMAT. */
 qmm_status qmm_fmt_run(int fmt, const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
                        float* Y_dev, int M, cudaStream_t stream);
+
+/* One entry of a batched call over weight formats: an independent product in format fmt. */
+typedef struct {
+  int fmt;             /* qmm_format code */
+  const void* Wq;      /* device, packed N x K in format fmt */
+  const uint16_t* X;   /* device, M x K bf16 */
+  float* Y;            /* device, M x N fp32 */
+  int64_t N;
+  int64_t K;
+} qmm_fmt_entry;
+
+/* Run `count` independent products sharing one M whose weights may be in different formats (a
+ * model file mixes k-quant widths, "sixi-asi 0.9", section "Numbers"): the entries are grouped
+ * by format and each group runs as qmm_run_batched does (one launch per format present, in
+ * order of format code, on `stream`).  Entries are validated as in qmm_fmt_run; the first
+ * invalid entry's error is returned and nothing is launched.  Each result equals the one of a
+ * single qmm_fmt_run call bit for bit. */
+qmm_status qmm_fmt_run_batched(const qmm_fmt_entry* entries_host, int count, int M, cudaStream_t stream);
 
 /* Test hook: out_dev[N x K] = the dequantized weights of format fmt, computed on the device
  * with the decode steps of the product kernel.  Bit-exact to the definitions above. */

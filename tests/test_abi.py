@@ -164,3 +164,15 @@ def test_fmt_argument_errors_need_no_gpu(qmm):
     assert lib.qmm_fmt_pack(5, W.ctypes.data_as(ctypes.c_void_p), 2, 256,
                             small.ctypes.data_as(ctypes.c_void_p), small.nbytes, 1) == 11
     assert lib.qmm_strerror(11) == b"unknown weight format code"
+
+
+def test_fmt_batched_argument_errors_need_no_gpu(qmm):
+    lib = qmm.load()
+    ok = (qmm.FMT_NVFP4, 16, 16, 16, 4, 256)
+    assert lib.qmm_fmt_run_batched(None, 1, 1, None) == 1
+    ents = qmm.make_fmt_entries([ok])
+    assert lib.qmm_fmt_run_batched(ents, 0, 1, None) == 8
+    assert lib.qmm_fmt_run_batched(ents, 1, 0, None) == 3
+    assert lib.qmm_fmt_run_batched(qmm.make_fmt_entries([ok, (7, 16, 16, 16, 4, 256)]), 2, 1, None) == 11
+    assert lib.qmm_fmt_run_batched(qmm.make_fmt_entries([ok, (qmm.FMT_Q6K, 16, 16, 16, 4, 300)]), 2, 1, None) == 2
+    assert lib.qmm_fmt_run_batched(qmm.make_fmt_entries([ok, (qmm.FMT_Q5K, 24, 16, 16, 4, 256)]), 2, 1, None) == 4

@@ -210,3 +210,59 @@ def test_full_size_sampled_rows(qmm, oracle_lib, fmt_name, name, N, K, Ms):
         assert_within(Y[:, rows], Yref, S, f"{fmt_name} {name} M={M}")
     del Wd
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ batched ------------------
+
+@pytest.mark.parametrize("fmt_name", FMTS)
+@pytest.mark.parametrize("M", [3, 8, 16, 32])
+def test_batched_equals_single_calls(qmm, oracle_lib, fmt_name, M):
+    """One launch over several products of one format (shared and distinct X, a product that a
+    single call splits along K) gives every product's single-call bits."""
+    fmt, ofmt = fmt_codes(qmm, oracle_lib, fmt_name)
+    shapes = [(1001, 2304), (300, 17408), (130, 5120), (64, 2560)]
+    Xs = {K: dev_x(inputs.activations_bf16_bits(M, K, 300 + K % 97)) for _, K in shapes}
+    X2 = dev_x(inputs.activations_bf16_bits(M, 2304, 999))
+    items, singles = [], []
+    for idx, (N, K) in enumerate(shapes + [(1001, 2304)]):
+        Wd = dev_bytes(packed(oracle_lib, ofmt, N, K, 41 if (N, K) == (1001, 2304) else 51 + N))
+        X = X2 if idx == len(shapes) else Xs[K]
+        Y = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+        items.append((fmt, Wd, X, Y, N, K))
+        singles.append(gpu_run(qmm, fmt, Wd, N, K, X, M))
+    qmm.fmt_run_batched(qmm.make_fmt_entries(items), M)
+    torch.cuda.synchronize()
+    assert qmm.device_status() == 0
+    for (f, Wd, X, Y, N, K), ys in zip(items, singles):
+        assert np.array_equal(Y.cpu().numpy().view(np.uint32), ys.view(np.uint32)), (N, K)
+
+
+def test_batched_many_entries_and_mixed_formats(qmm, oracle_lib):
+    """More entries than one launch takes (170 of one format), and every format in one call;
+    the Q4K entries go through the library's dispatcher and are checked against the oracle."""
+    M = 5
+    N, K = 128, 512
+    X = inputs.activations_bf16_bits(M, K, 55)
+    Xd = dev_x(X)
+    items, refs = [], []
+    for i in range(170):
+        Wq = oracle_lib.fmt_pack(oracle_lib.FMT_NVFP4, inputs.weights_f32(N, K, 1000 + i % 7))
+        Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        items.append((qmm.FMT_NVFP4, dev_bytes(Wq), Xd, Y, N, K))
+        refs.append(Wq)
+    for name in ["q4k", "q5k", "q6k", "int4", "q4k"]:
+        fmt, ofmt = fmt_codes(qmm, oracle_lib, name)
+        Wq = oracle_lib.fmt_pack(ofmt, inputs.weights_f32(N, K, 77 + fmt))
+        Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        items.append((fmt, dev_bytes(Wq), Xd, Y, N, K))
+        refs.append(Wq)
+    qmm.fmt_run_batched(qmm.make_fmt_entries(items), M)
+    torch.cuda.synchronize()
+    assert qmm.device_status() == 0
+    for (fmt, Wd, _, Y, _, _), Wq in zip(items, refs):
+        ofmt = fmt   # the format codes of the library and of the oracle agree
+        Yref, S = oracle_lib.fmt_matmul(ofmt, Wq, N, K, X)
+        assert_within(Y.cpu().numpy(), Yref, S, f"fmt {fmt}")
+        if fmt != qmm.FMT_Q4K:
+            ys = gpu_run(qmm, fmt, Wd, N, K, Xd, M)
+            assert np.array_equal(Y.cpu().numpy().view(np.uint32), ys.view(np.uint32))
