@@ -454,7 +454,18 @@ def run_ffn(args):
         ws = torch.empty(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
         fn = lambda: [qmm.run_ffn(g, d, F, K, X, Y, ws, M=M) for g, d in pairs]
         ms = time_steps(fn, max(2, args.steps // 5), 3, stream, lambda: None) / len(pairs)
+        # the same calls captured once into a CUDA graph and replayed: no host work per block
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()   # sizes the side stream's workspace before capture
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                fn()
+        stream.wait_stream(side)
+        ms_graph = time_steps(graph.replay, max(2, args.steps // 5), 3, stream, lambda: None) / len(pairs)
         res[str(M)] = {"us": round(ms * 1e3, 2), "gbps": round(weight_gbps(wbytes, ms), 1),
+                       "graph_us": round(ms_graph * 1e3, 2), "graph_gbps": round(weight_gbps(wbytes, ms_graph), 1),
                        "variants": [qmm.VARIANT_NAMES[qmm.select_variant(M, 2 * F, K)],
                                     qmm.VARIANT_NAMES[qmm.select_variant(M, K, F)]]}
         if qmm.device_status() != 0:
