@@ -1,4 +1,6 @@
-// q4k_tc.cu — tensor-core (tcgen05) variant of the skinny Q4K x bf16 product (sm_103a).
+// q4k_tc.cu — tensor-core (tcgen05) variant of the skinny product of packed weights x bf16
+// activations (sm_103a): Q4K, and through the FMT template the other weight formats (Q5K, Q6K,
+// NVFP4, INT4 with one scale per 128 columns; their decode steps are in q4k_formats.cuh).
 //
 // The skinny product of the pages' verify pass ("sixi-asi 0.9", section "What I got wrong in
 // 0.8") is a weight stream: every weight is read once and used by M <= 32 activation rows.  On
@@ -7,7 +9,7 @@
 // instruction per pair of weights, the same for every M.  That is the M-dependent tiling of the
 // pages (a matrix kernel from a few rows on, section "The patch") done with GB300's units.
 //
-// Operands ("swap AB": the 128-row MMA dimension runs over weight rows):
+// Operands ("swap AB": the 128-row MMA dimension runs over weight rows), described for Q4K:
 //   A[128 rows x 16 k] fp16 in tensor memory (TMEM): A = sc_j * q_t, an integer <= 945, exact.
 //     Written by the dequant warps with tcgen05.st, one thread per weight row (lane).
 //   B[16 k x Mpad] fp16 in shared memory: the activations of one super-block, x * 2^-s with one
@@ -18,6 +20,10 @@
 //   dmin term also comes from the tensor cores.  The epilogue forms, per super-block,
 //     y += (D*2^s) * acc - (Dm*2^s*64) * acc_ext
 //   in fp32 registers.  Products in the MMAs are exact; only fp32 accumulation rounds.
+//   The other formats keep A exact in fp16 too (Q5K sc*q <= 1953; Q6K sc*(q-32) <= 2048 with
+//   7-bit scales; NVFP4 s*v, at most 6 significant bits; INT4 q itself) and differ in the
+//   epilogue: NVFP4 and Q6K have one accumulator (factor g*2^s or d*2^s), INT4 one per K half
+//   (its two scale groups), Q5K the Q4K pair.
 //
 // K order inside a super-block: the nibble trick below yields the quants of one 32-bit word as
 // fp16 pairs (q0,q4) (q1,q5) (q2,q6) (q3,q7); TMEM column 4w+c holds k = 8w+c (low half) and
@@ -35,11 +41,12 @@
 //                one accumulator in TMEM.  Per super-block: read the stage, write the A slot one
 //                K half at a time (each half handed to the MMA lane as soon as it is written),
 //                wait for the MMAs, read the accumulator and scale it into y.
-//   copy warp    per super-block one 2D TMA tile copy of the weights (128 rows x 144 bytes) and
-//                one bulk copy of the prepared activation block into a stage of an 8-deep ring
-//                (6 at Mpad 32), in the CTA's super-block order: rounds over the groups.
-//   MMA warp     owns TMEM; one elected lane issues each super-block's 17 MMAs (8 per K half and
-//                one for the dmin term) in the same order.  Issuing from an elect.sync branch
+//   copy warp    per super-block one 2D TMA tile copy of the weights (128 rows x the format's
+//                bytes per 256 weights) and one bulk copy of the prepared activation block into
+//                a stage of the ring (8 stages for 8 token columns, 7 for 16, 5 for 32; fewer for
+//                the wider formats), in the CTA's super-block order: rounds over the groups.
+//   MMA warp     owns TMEM; one elected lane issues each super-block's MMAs (8 per K half, and
+//                one for the dmin term of the k-quants) in the same order.  Issuing from an elect.sync branch
 //                keeps the operands in uniform registers (~14 cycles per MMA).
 // Every barrier is waited on only by threads that see all of its phases in order (a parity wait
 // is exact only then): full barriers per (group, stage), handoff and completion barriers per
