@@ -65,9 +65,23 @@ CostModel model(const q4k::Job* jobs, int count, int M) {
   return c;
 }
 
+// QMM_FORCE_VARIANT=fma|tc (read once): every automatic choice takes that family instead of
+// the cost model's (for tests and benchmarks; any other value is ignored).
+int forced_variant() {
+  static const int v = [] {
+    const char* e = std::getenv("QMM_FORCE_VARIANT");
+    if (!e) return QMM_VARIANT_AUTO;
+    if (std::strcmp(e, "fma") == 0) return QMM_VARIANT_FMA;
+    if (std::strcmp(e, "tc") == 0) return QMM_VARIANT_TC;
+    return QMM_VARIANT_AUTO;
+  }();
+  return v;
+}
+
 int select_variant_jobs(const q4k::Job* jobs, int count, int M) {
   for (int k = 0; k < count; ++k)
     if (!q4k::tc_supports(M, jobs[k].N, jobs[k].K)) return QMM_VARIANT_FMA;
+  if (forced_variant() != QMM_VARIANT_AUTO) return forced_variant();
   const CostModel c = model(jobs, count, M);
   return (c.tc_us < c.fma_us) ? QMM_VARIANT_TC : QMM_VARIANT_FMA;
 }

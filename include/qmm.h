@@ -157,7 +157,9 @@ typedef enum {
 qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
                            float* Y_dev, int M, int variant, cudaStream_t stream);
 
-/* The variant qmm_run uses for this shape (never QMM_VARIANT_AUTO). */
+/* The variant qmm_run uses for this shape (never QMM_VARIANT_AUTO).  The environment variable
+ * QMM_FORCE_VARIANT=fma or =tc, read once per process, makes every automatic choice take that
+ * family (for tests and benchmarks). */
 int qmm_select_variant(int M, int64_t N, int64_t K);
 
 /* The variant qmm_run_batched uses for these entries (one family runs the whole batch);

@@ -176,3 +176,23 @@ def test_fmt_batched_argument_errors_need_no_gpu(qmm):
     assert lib.qmm_fmt_run_batched(qmm.make_fmt_entries([ok, (7, 16, 16, 16, 4, 256)]), 2, 1, None) == 11
     assert lib.qmm_fmt_run_batched(qmm.make_fmt_entries([ok, (qmm.FMT_Q6K, 16, 16, 16, 4, 300)]), 2, 1, None) == 2
     assert lib.qmm_fmt_run_batched(qmm.make_fmt_entries([ok, (qmm.FMT_Q5K, 24, 16, 16, 4, 256)]), 2, 1, None) == 4
+
+
+def test_force_variant_environment_override(qmm):
+    """QMM_FORCE_VARIANT=fma|tc overrides the automatic choice (read once per process, so each
+    setting runs in a fresh interpreter; no GPU needed to ask for the choice)."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); from bit_quantized_skinny_gb300 import qmm; "
+            "print(qmm.select_variant(8, 248320, 5120), qmm.select_variant(1, 1024, 5120))") % ROOT
+    picks = {}
+    for val in (None, "fma", "tc", "bogus"):
+        env = dict(os.environ)
+        env.pop("QMM_FORCE_VARIANT", None)
+        if val:
+            env["QMM_FORCE_VARIANT"] = val
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+        picks[val] = tuple(int(v) for v in out.stdout.split())
+    assert picks["fma"] == (qmm.VARIANT_FMA, qmm.VARIANT_FMA)
+    assert picks["tc"] == (qmm.VARIANT_TC, qmm.VARIANT_TC)
+    assert picks["bogus"] == picks[None]
