@@ -26,7 +26,8 @@ def qmm():
 
 
 def dev_bytes(host_u8):
-    return torch.from_numpy(np.ascontiguousarray(host_u8)).cuda()
+    a = np.ascontiguousarray(host_u8)
+    return torch.from_numpy(a if a.flags.writeable else a.copy()).cuda()
 
 
 def dev_x(bits):
