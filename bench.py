@@ -464,8 +464,22 @@ def run_ffn(args):
                 fn()
         stream.wait_stream(side)
         ms_graph = time_steps(graph.replay, max(2, args.steps // 5), 3, stream, lambda: None) / len(pairs)
+        # the fused block (gating in the gate/up epilogue; the weights read as row-interleaved:
+        # the same bytes, so the same work)
+        wsf = torch.empty(qmm.ffn_fused_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
+        fnf = lambda: [qmm.run_ffn_fused(g, d, F, K, X, Y, wsf, M=M) for g, d in pairs]
+        ms_f = time_steps(fnf, max(2, args.steps // 5), 3, stream, lambda: None) / len(pairs)
+        with torch.cuda.stream(side):
+            fnf()
+            graph_f = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_f, stream=side):
+                fnf()
+        stream.wait_stream(side)
+        ms_fg = time_steps(graph_f.replay, max(2, args.steps // 5), 3, stream, lambda: None) / len(pairs)
         res[str(M)] = {"us": round(ms * 1e3, 2), "gbps": round(weight_gbps(wbytes, ms), 1),
                        "graph_us": round(ms_graph * 1e3, 2), "graph_gbps": round(weight_gbps(wbytes, ms_graph), 1),
+                       "fused_us": round(ms_f * 1e3, 2), "fused_graph_us": round(ms_fg * 1e3, 2),
+                       "fused_graph_gbps": round(weight_gbps(wbytes, ms_fg), 1),
                        "variants": [qmm.VARIANT_NAMES[qmm.select_variant(M, 2 * F, K)],
                                     qmm.VARIANT_NAMES[qmm.select_variant(M, K, F)]]}
         if qmm.device_status() != 0:

@@ -20,6 +20,9 @@ struct Job {
   int64_t K;
   int fmt = kFmtQ4K;
   const void* aux = nullptr;
+  // gated: rows 2f and 2f+1 are the gate and up rows of output f; Y is then the bf16 matrix
+  // H[M x N/2] = bf16(silu(gate) * up) instead of the fp32 product (tensor cores, no K split)
+  bool gated = false;
 };
 
 // Launch the CUDA-core (fma) kernel over `count` jobs sharing M, in one launch.

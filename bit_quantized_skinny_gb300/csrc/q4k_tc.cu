@@ -73,6 +73,7 @@
 #include <vector>
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "q4k_device.cuh"
@@ -212,7 +213,7 @@ struct TcParams {
   int count;
   int M;
   int tasks_total;
-  int pad_;
+  int gated;   // one product whose row pairs (2f, 2f+1) are (gate f, up f): Y holds bf16 H[M x N/2]
   const void* aux[NAUX];
 };
 __host__ __device__ constexpr int naux(int f, int maxe) { return f == kFmtQ4K ? 1 : maxe; }
@@ -361,6 +362,25 @@ __device__ __noinline__ void reduce_chunks(const float* part, int chunks, int M,
 #pragma unroll
     for (int k = 0; k < MT; ++k)
       if (k < M) y[(int64_t)k * N] = v[k];
+  }
+}
+
+// The feed-forward gating of a finished task whose running sums are in shared memory (token k
+// of this thread's row at ysum[k * 128]): lanes r and r ^ 1 hold rows 2f (gate) and 2f+1 (up);
+// the even lane stores bf16(silu(gate) * up) to H[k][f], silu(g) = g / (1 + e^-g), fp32 then
+// one round to nearest even.  Out of line: it runs once per task and would otherwise take
+// registers from the hot loop.
+template <int MT>
+__device__ __noinline__ void gate_store_smem(const float* ysum, int r, int row, int N, int M, uint16_t* H) {
+  const int64_t F = N >> 1;
+  for (int k = 0; k < MT; ++k) {
+    const float mine = ysum[k * kTileRows];
+    const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+    if (k < M && !(r & 1) && row < N) {
+      const float h = mine / (1.0f + expf(-mine)) * other;
+      const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+      H[(int64_t)k * F + (row >> 1)] = *reinterpret_cast<const uint16_t*>(&hb);
+    }
   }
 }
 
@@ -940,7 +960,27 @@ __global__ void __launch_bounds__(threads(MPAD), 1)
       }
       if (task_end) {
         const int row = tile * kTileRows + r;
-        if (E.splits == 1) {
+        if (E.splits == 1 && P.gated) {
+          // the feed-forward gating in the epilogue: lane r holds row 2f (gate) or 2f+1 (up) of
+          // the same tile; the even lane forms silu(gate) * up in fp32 and stores its bf16
+          // (round to nearest even), silu(g) = g / (1 + e^-g)
+          uint16_t* H = reinterpret_cast<uint16_t*>(E.Y);
+          if constexpr (kYtotSmem) {
+            gate_store_smem<MT>(ytot_s, r, row, E.N, P.M, H);
+          } else {
+            const int64_t F = E.N >> 1;
+#pragma unroll
+            for (int k = 0; k < MT; ++k) {
+              const float mine = ytot(k);
+              const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+              if (k < P.M && !(r & 1) && row < E.N) {
+                const float h = mine / (1.0f + expf(-mine)) * other;
+                const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+                H[(int64_t)k * F + (row >> 1)] = *reinterpret_cast<const uint16_t*>(&hb);
+              }
+            }
+          }
+        } else if (E.splits == 1) {
           if (row < E.N) {
 #pragma unroll
             for (int k = 0; k < MT; ++k)
@@ -1139,6 +1179,7 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
     tasks += tiles * sp[k].splits;
   }
   par.tasks_total = tasks;
+  par.gated = (count == 1 && jobs[0].gated) ? 1 : 0;
   for (int k = 0; k < naux(FMT, MAXE) && k < count; ++k) par.aux[k] = jobs[k].aux;
   // Programmatic dependent launch: the kernel may start while the preparation kernel before it
   // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
@@ -1251,7 +1292,7 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
   std::vector<Split> sp(count);
   size_t split_bytes = 0, zero_words = 0;
   for (int k = 0; k < count; ++k) {
-    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, count > 1);
+    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, count > 1 || jobs[k].gated);   // gating needs whole rows
     const SplitSpace s = split_space<MPAD>(jobs[k].N, jobs[k].K, sp[k]);
     split_bytes += s.partial_bytes;
     zero_words += s.counter_words;

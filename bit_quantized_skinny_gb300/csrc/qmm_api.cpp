@@ -192,6 +192,30 @@ qmm_status qmm_run_ffn(const void* Wgu_dev, const void* Wdown_dev, int64_t F, in
   return run_jobs(&down, 1, M, QMM_VARIANT_AUTO, stream);
 }
 
+size_t qmm_ffn_fused_workspace_bytes(int M, int64_t F) {
+  if (M < 1 || M > QMM_MAX_M || check_shape(1, F) != QMM_OK) return 0;
+  return ((size_t)M * (size_t)F * sizeof(uint16_t) + 15) & ~(size_t)15;
+}
+
+qmm_status qmm_run_ffn_fused(const void* Wgu_dev, const void* Wdown_dev, int64_t F, int64_t K, const uint16_t* X_dev,
+                             float* Y_dev, int M, void* workspace_dev, size_t workspace_bytes, cudaStream_t stream) {
+  if (!workspace_dev) return QMM_ERR_NULL;
+  qmm_status s = check_job(Wgu_dev, 2 * F, K, X_dev, Y_dev);
+  if (s != QMM_OK) return s;
+  s = check_job(Wdown_dev, K, F, X_dev, Y_dev);
+  if (s != QMM_OK) return s;
+  if (M < 1 || M > QMM_MAX_M) return QMM_ERR_M_RANGE;
+  if (!aligned(workspace_dev, 16)) return QMM_ERR_ALIGN;
+  if (workspace_bytes < qmm_ffn_fused_workspace_bytes(M, F)) return QMM_ERR_BUFSIZE;
+  uint16_t* H = static_cast<uint16_t*>(workspace_dev);
+  q4k::Job gate_up{Wgu_dev, X_dev, reinterpret_cast<float*>(H), 2 * F, K};
+  gate_up.gated = true;
+  cudaError_t e = q4k::launch_tc(&gate_up, 1, M, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const q4k::Job down{Wdown_dev, H, Y_dev, K, F};
+  return run_jobs(&down, 1, M, QMM_VARIANT_AUTO, stream);
+}
+
 // Indexed-expert product.  Workspace: the gathered activation rows (M rows, then M rows of
 // zeros that the last expert's block may read past its own rows) and the gathered results
 // (used experts x rows of the largest expert; at most (M+1)^2/4 blocks of rows).

@@ -34,7 +34,8 @@ EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_de
            "qmm_run_variant", "qmm_select_variant", "qmm_device_status", "qmm_strerror",
            "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
            "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed",
-           "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant", "qmm_fmt_run_batched"]
+           "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant", "qmm_fmt_run_batched",
+           "qmm_ffn_fused_workspace_bytes", "qmm_run_ffn_fused"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -93,6 +94,10 @@ def load(path: str | None = None):
     lib.qmm_ffn_workspace_bytes.restype = ctypes.c_size_t
     lib.qmm_run_ffn.argtypes = [vp, vp, i64, i64, vp, vp, i32, vp, ctypes.c_size_t, vp]
     lib.qmm_run_ffn.restype = i32
+    lib.qmm_ffn_fused_workspace_bytes.argtypes = [i32, i64]
+    lib.qmm_ffn_fused_workspace_bytes.restype = ctypes.c_size_t
+    lib.qmm_run_ffn_fused.argtypes = [vp, vp, i64, i64, vp, vp, i32, vp, ctypes.c_size_t, vp]
+    lib.qmm_run_ffn_fused.restype = i32
     lib.qmm_indexed_workspace_bytes.argtypes = [i32, i64, i64]
     lib.qmm_indexed_workspace_bytes.restype = ctypes.c_size_t
     lib.qmm_run_indexed.argtypes = [ctypes.POINTER(vp), i32, i64, i64, ctypes.POINTER(ctypes.c_int32), vp, vp, i32,
@@ -204,6 +209,23 @@ def run_ffn(Wgu, Wdown, F: int, K: int, X, Y, workspace, M: int | None = None, s
                             ctypes.c_void_p(X.data_ptr()), ctypes.c_void_p(Y.data_ptr()), M,
                             ctypes.c_void_p(workspace.data_ptr()), nbytes, _stream_handle(stream))
     _check(st, "qmm_run_ffn")
+
+
+def ffn_fused_workspace_bytes(M: int, F: int) -> int:
+    return load().qmm_ffn_fused_workspace_bytes(M, F)
+
+
+def run_ffn_fused(Wgu_interleaved, Wdown, F: int, K: int, X, Y, workspace, M: int | None = None, stream=None):
+    """The feed-forward block with the gating in the gate/up product's epilogue.  Wgu_interleaved:
+    packed (2F) x K weights with row 2f = gate row f and row 2f+1 = up row f.  `workspace`: a
+    device tensor of >= ffn_fused_workspace_bytes(M, F) bytes (holds H)."""
+    if M is None:
+        M = X.shape[0]
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load().qmm_run_ffn_fused(ctypes.c_void_p(Wgu_interleaved.data_ptr()), ctypes.c_void_p(Wdown.data_ptr()),
+                                  F, K, ctypes.c_void_p(X.data_ptr()), ctypes.c_void_p(Y.data_ptr()), M,
+                                  ctypes.c_void_p(workspace.data_ptr()), nbytes, _stream_handle(stream))
+    _check(st, "qmm_run_ffn_fused")
 
 
 def indexed_workspace_bytes(M: int, N: int, K: int) -> int:

@@ -211,6 +211,18 @@ size_t qmm_ffn_workspace_bytes(int M, int64_t F);
 qmm_status qmm_run_ffn(const void* Wgu_dev, const void* Wdown_dev, int64_t F, int64_t K, const uint16_t* X_dev,
                        float* Y_dev, int M, void* workspace_dev, size_t workspace_bytes, cudaStream_t stream);
 
+/* The same block with the gating fused into the gate/up product's epilogue (no G in memory, one
+ * launch fewer): Wgu_dev holds the gate and up rows interleaved, row 2f = gate row f and row
+ * 2f+1 = up row f, so that each pair sits in neighbouring lanes of the kernel; H is formed from
+ * the fp32 results of the pair exactly as qmm_run_ffn forms it from G.  The gate/up product
+ * always runs on the tensor cores and is never split along K; the down product is chosen as in
+ * qmm_run.  workspace_dev (16-byte aligned) holds H: at least qmm_ffn_fused_workspace_bytes(M, F)
+ * bytes.  Errors as qmm_run_ffn. */
+size_t qmm_ffn_fused_workspace_bytes(int M, int64_t F);
+qmm_status qmm_run_ffn_fused(const void* Wgu_interleaved_dev, const void* Wdown_dev, int64_t F, int64_t K,
+                             const uint16_t* X_dev, float* Y_dev, int M, void* workspace_dev,
+                             size_t workspace_bytes, cudaStream_t stream);
+
 /* Indexed-expert product (the matrix-product-by-id case that the pages' backend op tests cover
  * next to the plain product: "sixi-asi 0.9", section "The patch", MUL_MAT and MUL_MAT_ID): row i
  * of X is multiplied by the weight matrix of expert ids_host[i],

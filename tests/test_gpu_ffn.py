@@ -83,3 +83,65 @@ def test_ffn_argument_errors(qmm):
         qmm.run_ffn(W, W, F, K, X, Y, small, M=M)
     assert ei.value.status == 5   # QMM_ERR_BUFSIZE
     assert qmm.ffn_workspace_bytes(M, 100) == 0   # F not a multiple of 256
+
+
+def _interleave_rows(packed, F, K):
+    """Packed (2F) x K Q4K rows (gate 0..F-1, up F..2F-1) -> rows 2f = gate f, 2f+1 = up f."""
+    rows = packed.reshape(2 * F, (K // 256) * 144)
+    out = np.empty_like(rows)
+    out[0::2] = rows[:F]
+    out[1::2] = rows[F:]
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("F,K,Ms", [(512, 256, [1, 3, 8]), (768, 512, [16, 32]), (1536, 1024, [2, 9, 24])])
+def test_fused_ffn_matches_the_chain(qmm, oracle_lib, F, K, Ms):
+    """qmm_run_ffn_fused on the row-interleaved gate/up matrix: H is the SwiGLU of the gate/up
+    product's fp32 results (checked against the oracle's fp64 SwiGLU of the tensor-core product
+    of the same rows, within one bf16 step and nearly always identical), equal bit for bit to
+    the unfused chain's H whenever that chain's gate/up product runs on the tensor cores too, and
+    Y is the down product of H."""
+    Wgu = oracle_lib.pack(inputs.weights_f32(2 * F, K, 710 + F))
+    Wdn = oracle_lib.pack(inputs.weights_f32(K, F, 810 + F))
+    Wgu_d, Wint_d, Wdn_d = _dev_bytes(Wgu), _dev_bytes(_interleave_rows(Wgu, F, K)), _dev_bytes(Wdn)
+    for M in Ms:
+        X = inputs.activations_bf16_bits(M, K, 910 + M)
+        Xd = _dev_x(X)
+        Yf = torch.full((M, K), 7.0, dtype=torch.float32, device="cuda")
+        wsf = torch.full((qmm.ffn_fused_workspace_bytes(M, F),), 255, dtype=torch.uint8, device="cuda")
+        qmm.run_ffn_fused(Wint_d, Wdn_d, F, K, Xd, Yf, wsf, M=M)
+        Gtc = torch.empty((M, 2 * F), dtype=torch.float32, device="cuda")
+        qmm.run(Wgu_d, 2 * F, K, Xd, Gtc, M=M, variant=qmm.VARIANT_TC)
+        Yu = torch.full((M, K), 7.0, dtype=torch.float32, device="cuda")
+        wsu = torch.zeros(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
+        qmm.run_ffn(Wgu_d, Wdn_d, F, K, Xd, Yu, wsu, M=M)
+        torch.cuda.synchronize()
+        assert qmm.device_status() == 0
+        Hf = wsf.cpu().numpy()[:M * F * 2].view(np.uint16).reshape(M, F)
+        G = Gtc.cpu().numpy()
+        Gref, SG = oracle_lib.matmul(Wgu, 2 * F, K, X)
+        _within(G, Gref, SG, f"gate/up M={M}")
+        href = oracle_lib.swiglu(G.astype(np.float64), F)
+        step = np.ldexp(1.0, np.frexp(np.abs(href))[1] - 8)
+        assert np.all(np.abs(_bf16_to_f64(Hf) - href) <= step), f"fused H off by more than one bf16 step, M={M}"
+        assert np.mean(Hf == oracle_lib.bf16_round(href)) > 0.99
+        if qmm.select_variant(M, 2 * F, K) == qmm.VARIANT_TC:
+            g_bytes = (M * 2 * F * 4 + 15) // 16 * 16
+            Hu = wsu.cpu().numpy()[g_bytes:g_bytes + M * F * 2].view(np.uint16).reshape(M, F)
+            assert np.array_equal(Hf, Hu), f"fused and chained H differ, M={M}"
+            assert torch.equal(Yf.view(torch.int32), Yu.view(torch.int32))
+        Yref, SY = oracle_lib.matmul(Wdn, K, F, Hf)
+        _within(Yf.cpu().numpy(), Yref, SY, f"fused down M={M}")
+
+
+def test_fused_ffn_argument_errors(qmm):
+    F, K, M = 256, 256, 2
+    W = torch.zeros(2 * F * (K // 256) * 144, dtype=torch.uint8, device="cuda")
+    X = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros((M, K), device="cuda")
+    small = torch.zeros(qmm.ffn_fused_workspace_bytes(M, F) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.run_ffn_fused(W, W, F, K, X, Y, small, M=M)
+    assert ei.value.status == 5
+    assert qmm.ffn_fused_workspace_bytes(M, 100) == 0
+    assert qmm.ffn_fused_workspace_bytes(M, F) == M * F * 2
