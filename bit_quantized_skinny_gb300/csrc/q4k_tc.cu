@@ -606,8 +606,9 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
 
 // FMT: weight format.  MPAD: MMA width (token columns of B and of the accumulators, 16 or 32).
 // MT: the token columns the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M
-// hold zeros.
-template <int FMT, int MPAD, int MT, int MAXE>
+// hold zeros.  GATED: the feed-forward gating in the epilogue (a separate instance: its code in
+// the regular kernels measured 2.5 % slower at M <= 8).
+template <int FMT, int MPAD, int MT, int MAXE, bool GATED>
 __global__ void __launch_bounds__(threads(MPAD), 1)
     q4k_tc_kernel(const __grid_constant__ TcParams<MAXE, naux(FMT, MAXE)> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
@@ -960,7 +961,7 @@ __global__ void __launch_bounds__(threads(MPAD), 1)
       }
       if (task_end) {
         const int row = tile * kTileRows + r;
-        if (E.splits == 1 && P.gated) {
+        if constexpr (GATED) {
           // the feed-forward gating in the epilogue: lane r holds row 2f (gate) or 2f+1 (up) of
           // the same tile; the even lane forms silu(gate) * up in fp32 and stores its bf16
           // (round to nearest even), silu(g) = g / (1 + e^-g)
@@ -1097,14 +1098,14 @@ cudaError_t weight_map(const void* W, int64_t N, int64_t K, int fmt, CUtensorMap
   return cudaSuccess;
 }
 
-template <int FMT, int MPAD, int MT, int MAXE>
+template <int FMT, int MPAD, int MT, int MAXE, bool GATED>
 cudaError_t set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(q4k_tc_kernel<FMT, MPAD, MT, MAXE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(q4k_tc_kernel<FMT, MPAD, MT, MAXE, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TcSmem<MPAD, FMT, MT>::kTotal);
   if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return err;
@@ -1192,18 +1193,36 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if constexpr (FMT == kFmtQ4K && MAXE == 1) {
+    if (par.gated) {   // one product split into no tasks along K (split_for with whole rows)
+      if constexpr (MPAD == 16) {
+        if (M <= 8) {
+          cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE, true>();
+          if (err != cudaSuccess) return err;
+          cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
+          return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE, true>, par);
+        }
+      }
+      cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE, true>();
+      if (err != cudaSuccess) return err;
+      cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
+      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE, true>, par);
+    }
+  } else {
+    if (par.gated) return cudaErrorNotSupported;   // the gated epilogue is Q4K's, single products
+  }
   if constexpr (MPAD == 16) {
     if (M <= 8) {
-      cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE>();
+      cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE, false>();
       if (err != cudaSuccess) return err;
       cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
-      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE>, par);
+      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE, false>, par);
     }
   }
-  cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE>();
+  cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE, false>();
   if (err != cudaSuccess) return err;
   cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
-  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE>, par);
+  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE, false>, par);
 }
 
 template <int MPAD, int NX, bool NAT>
