@@ -34,8 +34,9 @@
 // of k) and the chunk sums are added in chunk order; splits cut only at chunk boundaries, so a
 // product's bits depend neither on M nor on how its work is split or batched.  One CTA per SM.
 //
-// Roles (448 threads at Mpad 16, 320 at Mpad 32):
-//   dequant groups (3 at Mpad 16, 2 at Mpad 32; 4 warps each, warp q <-> TMEM lanes 32q..32q+31,
+// Roles (448 threads at Mpad 16, 320 at Mpad 32; 448 for the one-accumulator formats):
+//   dequant groups (3 at Mpad 16, 2 at Mpad 32 -- 3 for NVFP4 and Q6K, whose groups own one
+//                accumulator block instead of two; 4 warps each, warp q <-> TMEM lanes 32q..32q+31,
 //                the rows of the tile).  The CTA's tasks are dealt to the groups round robin; a
 //                group walks its tasks' super-blocks in order.  Each group owns one A slot and
 //                one accumulator in TMEM.  Per super-block: read the stage, write the A slot one
@@ -91,11 +92,15 @@ __device__ unsigned g_status;   // this file's kernels' status word
 constexpr int kTileRows = 128;
 constexpr int kGroupWarps = 4;     // a dequant group: one warp per TMEM lane quarter (32 rows)
 constexpr int kMaxGroups = 3;
-// Dequant groups: three at Mpad 16, two at Mpad 32 (what tensor memory holds, below).  With the
-// copy and MMA warps that is at most 14 warps, at most 4 per SM sub-partition, which leaves each
-// thread 128 registers (a sub-partition holds 16384).
-__host__ __device__ constexpr int groups(int mpad) { return mpad <= 16 ? 3 : 2; }
-__host__ __device__ constexpr int threads(int mpad) { return 32 * (groups(mpad) * kGroupWarps + 2); }
+// Dequant groups: three at Mpad 16, two at Mpad 32 (what tensor memory holds, below) -- three
+// for the formats with one accumulator block per group.  With the copy and MMA warps that is at
+// most 14 warps, at most 4 per SM sub-partition, which leaves each thread 128 registers (a
+// sub-partition holds 16384).
+// The formats with one accumulator block per group (no dmin term, one scale group per
+// super-block).
+__host__ __device__ constexpr bool single_acc(int f) { return f == kFmtNVFP4 || f == kFmtQ6K; }
+__host__ __device__ constexpr int groups(int mpad, int f = kFmtQ4K) { return (mpad <= 16 || single_acc(f)) ? 3 : 2; }
+__host__ __device__ constexpr int threads(int mpad, int f = kFmtQ4K) { return 32 * (groups(mpad, f) * kGroupWarps + 2); }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
@@ -134,9 +139,13 @@ constexpr uint32_t kACols = 136;
 // only ever cuts at chunk boundaries, so the bits of a product do not depend on the split.
 constexpr int kChunkSb = 4;
 __host__ __device__ constexpr uint32_t a_col(int g) { return kACols * g; }
-__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g) { return 512u - 2u * mpad * groups(mpad) + 2u * mpad * g; }
-__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g) { return acc1_col(mpad, g) + mpad; }
-static_assert(a_col(groups(16)) <= acc1_col(16, 0) && a_col(groups(32)) <= acc1_col(32, 0),
+__host__ __device__ constexpr uint32_t acc_cols(int mpad, int f) { return single_acc(f) ? mpad : 2u * mpad; }
+__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f = kFmtQ4K) {
+  return 512u - acc_cols(mpad, f) * groups(mpad, f) + acc_cols(mpad, f) * g;
+}
+__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f = kFmtQ4K) { return acc1_col(mpad, g, f) + mpad; }
+static_assert(a_col(groups(16)) <= acc1_col(16, 0) && a_col(groups(32)) <= acc1_col(32, 0) &&
+              a_col(groups(32, kFmtNVFP4)) <= acc1_col(32, 0, kFmtNVFP4),
               "TMEM column plan overlaps");
 
 // Barrier indices inside the barrier block.  Every barrier is waited on by threads that see
@@ -156,10 +165,10 @@ enum : int {
 // With 16 or 32 token columns each group's running sum of chunk sums (MT tokens x 128 rows of
 // fp32) lives in shared memory, not in registers (there it spilled); it is touched once per
 // chunk of 4 super-blocks.
-__host__ __device__ constexpr int ytot_bytes(int mpad, int mt) { return mt >= 16 ? groups(mpad) * mt * kTileRows * 4 : 0; }
+__host__ __device__ constexpr int ytot_bytes(int mpad, int mt, int f = kFmtQ4K) { return mt >= 16 ? groups(mpad, f) * mt * kTileRows * 4 : 0; }
 // Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens).
 __host__ __device__ constexpr int stages_fit(int mpad, int f, int mt) {
-  return (kSmemLimit - ytot_bytes(mpad, mt) - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+  return (kSmemLimit - ytot_bytes(mpad, mt, f) - kNumBars * 8 - 32) / stage_bytes(mpad, f);
 }
 __host__ __device__ constexpr int stages(int mpad, int f, int mt) {
   return stages_fit(mpad, f, mt) < (mpad <= 16 ? 8 : 5) ? stages_fit(mpad, f, mt) : (mpad <= 16 ? 8 : 5);
@@ -169,7 +178,7 @@ template <int MPAD, int FMT, int MT>
 struct TcSmem {
   static constexpr int kW = 0;
   static constexpr int kYtot = kW + stages(MPAD, FMT, MT) * stage_bytes(MPAD, FMT);
-  static constexpr int kBars = kYtot + ytot_bytes(MPAD, MT);
+  static constexpr int kBars = kYtot + ytot_bytes(MPAD, MT, FMT);
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
@@ -609,12 +618,12 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
 // hold zeros.  GATED: the feed-forward gating in the epilogue (a separate instance: its code in
 // the regular kernels measured 2.5 % slower at M <= 8).
 template <int FMT, int MPAD, int MT, int MAXE, bool GATED>
-__global__ void __launch_bounds__(threads(MPAD), 1)
+__global__ void __launch_bounds__(threads(MPAD, FMT), 1)
     q4k_tc_kernel(const __grid_constant__ TcParams<MAXE, naux(FMT, MAXE)> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = TcSmem<MPAD, FMT, MT>;
-  constexpr int NG = groups(MPAD);
+  constexpr int NG = groups(MPAD, FMT);
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
   constexpr int kMmaWarp = kProdWarp + 1;       // MMA issue; owns TMEM
   constexpr int kBB = bblock_bytes(MPAD);
@@ -739,14 +748,14 @@ __global__ void __launch_bounds__(threads(MPAD), 1)
             gbits ^= bit;
             tc::fence_after_sync();
             const uint64_t bdesc = tc::smem_desc_kmajor(sW + ws * kSB + kWSB, 128, 4096);   // + 16 per MMA: 256 bytes
-            tc::mma_f16_ts_x8(tmem + acc1_col(MPAD, g), tmem + a_col(g), bdesc, 16, idesc, 0);
+            tc::mma_f16_ts_x8(tmem + acc1_col(MPAD, g, FMT), tmem + a_col(g), bdesc, 16, idesc, 0);
             ok = wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u);
           }
           if (ok && i < n[g]) {
             tc::fence_after_sync();
             const uint32_t abase = tmem + a_col(g);
-            const uint32_t d1 = tmem + acc1_col(MPAD, g);
-            const uint32_t d2 = tmem + acc2_col(MPAD, g);
+            const uint32_t d1 = tmem + acc1_col(MPAD, g, FMT);
+            const uint32_t d2 = tmem + acc2_col(MPAD, g, FMT);
             const uint32_t bslot = sW + ws * kSB + kWSB;
             const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);
             if constexpr (FMT == kFmtINT4) {
@@ -791,8 +800,8 @@ __global__ void __launch_bounds__(threads(MPAD), 1)
     auto ytot = [&](int k) -> float& { if constexpr (kYtotSmem) return ytot_s[k * kTileRows]; else return ytot_r[k]; };
 
     const uint32_t aslot = tl + a_col(grp);         // this group's A slot (this warp's lanes)
-    const uint32_t acc1 = tl + acc1_col(MPAD, grp);  // and accumulators
-    const uint32_t acc2 = tl + acc2_col(MPAD, grp);
+    const uint32_t acc1 = tl + acc1_col(MPAD, grp, FMT);  // and accumulators
+    const uint32_t acc2 = tl + acc2_col(MPAD, grp, FMT);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // split counters zeroed, activations written
     uint32_t sbits = 0;   // parity of this group's full barrier of each stage
     GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur;
@@ -1186,7 +1195,7 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)std::min(tasks, num_sms()));
-  cfg.blockDim = dim3(threads(MPAD));
+  cfg.blockDim = dim3(threads(MPAD, FMT));
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
