@@ -166,7 +166,7 @@ int qmm_select_variant(int M, int64_t N, int64_t K);
  * -1 if the arguments are invalid. */
 int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M);
 
-/* Allocation-free variant of qmm_run (the paper has no counterpart; it exists for callers of
+/* Allocation-free variant of qmm_run (the pages have no counterpart; it exists for callers of
  * this library).  Some callers cannot allocate device memory when they call in: code that runs
  * while a stream is being captured into a CUDA graph (allocation is not a stream operation and
  * breaks or is barred from the capture), latency-critical decode loops that must never touch the
