@@ -254,6 +254,10 @@ qmm_status qmm_run_indexed(const void* const* experts_host, int n_experts, int64
     rows += count[e];
     mmax = count[e] > mmax ? count[e] : mmax;
   }
+  if (used == 1) {   // every row goes to the same expert: X and Y are already its gathered blocks
+    const q4k::Job job{experts_host[ids_host[0]], X_dev, Y_dev, N, K};
+    return run_jobs(&job, 1, M, QMM_VARIANT_AUTO, stream);
+  }
   uint16_t* Xg = static_cast<uint16_t*>(workspace_dev);
   float* Yg = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace_dev) + indexed_x_bytes(M, K));
   q4k::RowMap gather{}, scatter{};

@@ -228,7 +228,8 @@ qmm_status qmm_run_ffn_fused(const void* Wgu_interleaved_dev, const void* Wdown_
  * of X is multiplied by the weight matrix of expert ids_host[i],
  *     Y[i][n] = sum_k w_{ids[i]}[n][k] * x[i][k],   0 <= i < M,
  * with the same dequantization and rounding as qmm_run (each expert's rows are one product of
- * the batched launch; results as qmm_run_batched on those rows).
+ * the batched launch; results as qmm_run_batched on those rows).  When every row has the same
+ * expert, the call is that expert's qmm_run on X and Y directly (no gather, no scatter).
  *   experts_host: n_experts device pointers (host array), each a packed N x K matrix.
  *   ids_host: M expert indices (host array, read during the call), 0 <= ids[i] < n_experts.
  *   X_dev: M x K bf16; Y_dev: M x N fp32 (overwritten).
