@@ -196,3 +196,29 @@ def test_force_variant_environment_override(qmm):
     assert picks["fma"] == (qmm.VARIANT_FMA, qmm.VARIANT_FMA)
     assert picks["tc"] == (qmm.VARIANT_TC, qmm.VARIANT_TC)
     assert picks["bogus"] == picks[None]
+
+
+@pytest.mark.parametrize("fmt_name", ["q4k", "q5k", "q6k", "nvfp4", "int4"])
+def test_packed_weights_fmt_replicates_rows(qmm, fmt_name):
+    """The benchmark's timing buffers: the first chunk of rows packed by the library and repeated
+    down to row N, each plane of the format repeated on its own (host memory, no GPU)."""
+    from bit_quantized_skinny_gb300 import workloads
+    fmt = qmm.FORMATS[fmt_name]
+    N, K = inputs.ROWS_PER_CHUNK * 2 + 5, 512
+    out = workloads.packed_weights_fmt(fmt, N, K, 7, device="cpu").numpy()
+    chunk = qmm.fmt_pack(fmt, inputs.weights_f32(inputs.ROWS_PER_CHUNK, K, 7))
+    R = inputs.ROWS_PER_CHUNK
+    idx = np.arange(N) % R
+    if fmt == qmm.FMT_INT4:
+        planes = [(K // 2, 0, 0), (K // 64, N * K // 2, R * K // 2)]
+    elif fmt == qmm.FMT_Q6K:
+        planes = [((K // 256) * 208, 0, 0), ((K // 256) * 2, N * (K // 256) * 208, R * (K // 256) * 208)]
+    else:
+        planes = [((K // 256) * (176 if fmt == qmm.FMT_Q5K else 144), 0, 0)]
+    for rb, off, coff in planes:
+        got = out[off:off + N * rb].reshape(N, rb)
+        ref = chunk[coff:coff + R * rb].reshape(R, rb)[idx]
+        assert np.array_equal(got, ref)
+    if fmt == qmm.FMT_NVFP4:
+        assert np.array_equal(out[-16:], chunk[-16:])
+    assert out.size == qmm.fmt_packed_bytes(fmt, N, K)
