@@ -13,10 +13,14 @@
 //     (cp.async.bulk, completion on an mbarrier) per row brings a box of 4 rows x 576 bytes; the
 //     copy for box u+4 is issued as soon as box u is consumed.
 //   * Decode: lane l owns sub-block l%8 of super-block l/8 of the chunk: 32 weights, 16 bytes of
-//     quants.  Its 32 activations per row of X live in registers as fp32 pairs, loaded once per
-//     chunk.  Nibbles become exact fp32 values (exponent trick + one add.f32x2 per pair), the
-//     dot product runs on fma.f32x2, and the scales are applied once per sub-block:
-//     part = (D*sc_j) * sum_t q_t x_t - (Dm*m_j) * sum_t x_t.
+//     quants.  Its 32 activations per row of X live in registers as fp32 values, loaded once
+//     per chunk.  Nibbles become exact fp32 values (exponent trick + one subtraction), each
+//     weight is formed by its definition, w_t = fma(D*sc_j, q_t, -(Dm*m_j)) (one rounding of the
+//     exact value: the weight the oracle and qmm_dequant compute), and the dot product runs on
+//     fp32 FMAs: part = sum_t w_t x_t.  Forming the weight first keeps the error of a part
+//     within a few units of fp32 rounding of sum_t |w_t x_t|, also where d*sc_j*q_t and
+//     dmin*m_j nearly cancel (a factored form (D*sc_j) sum q x - (Dm*m_j) sum x would round two
+//     large sums separately).
 //   * K-reduction: a warp-shuffle butterfly sums the 32 lanes (one chunk) for the 4 rows x MT
 //     activation rows of a box; chunk partials go to shared memory and are summed over the
 //     chunks in increasing order at the end of the task.  The order of every addition depends
@@ -139,7 +143,6 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
       for (int u = u_begin; u < min(u_end, u_begin + kStages); ++u) issue(u);
 
     float xf[MT][32];
-    float negxs[MT];
     int cur_c = -1;
     bool lane_valid = false;
 
@@ -163,7 +166,6 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
 #pragma unroll
             for (int g = 0; g < 4; ++g) v[g] = make_uint4(0, 0, 0, 0);
           }
-          float s = 0.f;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const uint32_t w4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
@@ -171,11 +173,8 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
             for (int h = 0; h < 4; ++h) {
               xf[i][8 * g + 2 * h] = __uint_as_float(w4[h] << 16);
               xf[i][8 * g + 2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
-              s += xf[i][8 * g + 2 * h];
-              s += xf[i][8 * g + 2 * h + 1];
             }
           }
-          negxs[i] = -s;
         }
       }
 
@@ -205,6 +204,9 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
           nibbles_to_f32(q.y, *reinterpret_cast<float(*)[8]>(&qf[8]));
           nibbles_to_f32(q.z, *reinterpret_cast<float(*)[8]>(&qf[16]));
           nibbles_to_f32(q.w, *reinterpret_cast<float(*)[8]>(&qf[24]));
+          const float ndmm = -sc.dmm;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) qf[t] = fmaf(sc.dsc, qf[t], ndmm);   // the weight w_t
 #pragma unroll
           for (int i = 0; i < MT; ++i) {
             // four accumulators (weights t = 4k, 4k+1, 4k+2, 4k+3), summed in a fixed order
@@ -217,8 +219,7 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
               a3 = fmaf(qf[t + 3], xf[i][t + 3], a3);
             }
             const float dot = (a0 + a1) + (a2 + a3);
-            const float part = fmaf(sc.dmm, negxs[i], sc.dsc * dot);
-            vals[s * (V / kRB) + i] = lane_valid ? part : 0.f;
+            vals[s * (V / kRB) + i] = lane_valid ? dot : 0.f;
           }
         }
       }

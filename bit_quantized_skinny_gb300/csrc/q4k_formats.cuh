@@ -17,17 +17,18 @@ namespace q4k {
 // H of the sub-block (bit 4i + ww is the high bit of weight i of word ww).  Returns
 //   p[0] = (1024 + q0, 1024 + q4)          p[1] = (1024 + 16 q1, 1024 + 16 q5)
 //   p[2] = (1024 + q2, 1024 + q6)          p[3] = (1024 + 16 q3, 1024 + 16 q7)
-// with q the 5-bit quants (each at most 1024 + 496 < 2048: exact in fp16).
-template <int WW>
+// with q the 5-bit quants (each at most 1024 + 496 < 2048: exact in fp16).  With MAGIC = 0 the
+// exponent field stays 0 and the pairs are the fp16 subnormals (q 2^-24, 16 q 2^-24).
+template <int WW, uint32_t MAGIC = 0x64006400u>
 __device__ __forceinline__ void q5k_magic(uint32_t w, uint32_t H, uint32_t (&p)[4]) {
   const uint32_t hl = H << (4 - WW);   // high bits of weights 0, 4 at bits 4, 20; of 1, 5 at 8, 24
   const uint32_t hr = H >> (4 + WW);   // of weights 2, 6 at bits 4, 20; of 3, 7 at 8, 24
   const uint32_t b8 = w >> 8;
   uint32_t u0, u1, u2, u3;
-  asm("lop3.b32 %0, %1, 0x00100010, 0x64006400, 0xEA;" : "=r"(u0) : "r"(hl));
-  asm("lop3.b32 %0, %1, 0x01000100, 0x64006400, 0xEA;" : "=r"(u1) : "r"(hl));
-  asm("lop3.b32 %0, %1, 0x00100010, 0x64006400, 0xEA;" : "=r"(u2) : "r"(hr));
-  asm("lop3.b32 %0, %1, 0x01000100, 0x64006400, 0xEA;" : "=r"(u3) : "r"(hr));
+  asm("lop3.b32 %0, %1, 0x00100010, %2, 0xEA;" : "=r"(u0) : "r"(hl), "n"(MAGIC));
+  asm("lop3.b32 %0, %1, 0x01000100, %2, 0xEA;" : "=r"(u1) : "r"(hl), "n"(MAGIC));
+  asm("lop3.b32 %0, %1, 0x00100010, %2, 0xEA;" : "=r"(u2) : "r"(hr), "n"(MAGIC));
+  asm("lop3.b32 %0, %1, 0x01000100, %2, 0xEA;" : "=r"(u3) : "r"(hr), "n"(MAGIC));
   asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(p[0]) : "r"(w), "r"(u0));
   asm("lop3.b32 %0, %1, 0x00F000F0, %2, 0xEA;" : "=r"(p[1]) : "r"(w), "r"(u1));
   asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(p[2]) : "r"(b8), "r"(u2));

@@ -59,6 +59,10 @@ cudaError_t launch_scatter_rows(const RowMap& map, int M, const float* Yg, int64
 cudaError_t launch_dequant(const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 cudaError_t launch_dequant_fmt(int fmt, const void* W, int64_t N, int64_t K, float* out, cudaStream_t stream);
 
+// The tensor-core kernel's per-(device, stream) workspaces: free them all; bytes held now.
+cudaError_t release_workspaces();
+size_t workspace_bytes_held();
+
 // Device status words of the kernel files: read and clear (synchronous; 0 = no error).
 cudaError_t read_and_clear_fma_status(unsigned* out);
 cudaError_t read_and_clear_tc_status(unsigned* out);

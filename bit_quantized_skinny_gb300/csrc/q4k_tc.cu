@@ -100,7 +100,6 @@ constexpr int kMaxGroups = 3;
 // super-block).
 __host__ __device__ constexpr bool single_acc(int f) { return f == kFmtNVFP4 || f == kFmtQ6K; }
 __host__ __device__ constexpr int groups(int mpad, int f = kFmtQ4K) { return (mpad <= 16 || single_acc(f)) ? 3 : 2; }
-__host__ __device__ constexpr int threads(int mpad, int f = kFmtQ4K) { return 32 * (groups(mpad, f) * kGroupWarps + 2); }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
@@ -117,7 +116,23 @@ __host__ __device__ constexpr int blk_bytes(int f) {
 __host__ __device__ constexpr bool has_min(int f) { return f == kFmtQ4K || f == kFmtQ5K; }
 __host__ __device__ constexpr int w_stage_bytes(int f) { return kTileRows * blk_bytes(f); }
 
-__host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 544 + 16; }
+// Prepared activation block of one super-block (bblock_bytes(MPAD) bytes, written by the
+// preparation kernel, read by the product kernel from a stage of its ring):
+//   [0, MPAD*512)         B: the 256 activations of every token column i as fp16 x * 2^-s_i,
+//                         K-major core matrices (8 tokens x 8 k, 128 bytes; 32 of them along k
+//                         per group of 8 tokens: 4096 bytes)
+//   [MPAD*512, MPAD*576)  B_ext: 32 rows per token, sub-block j's activation sum X_j * 2^(-s_i-6)
+//                         as an fp16 pair (hi, lo): rows 4j .. 4j+3 = (hi, hi, lo, lo)
+//                         (8 tokens x 4 core matrices: 512 bytes per group of 8 tokens)
+//   [MPAD*576, MPAD*580)  sigma_i = 2^(s_i + 14) per token column, fp32
+//   [MPAD*580, +16)       the mask of "hard" tokens (bit i), K, and the address of X (8 bytes)
+// A hard token's staging would not be exact (see q4k_xprep_kernel); its B and B_ext rows are
+// zero (its accumulator columns come out exactly 0) and the product kernel computes its part of
+// the super-block from X itself.
+__host__ __device__ constexpr int bext_off(int mpad) { return mpad * 512; }
+__host__ __device__ constexpr int sig_off(int mpad) { return mpad * 576; }
+__host__ __device__ constexpr int mask_off(int mpad) { return mpad * 580; }
+__host__ __device__ constexpr int bblock_bytes(int mpad) { return mpad * 580 + 16; }
 // A stage holds one super-block of a tile (the weight rows) and the prepared activation block
 // of the same super-block: both arrive on one barrier, issued the same distance ahead.
 // (rounded up to 128 bytes: a TMA tile copy writes to a 128-byte aligned address; INT4 tiles
@@ -128,24 +143,47 @@ __host__ __device__ constexpr int stage_bytes(int mpad, int f) {
 }
 constexpr int kMaxStages = 8;
 // TMEM columns.  Each group owns one A slot (one super-block: 64 columns of fp16 pairs per K
-// half and 8 columns of (m_j) pairs for the dmin MMA, 136 in all) and one accumulator (Mpad
-// columns of the product and Mpad of the dmin term -- or, for INT4, of the second K half --
-// at the top of the 512 columns):
-//   Mpad 16: A slots 0..407, accumulators 416..511
-//   Mpad 32: A slots 0..271, accumulators 384..511
-constexpr uint32_t kACols = 136;
+// half) and one accumulator block at the top of the 512 columns.
+//   k-quants (Q4K, Q5K) have the min-term MMAs: A_ext, 16 columns (K = 32), after the slot's
+//   128 columns.  With 8 token columns (M <= 8) the min-term MMAs accumulate into columns 8..15
+//   of the product's own 16-column accumulator (their B_ext has the tokens in columns 8..15,
+//   the product's B zeros there); otherwise the min term has its own Mpad-column accumulator.
+//   With 16 token columns three such groups do not fit: there A_ext reuses the slot's first 16
+//   columns once the first K half's MMAs have completed, and each group has its own MMA warp
+//   (with one MMA warp for all groups, a group waiting for its first half's MMAs would hold up
+//   the other groups' MMAs, issued in order).
+//   INT4: two accumulators (one per K half, its two scale groups); NVFP4, Q6K: one.
+//     Q4K, Q5K   8 tokens: 3 x (144 + 16) = 480;  16 tokens: 3 x (128 + 32) = 480;  Mpad 32: 2 x (144 + 64)
+//     INT4       3 x (128 + 32) = 480 at Mpad 16;  2 x (128 + 64) at Mpad 32
+//     NVFP4, Q6K 3 x (128 + Mpad): 432 / 480
+__host__ __device__ constexpr bool ext_in_a(int f, int mt) { return has_min(f) && mt == 16; }
+__host__ __device__ constexpr uint32_t acols(int f, int mt) { return (has_min(f) && mt != 16) ? 144u : 128u; }
+// MMA-issuing warps: one per group.  (With one MMA warp serving the groups in order, its wait
+// for one group's handoff held up the MMAs of the others: measured on GB300 with clock stamps,
+// the groups then advanced one at a time.)
+__host__ __device__ constexpr int mma_warps(int mpad, int f, int mt) { return groups(mpad, f) + 0 * mt; }
+// Threads of a CTA: the dequant groups, the copy warp and the MMA warp(s).
+__host__ __device__ constexpr int cta_threads(int mpad, int f, int mt) {
+  return 32 * (groups(mpad, f) * kGroupWarps + 1 + mma_warps(mpad, f, mt));
+}
 // Summation order of a product: the super-blocks of a row are summed in chunks of kChunkSb (each
 // chunk from zero, in order of k), and the chunk sums are then added in chunk order.  A K split
 // only ever cuts at chunk boundaries, so the bits of a product do not depend on the split.
 constexpr int kChunkSb = 4;
-__host__ __device__ constexpr uint32_t a_col(int g) { return kACols * g; }
-__host__ __device__ constexpr uint32_t acc_cols(int mpad, int f) { return single_acc(f) ? mpad : 2u * mpad; }
-__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f = kFmtQ4K) {
-  return 512u - acc_cols(mpad, f) * groups(mpad, f) + acc_cols(mpad, f) * g;
+__host__ __device__ constexpr uint32_t a_col(int g, int f, int mt) { return acols(f, mt) * g; }
+__host__ __device__ constexpr uint32_t acc_cols(int mpad, int f, int mt) {
+  return single_acc(f) ? mpad : ((has_min(f) && mt == 8) ? mpad : 2u * mpad);
 }
-__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f = kFmtQ4K) { return acc1_col(mpad, g, f) + mpad; }
-static_assert(a_col(groups(16)) <= acc1_col(16, 0) && a_col(groups(32)) <= acc1_col(32, 0) &&
-              a_col(groups(32, kFmtNVFP4)) <= acc1_col(32, 0, kFmtNVFP4),
+__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f, int mt) {
+  return 512u - acc_cols(mpad, f, mt) * groups(mpad, f) + acc_cols(mpad, f, mt) * g;
+}
+__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f, int mt) { return acc1_col(mpad, g, f, mt) + mpad; }
+__host__ __device__ constexpr bool tmem_fits(int mpad, int f, int mt) {
+  return a_col(groups(mpad, f), f, mt) <= acc1_col(mpad, 0, f, mt);
+}
+static_assert(tmem_fits(16, kFmtQ4K, 8) && tmem_fits(16, kFmtQ4K, 16) && tmem_fits(32, kFmtQ4K, 32) &&
+              tmem_fits(16, kFmtINT4, 8) && tmem_fits(16, kFmtINT4, 16) && tmem_fits(32, kFmtINT4, 32) &&
+              tmem_fits(16, kFmtNVFP4, 16) && tmem_fits(32, kFmtNVFP4, 32) && tmem_fits(32, kFmtQ6K, 32),
               "TMEM column plan overlaps");
 
 // Barrier indices inside the barrier block.  Every barrier is waited on by threads that see
@@ -153,22 +191,28 @@ static_assert(a_col(groups(16)) <= acc1_col(16, 0) && a_col(groups(32)) <= acc1_
 //   GFull[g][s]  stage s holds a super-block of group g (copies landed); group g, MMA lane
 //   WEmpty[s]    stage s consumed (the group's 4 warps + the MMA commit); copy lane
 //   AFull[g][h]  K half h of group g's A slot written; MMA lane
+//   H0Done[g]    the first K half's MMAs of group g's latest super-block completed; group g
+//                (only where A_ext reuses the first K half's columns)
 //   GDone[g]     the MMAs of group g's latest super-block completed; group g
 //   Drain        the last MMAs of the CTA completed; MMA lane
 enum : int {
   kBarGFull = 0, kBarWEmpty = kBarGFull + kMaxGroups * kMaxStages,
   kBarAFull = kBarWEmpty + kMaxStages, kBarGDone = kBarAFull + 2 * kMaxGroups,
-  kBarDrain = kBarGDone + kMaxGroups,
-  kNumBars = kBarDrain + 1
+  kBarH0Done = kBarGDone + kMaxGroups, kBarDrain = kBarH0Done + kMaxGroups,
+  kNumBars = kBarDrain + kMaxGroups
 };
 
 // With 16 or 32 token columns each group's running sum of chunk sums (MT tokens x 128 rows of
 // fp32) lives in shared memory, not in registers (there it spilled); it is touched once per
 // chunk of 4 super-blocks.
 __host__ __device__ constexpr int ytot_bytes(int mpad, int mt, int f = kFmtQ4K) { return mt >= 16 ? groups(mpad, f) * mt * kTileRows * 4 : 0; }
+// Each dequant warp keeps its own copy of the current super-block's per-token scales (the stage
+// that brought them is released before the epilogue needs them): 32 floats for each of the
+// two super-blocks in flight, per warp.
+constexpr int kSigBytes = kMaxGroups * kGroupWarps * 64 * 4;
 // Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens).
 __host__ __device__ constexpr int stages_fit(int mpad, int f, int mt) {
-  return (kSmemLimit - ytot_bytes(mpad, mt, f) - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+  return (kSmemLimit - ytot_bytes(mpad, mt, f) - kSigBytes - kNumBars * 8 - 32) / stage_bytes(mpad, f);
 }
 __host__ __device__ constexpr int stages(int mpad, int f, int mt) {
   return stages_fit(mpad, f, mt) < (mpad <= 16 ? 8 : 5) ? stages_fit(mpad, f, mt) : (mpad <= 16 ? 8 : 5);
@@ -178,7 +222,8 @@ template <int MPAD, int FMT, int MT>
 struct TcSmem {
   static constexpr int kW = 0;
   static constexpr int kYtot = kW + stages(MPAD, FMT, MT) * stage_bytes(MPAD, FMT);
-  static constexpr int kBars = kYtot + ytot_bytes(MPAD, MT, FMT);
+  static constexpr int kSig = kYtot + ytot_bytes(MPAD, MT, FMT);
+  static constexpr int kBars = kSig + kSigBytes;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
@@ -194,7 +239,8 @@ static_assert(stages(16, kFmtQ4K, 8) == 8 && stages(16, kFmtQ4K, 16) == 7 && sta
               stages(16, kFmtQ6K, 16) >= 4 && stages(32, kFmtQ6K, 32) >= 3, "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
 static_assert(stage_bytes(16, kFmtQ4K) % 128 == 0 && stage_bytes(32, kFmtQ5K) % 128 == 0 &&
-              stage_bytes(16, kFmtINT4) % 1024 == 0 && w_stage_bytes(kFmtQ5K) % 128 == 0, "stage alignment");
+              stage_bytes(16, kFmtINT4) % 1024 == 0 && w_stage_bytes(kFmtQ5K) % 128 == 0 &&
+              bblock_bytes(16) % 16 == 0 && bblock_bytes(32) % 16 == 0, "stage alignment");
 
 struct TcEntry {
   float* Y;
@@ -240,6 +286,7 @@ struct PrepParams {
   int M;
   int blocks_total;
   int zero_words;      // split counters of the main launches of this call, zeroed here
+  int shift_ext;       // B_ext token columns moved up by 8 (the 8-token product kernels, M <= 8)
   unsigned* zero;
   PrepEntry e[NX];
 };
@@ -249,15 +296,25 @@ __device__ __forceinline__ __half2 bits2h(uint32_t v) { return *reinterpret_cast
 
 // ------------------------------------------------------------------------------------------
 // Activation preparation.  Block = 8*MPAD threads; thread (i = t/8, j = t%8) handles token i,
-// sub-block j (32 activations) of one super-block.  Each 8-activation word is stored as fp16
-// pairs in the order of the weight decode: (x_c, x_c+4), c = 0..3, or with NAT (NVFP4) the
-// natural (x_2c, x_2c+1).
+// sub-block j (32 activations) of one super-block; the 8 threads of a token are 8 neighbouring
+// lanes of one warp.
+//
+// Every token has its own power of two: s_i puts the largest |x| of its 256 activations in
+// [2^14, 2^15) (s_i in [-112, 113]).  The token is staged exactly when
+//   (a) every x * 2^-s_i is an fp16 value (true unless x is below about 2^-31 of that largest
+//       value, or the largest value is a bf16 subnormal far below 2^-112), and
+//   (b) every sub-block j with a nonzero activation has sum_t |x_t * 2^-s_i| >= 1/4: then the
+//       fp16 pair (hi, lo) that carries X_j * 2^(-s_i-6) is within 2^-19 of sum_t |x_t|.
+// Otherwise the token is "hard": its B and B_ext rows are zeros, and the product kernel computes
+// its outputs for this super-block on CUDA cores in fp32 from X.
+// B pairs are in the order of the weight decode: (x_c, x_c+4), c = 0..3, of each 8-activation
+// word, or with NAT (NVFP4) the natural (x_2c, x_2c+1).
 template <int MPAD, int NX, bool NAT>
 __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_constant__ PrepParams<NX> P) {
   // the product kernel that follows may start its prologue now (programmatic dependent launch);
   // it waits for this grid's completion before it reads what this grid writes
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ unsigned s_max[8];
+  __shared__ unsigned s_hard[8 * MPAD / 32];
   const int b = blockIdx.x;
   int e = 0;
   {
@@ -271,6 +328,7 @@ __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_consta
   const PrepEntry& E = P.e[e];
   const int sb = b - E.block_begin;
   const int t = threadIdx.x;
+  const int lane = t & 31;
   for (int z = b * (8 * MPAD) + t; z < P.zero_words; z += P.blocks_total * (8 * MPAD)) P.zero[z] = 0u;
   const int i = t >> 3, j = t & 7;
   const bool valid = i < P.M;
@@ -283,63 +341,83 @@ __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_consta
 #pragma unroll
     for (int g = 0; g < 4; ++g) v[g] = make_uint4(0, 0, 0, 0);
   }
+  // the token's largest |x| (bit pattern of |x|: larger patterns are larger values)
   unsigned mx = 0;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const uint32_t w4[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
 #pragma unroll
+    for (int h = 0; h < 4; ++h) mx = max(mx, max(w4[h] & 0x7FFFu, (w4[h] >> 16) & 0x7FFFu));
+  }
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  // largest |x| in [2^(E-127), 2^(E-126)), E = its biased exponent; scale it into [2^14, 2^15)
+  int s = 0;
+  if (mx != 0) s = min(113, max(-112, (int)(mx >> 7) - 141));
+  const float f = __uint_as_float((uint32_t)(127 - s) << 23);    // 2^-s
+  const float fs = __uint_as_float((uint32_t)(127 + s) << 23);   // 2^s
+
+  uint32_t packed[4][4];
+  float xsum = 0.f, asum = 0.f;
+  bool exact = true;
+#pragma unroll
+  for (int ww = 0; ww < 4; ++ww) {
+    const uint32_t w4[4] = {v[ww].x, v[ww].y, v[ww].z, v[ww].w};
+    float xv[8];   // the word's 8 activations in order of k
+#pragma unroll
     for (int h = 0; h < 4; ++h) {
-      mx = max(mx, w4[h] & 0x7FFFu);
-      mx = max(mx, (w4[h] >> 16) & 0x7FFFu);
+      xv[2 * h] = __uint_as_float(w4[h] << 16);
+      xv[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float xa = NAT ? xv[2 * c] : xv[c];
+      const float xb = NAT ? xv[2 * c + 1] : xv[c + 4];
+      const __half2 hh = __floats2half2_rn(xa * f, xb * f);
+      const float2 back = __half22float2(hh);
+      exact = exact && (back.x * fs == xa) && (back.y * fs == xb);
+      packed[ww][c] = h2bits(hh);
+      xsum += back.x + back.y;
+      asum += fabsf(xa * f) + fabsf(xb * f);
     }
   }
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if ((t & 31) == 0) s_max[t >> 5] = mx;
-  __syncthreads();
-  mx = 0;
-#pragma unroll
-  for (int w = 0; w < (8 * MPAD) / 32; ++w) mx = max(mx, s_max[w]);
-  // largest |x| in [2^(e-127), 2^(e-126)); scale it into [2^14, 2^15)
-  int s = 0;
-  if (mx != 0) s = min(120, max(-120, (int)(mx >> 7) - 141));
-  const float f = __uint_as_float((uint32_t)(127 - s) << 23);   // 2^-s
+  const bool bad = !exact || (asum > 0.f && asum < 0.25f);
+  const unsigned ballot = __ballot_sync(0xffffffffu, bad);
+  const bool hard = valid && ((ballot >> (lane & 24)) & 0xFFu) != 0u;
 
   uint8_t* out = E.out + (int64_t)sb * bblock_bytes(MPAD);
-  float xsum = 0.f;
 #pragma unroll
   for (int ww = 0; ww < 4; ++ww) {
     const int w = 4 * j + ww;  // word (8 activations) index within the super-block
-    const uint32_t w4[4] = {v[ww].x, v[ww].y, v[ww].z, v[ww].w};
-    float xv[8];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      xv[2 * h] = __uint_as_float(w4[h] << 16) * f;
-      xv[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) * f;
-    }
-    uint32_t packed[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      packed[c] = NAT ? h2bits(__floats2half2_rn(xv[2 * c], xv[2 * c + 1])) : h2bits(__floats2half2_rn(xv[c], xv[c + 4]));
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const __half2 hh = bits2h(packed[p & 3]);
-      xsum += (p < 4) ? __low2float(hh) : __high2float(hh);
-    }
     uint4* dst = reinterpret_cast<uint4*>(out + ((i >> 3) * 32 + w) * 128 + (i & 7) * 16);
-    *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    *dst = hard ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(packed[ww][0], packed[ww][1], packed[ww][2], packed[ww][3]);
   }
+  // B_ext: rows 4j .. 4j+3 of token column c = (hi, hi, lo, lo)
   const float xs = xsum * 0.015625f;  // 2^-6: a sum of 32 values below 2^15 stays below 2^14
   const __half hi = __float2half_rn(xs);
   const __half lo = __float2half_rn(xs - __half2float(hi));
-  __half* ext = reinterpret_cast<__half*>(out + MPAD * 512);
-  ext[(((i >> 3) * 2 + 0) * 128 + (i & 7) * 16) / 2 + j] = hi;
-  ext[(((i >> 3) * 2 + 1) * 128 + (i & 7) * 16) / 2 + j] = lo;
+  const uint32_t hb = __half_as_ushort(hi), lb = __half_as_ushort(lo);
+  const uint2 ev = hard ? make_uint2(0u, 0u) : make_uint2(hb * 0x10001u, lb * 0x10001u);
+  uint8_t* ext = out + bext_off(MPAD);
+  auto ext_at = [&](int c) { return reinterpret_cast<uint2*>(ext + (c >> 3) * 512 + (j >> 1) * 128 + (c & 7) * 16 + (j & 1) * 8); };
+  if (!P.shift_ext) {
+    *ext_at(i) = ev;
+  } else if (i < 8) {   // MPAD 16 and M <= 8: token i's rows in column i + 8, zeros in column i
+    *ext_at(i + 8) = ev;
+    *ext_at(i) = make_uint2(0u, 0u);
+  }
+  float* sig = reinterpret_cast<float*>(out + sig_off(MPAD));
+  if (j == 0) sig[i] = __uint_as_float((uint32_t)(127 + 14 + s) << 23);   // 2^(s+14)
+  const unsigned bits = __reduce_or_sync(0xffffffffu, (hard && j == 0) ? (1u << i) : 0u);
+  if (lane == 0) s_hard[t >> 5] = bits;
+  __syncthreads();
   if (t == 0) {
-    float* sig = reinterpret_cast<float*>(out + MPAD * 544);
-    sig[0] = __uint_as_float((uint32_t)(127 + s) << 23);  // 2^s
-    sig[1] = 0.f;
-    sig[2] = 0.f;
-    sig[3] = 0.f;
+    unsigned m = 0;
+#pragma unroll
+    for (int w = 0; w < (8 * MPAD) / 32; ++w) m |= s_hard[w];
+    const uint64_t xa = reinterpret_cast<uint64_t>(E.X);
+    *reinterpret_cast<uint4*>(out + mask_off(MPAD)) = make_uint4(m, (uint32_t)E.K, (uint32_t)xa, (uint32_t)(xa >> 32));
   }
 }
 
@@ -439,7 +517,8 @@ struct GroupCursor {
 // the i-th super-block of group g is
 //   su = sum_h min(n_h, i) + #{h < g : n_h > i}.
 template <int NG>
-__device__ __forceinline__ uint32_t su_of(const int (&n)[NG], int g, int i) {
+__device__ __forceinline__ uint32_t su_of(const int (&n)[NG], int g, int i, int nmin) {
+  if (i < nmin) return (uint32_t)(NG * i + g);   // every group still has a super-block in round i
   uint32_t s = 0;
 #pragma unroll
   for (int h = 0; h < NG; ++h) s += (uint32_t)min(n[h], i) + ((h < g && n[h] > i) ? 1u : 0u);
@@ -484,31 +563,101 @@ __device__ __forceinline__ void load_half(HalfIn<FMT>& in, uint32_t rb, int h) {
 
 // fp16 constants of the decodes, made once per thread (outside the super-block loop)
 struct DecodeConsts {
-  __half2 k1024, kn1024, k1o16, kn64, kn1032, kn72;
+  __half2 k1024, k0_1024, kn1024_1024, k1o16, kn1032, kn72;
   __device__ __forceinline__ DecodeConsts()
-      : k1024(bits2h(0x64006400u)), kn1024(__float2half2_rn(-1024.f)), k1o16(__float2half2_rn(0.0625f)),
-        kn64(__float2half2_rn(-64.f)), kn1032(__float2half2_rn(-1032.f)), kn72(__float2half2_rn(-72.f)) {}
+      : k1024(bits2h(0x64006400u)), k0_1024(bits2h(0x64000000u)), kn1024_1024(bits2h(0x6400E400u)),
+        k1o16(__float2half2_rn(0.0625f)), kn1032(__float2half2_rn(-1032.f)), kn72(__float2half2_rn(-72.f)) {}
 };
+
+// The k-quants' min term, folded into the operands.  Weight t of sub-block j is
+//   w_t = D sc_j q_t - Dm m_j = D (sc_j q_t - k_j) - rho_j,   rho_j = Dm m_j - D k_j,
+// for any integer k_j.  With k_j = rint(m_j Dm / D) clamped to [0, 2047] (0 when Dm / D < 0):
+//   * A_t = sc_j q_t - k_j is an integer in [-2047, 1953]: exact in fp16 (written as A_t 2^-14,
+//     a normal fp16 number or 0), so a weight that is exactly zero contributes exactly zero;
+//   * |rho_j| <= |w_t| for every t of the sub-block (unclamped: |rho_j| <= |D|/2 and
+//     |D A_t| >= |D| when A_t != 0; clamped, or k_j = 0 with opposite signs: every w_t has the
+//     sign of -rho_j and |w_t| >= |rho_j|), so the rho term only needs relative precision; and
+//     |rho_j| <= 63 |Dm|, so rho_j T stays below 2^15;
+//   * rho_j T (T = 2^(8-e), 2^e <= |Dm| < 2^(e+1)) is either >= 2^-3 in magnitude or a multiple
+//     of 2^-24 below 2^-3 with at most 21 bits, and it is carried as an fp16 pair (hi, lo):
+//     hi = rho_j T truncated to 11 significant bits, lo = the rest rounded to fp16, so
+//     hi + lo is exact or within 2^-22 of rho_j T.
+// The min-term MMAs take A_ext columns (hi_j, lo_j) twice per sub-block against the B_ext rows
+// (X_hi, X_hi) and (X_lo, X_lo), so that the accumulator receives (hi + lo)(X_hi + X_lo).
+struct Fold {
+  float R;     // Dm / D when >= 0, else 0 (+inf when D = 0: every k_j then clamps; D A_t vanishes)
+  float DT;    // D * T
+  float DmT;   // Dm * T, in [2^8, 2^9) (0 when Dm = 0, T = 1)
+};
+__device__ __forceinline__ Fold make_fold(float D, float Dm) {
+  Fold f;
+  float rD;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rD) : "f"(D));
+  f.R = fmaxf(Dm * rD, 0.f);   // opposite signs (and D = 0 with Dm = 0): k = 0
+  const uint32_t eb = __float_as_uint(Dm) & 0x7F800000u;
+  const float T = eb ? __uint_as_float((262u << 23) - eb) : 1.0f;
+  f.DT = D * T;
+  f.DmT = Dm * T;
+  return f;
+}
+// The factor of the min-term accumulator: y += sigma (D acc + fe(Dm) acc_ext), fe = -2^(e-16)
+// (acc_ext carries rho T X 2^(-s-6); sigma = 2^(s+14)).
+__device__ __forceinline__ float fold_ext_factor(float Dm) {
+  const uint32_t eb = __float_as_uint(Dm) & 0x7F800000u;
+  return eb ? -__uint_as_float(eb - (16u << 23)) : 0.f;
+}
+
+// The per-sub-block constants of the folded decode, computed ahead of it (12-bit group
+// gr = sc_j | m_j << 6): cm = the fp16 pair (-k_j 2^-14, sc_j 2^10) -- the decode's addend and
+// its first multiplier -- and ext = the A_ext pair (hi, lo) of rho_j T.
+__device__ __forceinline__ void fold_k(uint32_t gr, const Fold& fd, const DecodeConsts& C, uint32_t& cm,
+                                       uint32_t& ext) {
+  const float mf = (float)(gr >> 6);
+  const float tk = fmaf(mf, fd.R, 12582912.0f);               // 1.5 2^23 + rint(m R) while m R < 2^22
+  const uint32_t k = min(__float_as_uint(tk) - 0x4B400000u, 2047u);
+  // (k 2^-24, 1024 + sc): k 2^-24 has the bit pattern of k; minus (0, 1024), times (-1024, 1024)
+  const uint32_t v = ((gr & 63u) | 0x6400u) * 0x10000u + k;
+  cm = h2bits(__hmul2(__hsub2(bits2h(v), C.k0_1024), C.kn1024_1024));
+  const float rt = fmaf(-fd.DT, (float)k, mf * fd.DmT);       // (Dm m - D k) T
+  const float rhi = __uint_as_float(__float_as_uint(rt) & 0xFFFFE000u);
+  ext = h2bits(__floats2half2_rn(rhi, rt - rhi));
+}
+
+// The 12-bit (sc_j, m_j) group of sub-block j from a super-block's first 16 bytes.
+__device__ __forceinline__ uint32_t kq_group(const uint4& hd, int j) {
+  const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 at bits 0..47
+  const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 at bits 16..63
+  return (uint32_t)(j < 4 ? (G >> (12 * j)) : (H >> (16 + 12 * (j - 4)))) & 0xFFFu;
+}
+
+// All fold constants of a row's super-block (computed ahead of its decode).
+__device__ __forceinline__ void fold_consts(const uint4& hd, const DecodeConsts& C, uint32_t (&add)[8],
+                                            uint32_t (&ext)[8]) {
+  const float2 dd = __half22float2(bits2h(hd.x));
+  const Fold fd = make_fold(dd.x, dd.y);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) fold_k(kq_group(hd, j), fd, C, add[j], ext[j]);
+}
 
 template <int FMT>
 __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& hd, int h, uint32_t aaddr,
-                                            const DecodeConsts& C) {
+                                            const DecodeConsts& C, const uint32_t (&add4)[4]) {
   if constexpr (FMT == kFmtQ4K || FMT == kFmtQ5K) {
-    const __half2 k1024 = C.k1024, kn1024 = C.kn1024, k1o16 = C.k1o16, kn64 = C.kn64;
-    // the 12-bit (sc, m) groups of sub-blocks 4h .. 4h+3
-    const uint64_t F = h ? ((uint64_t)hd.w << 32 | hd.z) : ((uint64_t)hd.z << 32 | hd.y);
-    const int fbase = h ? 16 : 0;
-    __half2 sc2[4], scm[4], sc16[4], sc64[4];
+    // the addend (-k 2^-14) and multipliers (sc 2^10, sc 2^6) of the two nibble positions of
+    // sub-blocks 4h .. 4h+3, from the precomputed pairs (-k 2^-14, sc 2^10)
+    __half2 mlo[4], mhi[4], add[4];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t gr = (uint32_t)(F >> (fbase + 12 * jj)) & 0xFFFu;
-      const uint32_t scb = ((gr & 63u) | 0x6400u) * 0x10001u;      // (1024+sc, 1024+sc)
-      sc2[jj] = __hsub2(bits2h(scb), k1024);                       // (sc, sc) exact
-      scm[jj] = __hmul2(sc2[jj], kn1024);                           // -1024 sc
-      sc16[jj] = __hmul2(sc2[jj], k1o16);                           // sc / 16
-      sc64[jj] = __hmul2(sc2[jj], kn64);                            // -64 sc
+      const uint32_t cm = add4[jj];
+      uint32_t lo2, hi2;
+      asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(lo2) : "r"(cm));
+      asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(hi2) : "r"(cm));
+      add[jj] = bits2h(lo2);
+      mlo[jj] = bits2h(hi2);
+      mhi[jj] = __hmul2(mlo[jj], C.k1o16);
     }
-    // A = sc*q as fp16 pairs, 16 columns per sub-block
+    // A = (sc q - k) 2^-14 as fp16 pairs, 16 columns per sub-block.  The quants enter as fp16
+    // subnormals: q 2^-24 (bits 0..3 of a half) or 16 q 2^-24 (bits 4..7).
     const uint32_t hwords[4] = {in.hb.x, in.hb.y, in.hb.z, in.hb.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -520,21 +669,21 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
         const uint32_t wv = words[ww];
         uint32_t p[4];
         if constexpr (FMT == kFmtQ5K) {
-          if (ww == 0) q5k_magic<0>(wv, hwords[k], p);
-          if (ww == 1) q5k_magic<1>(wv, hwords[k], p);
-          if (ww == 2) q5k_magic<2>(wv, hwords[k], p);
-          if (ww == 3) q5k_magic<3>(wv, hwords[k], p);
+          if (ww == 0) q5k_magic<0, 0u>(wv, hwords[k], p);
+          if (ww == 1) q5k_magic<1, 0u>(wv, hwords[k], p);
+          if (ww == 2) q5k_magic<2, 0u>(wv, hwords[k], p);
+          if (ww == 3) q5k_magic<3, 0u>(wv, hwords[k], p);
         } else {
           const uint32_t b8 = wv >> 8;
-          asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p[0]) : "r"(wv));
-          asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p[1]) : "r"(wv));
-          asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(p[2]) : "r"(b8));
-          asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;" : "=r"(p[3]) : "r"(b8));
+          p[0] = wv & 0x000F000Fu;
+          p[1] = wv & 0x00F000F0u;
+          p[2] = b8 & 0x000F000Fu;
+          p[3] = b8 & 0x00F000F0u;
         }
-        cols[4 * ww + 0] = h2bits(__hfma2(bits2h(p[0]), sc2[k], scm[k]));   // (q0, q4) * sc
-        cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p[1]), sc16[k], sc64[k]));  // (q1, q5) * sc
-        cols[4 * ww + 2] = h2bits(__hfma2(bits2h(p[2]), sc2[k], scm[k]));   // (q2, q6) * sc
-        cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p[3]), sc16[k], sc64[k]));  // (q3, q7) * sc
+        cols[4 * ww + 0] = h2bits(__hfma2(bits2h(p[0]), mlo[k], add[k]));   // (q0, q4)
+        cols[4 * ww + 1] = h2bits(__hfma2(bits2h(p[1]), mhi[k], add[k]));   // (q1, q5)
+        cols[4 * ww + 2] = h2bits(__hfma2(bits2h(p[2]), mlo[k], add[k]));   // (q2, q6)
+        cols[4 * ww + 3] = h2bits(__hfma2(bits2h(p[3]), mhi[k], add[k]));   // (q3, q7)
       }
       tc::st_x16(aaddr + 16 * k, cols);
     }
@@ -613,24 +762,96 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Hard tokens (q4k_xprep_kernel): their part of a super-block's outputs in fp32 on CUDA cores:
+// this row's packed bytes from the stage at rb (the first 16 in hd), the activations from X
+// (super-block sb of each token's row of K).  Each weight is its format's definition (one
+// rounding of the exact value, as the dequantization hook computes it); the 256 products are
+// summed in order of k.  aux0 / aux1: Q6K d; INT4 the scales of the two K halves; NVFP4 the
+// tensor scale g.
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int FMT>
+__device__ __forceinline__ float weight_at(uint32_t rb, const uint4& hd, int t, float aux0, float aux1) {
+  if constexpr (FMT == kFmtQ4K || FMT == kFmtQ5K) {
+    const int j = t >> 5;
+    const uint64_t F = j < 5 ? ((uint64_t)hd.z << 32 | hd.y) : ((uint64_t)hd.w << 32 | hd.z);
+    const uint32_t gr = (uint32_t)(F >> (j < 5 ? 12 * j : 12 * j - 32)) & 0xFFFu;
+    const float2 dd = __half22float2(bits2h(hd.x));
+    uint32_t q;
+    if constexpr (FMT == kFmtQ4K) {
+      q = (lds_u8(rb + 16 + (t >> 1)) >> (4 * (t & 1))) & 15u;
+    } else {
+      const int c = (t >> 3) & 3, i = t & 7;
+      q = ((lds_u8(rb + 48 + (t >> 1)) >> (4 * (t & 1))) & 15u) + 16u * ((lds_u32(rb + 16 + 4 * j) >> (4 * i + c)) & 1u);
+    }
+    return fmaf(dd.x * (float)(gr & 63u), (float)q, -(dd.y * (float)(gr >> 6)));
+  } else if constexpr (FMT == kFmtQ6K) {
+    const int sc = (int)(lds_u8(rb + (t >> 4)) & 127u) - 64;
+    const int tt = t & 15, a = tt >> 3, i = tt & 7;
+    const uint32_t hi = (lds_u32(rb + 144 + 4 * (t >> 4)) >> (8 * a + 16 * (i >> 2) + 2 * (i & 3))) & 3u;
+    const uint32_t q = ((lds_u8(rb + 16 + (t >> 1)) >> (4 * (t & 1))) & 15u) + 16u * hi;
+    return (aux0 * (float)sc) * (float)((int)q - 32);
+  } else if constexpr (FMT == kFmtNVFP4) {
+    const float sb = __low2float(bits2h(e4m3x2_pair(lds_u8(rb + (t >> 4)))));
+    uint32_t pr;
+    const uint32_t code = lds_u8(rb + 16 + (t >> 1));
+    asm("{\n .reg .b8 b0;\n cvt.u8.u32 b0, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}" : "=r"(pr) : "r"(code));
+    const float v = (t & 1) ? __high2float(bits2h(pr)) : __low2float(bits2h(pr));
+    return aux0 * (sb * v);
+  } else {   // INT4: 128-byte rows copied with the 128-byte swizzle (chunk c at c ^ (row % 8))
+    const uint32_t bi = (uint32_t)t >> 1;
+    const uint32_t rbs = rb ^ ((rb >> 3) & 0x70u);
+    const uint32_t byte = lds_u8((rbs ^ (16u * (bi >> 4))) + (bi & 15u));
+    const int q = ((int)((byte >> (4 * (t & 1))) & 15u) ^ 8) - 8;
+    return (t < 128 ? aux0 : aux1) * (float)q;
+  }
+}
+
+template <int FMT, int MT>
+__device__ __noinline__ void hard_dot(uint32_t rb, const uint16_t* X, int K, int sb, uint4 hd, float aux0, float aux1,
+                                      uint32_t mask, float* out) {
+  for (int k = 0; k < MT; ++k) out[k] = 0.f;
+  for (int t = 0; t < 256; ++t) {
+    const float w = weight_at<FMT>(rb, hd, t, aux0, aux1);
+    for (int k = 0; k < MT; ++k) {
+      if ((mask >> k) & 1u) {
+        const uint32_t xbits = __ldg(X + (int64_t)k * K + (int64_t)sb * 256 + t);
+        out[k] = fmaf(w, __uint_as_float(xbits << 16), out[k]);
+      }
+    }
+  }
+}
+
 // FMT: weight format.  MPAD: MMA width (token columns of B and of the accumulators, 16 or 32).
 // MT: the token columns the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M
 // hold zeros.  GATED: the feed-forward gating in the epilogue (a separate instance: its code in
 // the regular kernels measured 2.5 % slower at M <= 8).
 template <int FMT, int MPAD, int MT, int MAXE, bool GATED>
-__global__ void __launch_bounds__(threads(MPAD, FMT), 1)
+__global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     q4k_tc_kernel(const __grid_constant__ TcParams<MAXE, naux(FMT, MAXE)> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = TcSmem<MPAD, FMT, MT>;
   constexpr int NG = groups(MPAD, FMT);
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
-  constexpr int kMmaWarp = kProdWarp + 1;       // MMA issue; owns TMEM
+  constexpr int kMmaWarp = kProdWarp + 1;       // (first) MMA issue warp; owns TMEM
+  constexpr int kMmaWarps = mma_warps(MPAD, FMT, MT);
   constexpr int kBB = bblock_bytes(MPAD);
   constexpr int kS = stages(MPAD, FMT, MT);
   constexpr int kSB = stage_bytes(MPAD, FMT);
   constexpr int kBlk = blk_bytes(FMT);
   constexpr int kWSB = w_stage_bytes(FMT);
+  constexpr bool kExtInA = ext_in_a(FMT, MT);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t sW = smem_addr(smem + L::kW);   // stage k: weights at sW + k*kSB, activations kWSB further
@@ -647,11 +868,12 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
       mbar_init(bar(kBarAFull + 2 * g), kGroupWarps);
       mbar_init(bar(kBarAFull + 2 * g + 1), kGroupWarps);
       mbar_init(bar(kBarGDone + g), 1);
+      mbar_init(bar(kBarH0Done + g), 1);
     }
     // the consuming group's warps once they hold their bytes, and the MMA commit once the MMAs
     // have read the activations
     for (int k = 0; k < kS; ++k) mbar_init(bar(kBarWEmpty + k), kGroupWarps + 1);
-    mbar_init(bar(kBarDrain), 1);
+    for (int m = 0; m < kMmaWarps; ++m) mbar_init(bar(kBarDrain + m), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -671,9 +893,9 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
   int n[NG];
-  int nmax = 0;
+  int nmax = 0, nmin = 1 << 30;
 #pragma unroll
-  for (int g = 0; g < NG; ++g) { n[g] = group_sbs[g]; nmax = max(nmax, n[g]); }
+  for (int g = 0; g < NG; ++g) { n[g] = group_sbs[g]; nmax = max(nmax, n[g]); nmin = min(nmin, n[g]); }
 
   auto wait = [&](uint32_t b, uint32_t parity) -> bool {
     if (mbar_try(b, parity)) return true;
@@ -725,61 +947,65 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
         mbar_wait(gfull((int)g, ws), ((gbits >> (g * kMaxStages + ws)) & 1u) ^ 1u, kWaitLimit);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
     // Super-block su of group g: its A slot, handed over one K half at a time (each half full
     // once the group's 4 warps have arrived, so the first 8 MMAs run while the group still
     // dequantizes the second half), its activations in stage su % kS, its accumulator (read by
-    // the group before it wrote the A slot again).  One elected lane waits, issues and commits,
-    // in super-block order.
+    // the group before it wrote the A slot again).  The k-quants add two min-term MMAs (A_ext
+    // against B_ext) after the second half.  One elected lane waits, issues and commits, in
+    // super-block order.
+    // Warp kMmaWarp + g serves group g.
+    const int g = warp - kMmaWarp;
     if (elect_one()) {
       constexpr uint32_t idesc = tc::idesc_f16_f32(128, MPAD);
-      uint32_t gbits = 0;   // parity of each (group, stage) full barrier
-      uint32_t su = 0;
-      bool ok = true;
-      for (int i = 0; i < nmax && ok; ++i) {
+      int ngl = 0;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const uint32_t ws = su % kS;
-          const uint32_t bit = 1u << (g * kMaxStages + ws);
-          if (ok && i < n[g])
-            ok = wait(bar(kBarAFull + 2 * g), (uint32_t)i & 1u) && wait(gfull(g, ws), (gbits & bit) ? 1u : 0u);
-          if (ok && i < n[g]) {
-            gbits ^= bit;
-            tc::fence_after_sync();
-            const uint64_t bdesc = tc::smem_desc_kmajor(sW + ws * kSB + kWSB, 128, 4096);   // + 16 per MMA: 256 bytes
-            tc::mma_f16_ts_x8(tmem + acc1_col(MPAD, g, FMT), tmem + a_col(g), bdesc, 16, idesc, 0);
-            ok = wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u);
-          }
-          if (ok && i < n[g]) {
-            tc::fence_after_sync();
-            const uint32_t abase = tmem + a_col(g);
-            const uint32_t d1 = tmem + acc1_col(MPAD, g, FMT);
-            const uint32_t d2 = tmem + acc2_col(MPAD, g, FMT);
-            const uint32_t bslot = sW + ws * kSB + kWSB;
-            const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);
-            if constexpr (FMT == kFmtINT4) {
-              // the second K half has its own scale: its own accumulator
-              tc::mma_f16_ts_x8(d2, abase + 64, bdesc + 8 * 16, 16, idesc, 0);
-            } else {
-              tc::mma_f16_ts_x8(d1, abase + 64, bdesc + 8 * 16, 16, idesc, 1);
-            }
-            if constexpr (has_min(FMT))
-              tc::mma_f16_ts(d2, abase + 128, tc::smem_desc_kmajor(bslot + MPAD * 512, 128, 256), idesc, 0);
-            tc::commit(bar(kBarGDone + g));
-            tc::commit(bar(kBarWEmpty + ws));
-            ++su;
-          }
+      for (int h = 0; h < NG; ++h) if (h == g) ngl = n[h];
+      const uint32_t abase = tmem + a_col(g, FMT, MT);
+      const uint32_t d1 = tmem + acc1_col(MPAD, g, FMT, MT);
+      const uint32_t d2 = tmem + acc2_col(MPAD, g, FMT, MT);
+      uint32_t gbits = 0;   // parity of this group's full barrier of each stage
+      for (int i = 0; i < ngl; ++i) {
+        const uint32_t ws = su_of<NG>(n, g, i, nmin) % kS;
+        if (!(wait(bar(kBarAFull + 2 * g), (uint32_t)i & 1u) && wait(gfull(g, ws), (gbits >> ws) & 1u))) break;
+        gbits ^= 1u << ws;
+        tc::fence_after_sync();
+        const uint32_t bslot = sW + ws * kSB + kWSB;
+        const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
+        tc::mma_f16_ts_x8(d1, abase, bdesc, 16, idesc, 0);
+        if constexpr (kExtInA) tc::commit(bar(kBarH0Done + g));   // the group may reuse these A columns
+        if (!wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u)) break;
+        tc::fence_after_sync();
+        if constexpr (FMT == kFmtINT4) {
+          // the second K half has its own scale: its own accumulator
+          tc::mma_f16_ts_x8(d2, abase + 64, bdesc + 8 * 16, 16, idesc, 0);
+        } else {
+          tc::mma_f16_ts_x8(d1, abase + 64, bdesc + 8 * 16, 16, idesc, 1);
         }
+        if constexpr (has_min(FMT)) {
+          // the min term: A_ext (16 columns, K = 32) against B_ext, into the product's
+          // accumulator (8 token columns: B_ext fills columns 8..15) or its own
+          constexpr bool kShiftExt = MT == 8;   // the min term in columns 8..15 of d1
+          const uint64_t edesc = tc::smem_desc_kmajor(bslot + bext_off(MPAD), 128, 512);
+          const uint32_t ea = abase + (kExtInA ? 0u : 128u);
+          tc::mma_f16_ts(kShiftExt ? d1 : d2, ea, edesc, idesc, kShiftExt ? 1u : 0u);
+          tc::mma_f16_ts(kShiftExt ? d1 : d2, ea + 8, edesc + 16, idesc, 1u);
+        }
+        tc::commit(bar(kBarGDone + g));
+        tc::commit(bar(kBarWEmpty + ws));
       }
       // every MMA issued has finished before TMEM is released
-      tc::commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0u, kWaitLimit);
+      tc::commit(bar(kBarDrain + g));
+      mbar_wait(bar(kBarDrain + g), 0u, kWaitLimit);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
-    // ------------------------------------------------------------------ dequant + epilogue
+    // Software-pipelined over the group's super-blocks: once super-block i is handed to the
+    // MMA warp, the group waits for the stage of super-block i+1 and computes what does not
+    // need tensor memory (its per-token scales, hard tokens, the k-quant fold constants) while
+    // the MMAs of i run; then it reads i's accumulator, and decodes i+1.
     const int grp = warp >> 2;       // dequant group: the CTA's local tasks j % NG == grp
     const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
     const int r = 32 * q + lane;     // row inside the tile
@@ -791,7 +1017,7 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
 #pragma unroll
     for (int k = 0; k < MT; ++k) y[k] = 0.f;
     // the task's running sum of chunk sums: registers, or shared memory (token k at [k * 128])
-    // for 32 tokens
+    // for 16 and 32 tokens
     constexpr bool kYtotSmem = MT >= 16;
     float ytot_r[kYtotSmem ? 1 : MT];
     float* ytot_s = reinterpret_cast<float*>(smem + L::kYtot) + (size_t)grp * MT * kTileRows + r;
@@ -799,43 +1025,198 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
     for (int k = 0; k < (kYtotSmem ? 1 : MT); ++k) ytot_r[k] = 0.f;
     auto ytot = [&](int k) -> float& { if constexpr (kYtotSmem) return ytot_s[k * kTileRows]; else return ytot_r[k]; };
 
-    const uint32_t aslot = tl + a_col(grp);         // this group's A slot (this warp's lanes)
-    const uint32_t acc1 = tl + acc1_col(MPAD, grp, FMT);  // and accumulators
-    const uint32_t acc2 = tl + acc2_col(MPAD, grp, FMT);
+    const uint32_t aslot = tl + a_col(grp, FMT, MT);           // this group's A slot (this warp's lanes)
+    const uint32_t aext = aslot + (kExtInA ? 0u : 128u);         // its min-term columns
+    const uint32_t acc1 = tl + acc1_col(MPAD, grp, FMT, MT);    // and accumulators
+    const uint32_t acc2 = tl + acc2_col(MPAD, grp, FMT, MT);
+    // this warp's copies of the per-token scales of two super-blocks in flight (by parity)
+    float* sigw = reinterpret_cast<float*>(smem + L::kSig) + warp * 64;
+    float hard_sum[2][MT];   // the hard tokens' sums of the super-blocks in flight (rarely used)
     asm volatile("griddepcontrol.wait;" ::: "memory");   // split counters zeroed, activations written
     uint32_t sbits = 0;   // parity of this group's full barrier of each stage
-    GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur;
-    cur.start(P, grp);
-    // With two groups (Mpad 32) the stage, header and 2^s of a group's next super-block are
-    // fetched while the MMAs of the current one run (measured faster there; with three groups,
-    // fetching them at the start of the iteration measured faster).
-    constexpr bool kFetchEarly = NG == 2;
-    uint32_t ws_n = 0;
-    uint4 hd_n = make_uint4(0, 0, 0, 0);
-    float sigma_n = 0.f;
-    for (int i = 0; cur.t >= 0; ++i) {
-      uint32_t ws;
-      uint4 hd;
-      float sigma;
-      if (kFetchEarly && i > 0) {
-        ws = ws_n;
-        hd = hd_n;
-        sigma = sigma_n;
-      } else {
-        ws = su_of<NG>(n, grp, i) % kS;
-        if (!wait_w(gfull(grp, ws), (sbits >> ws) & 1u)) break;
-        sbits ^= 1u << ws;
-        // this row's header and 2^s of the activation block from the stage
-        hd = FMT == kFmtINT4 ? make_uint4(0, 0, 0, 0) : lds128(sW + ws * kSB + r * kBlk);
-        sigma = lds_f32(sW + ws * kSB + kWSB + MPAD * 544);
+
+    // What the look-ahead of a super-block yields.
+    struct Ahead {
+      uint32_t ws;        // its stage
+      uint4 hd;           // this row's first 16 bytes
+      uint32_t hmask;     // its hard tokens
+      uint32_t add[8];    // k-quants: the pairs (-k_j 2^-14, sc_j 2^10) of the decode
+      uint32_t ext[8];    //           the A_ext pairs of rho_j T
+    };
+    // Wait for the i-th super-block of the group (task position c) and prepare it.
+    auto ahead = [&](int i, const GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG>& c, Ahead& A) -> bool {
+      A.ws = su_of<NG>(n, grp, i, nmin) % kS;
+      if (!wait_w(gfull(grp, A.ws), (sbits >> A.ws) & 1u)) return false;
+      sbits ^= 1u << A.ws;
+      const uint32_t rb = sW + A.ws * kSB + r * kBlk;
+      const uint32_t xblk = sW + A.ws * kSB + kWSB;
+      A.hd = FMT == kFmtINT4 ? make_uint4(0, 0, 0, 0) : lds128(rb);
+      float* sg = sigw + 32 * (i & 1);
+      if (lane < MT / 4) *reinterpret_cast<uint4*>(sg + 4 * lane) = lds128(xblk + sig_off(MPAD) + 16 * lane);
+      A.hmask = lds_u32(xblk + mask_off(MPAD)) & (MT == 32 ? 0xFFFFFFFFu : ((1u << MT) - 1u));
+      if (A.hmask != 0u) {   // uniform over the CTA: the mask belongs to the super-block of X
+        float a0 = 0.f, a1 = 0.f;
+        const TcEntry& E0 = P.e[c.e];
+        const int row0 = c.tile * kTileRows + r;
+        if constexpr (FMT == kFmtQ6K) {
+          if (row0 < E0.N)
+            a0 = __half2float(__ushort_as_half(
+                __ldg(static_cast<const unsigned short*>(P.aux[c.e]) + (int64_t)row0 * (E0.K >> 8) + c.sb)));
+        } else if constexpr (FMT == kFmtINT4) {
+          if (row0 < E0.N) {
+            const uint32_t sc2 = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux[c.e]) +
+                                                                         (int64_t)row0 * (E0.K >> 7)) + c.sb);
+            a0 = __low2float(bits2h(sc2));
+            a1 = __high2float(bits2h(sc2));
+          }
+        } else if constexpr (FMT == kFmtNVFP4) {
+          a0 = __ldg(static_cast<const float*>(P.aux[c.e]));
+        }
+        const uint4 tr = lds128(xblk + mask_off(MPAD));   // (mask, K, address of X)
+        const uint16_t* X = reinterpret_cast<const uint16_t*>((uint64_t)tr.z | ((uint64_t)tr.w << 32));
+        hard_dot<FMT, MT>(rb, X, (int)tr.y, c.sb, A.hd, a0, a1, A.hmask, hard_sum[i & 1]);
       }
-      // ---- the rest of this row's super-block (quants one K half at a time) from the stage;
-      // this warp's part of the stage is released once all are read
-      const uint32_t rb = sW + ws * kSB + r * kBlk;
+      if constexpr (has_min(FMT)) fold_consts(A.hd, dc, A.add, A.ext);
+      return true;
+    };
 
-      // (the A slot is free: this group waited for its previous MMAs below)
-
+    using Cursor = GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG>;
+    int ng = 0;   // super-blocks of this group
 #pragma unroll
+    for (int h = 0; h < NG; ++h) if (h == grp) ng = n[h];
+    // Iteration i: look ahead to super-block i (the only call site of ahead), finish super-block
+    // i - 1 (its accumulator, once its MMAs are done), then decode super-block i and hand it to
+    // the MMA warp.
+    Cursor cur;          // the super-block being finished (i - 1)
+    Cursor nx;           // super-block i
+    nx.start(P, grp);
+    Ahead A;
+    bool task_end = false;                 // super-block i - 1 ended its task
+    float sx = 0.f, sy = 0.f;              // the accumulator factors of super-block i - 1
+    uint32_t hm = 0;                       // its hard tokens
+    for (int i = 0;; ++i) {
+      if (i < ng && !ahead(i, nx, A)) break;
+      if (i >= 1) {
+        // ---- the accumulator of super-block i - 1 into y (MT token columns)
+        if (!wait_w(bar(kBarGDone + grp), (uint32_t)(i - 1) & 1u)) break;
+        tc::fence_after_sync();
+        constexpr bool kTwo = FMT != kFmtNVFP4 && FMT != kFmtQ6K;   // a second accumulator block to read
+        constexpr bool kShift = has_min(FMT) && MT == 8;             // the min term in columns 8..15
+        constexpr int kW = MT == 16 ? 16 : 8;   // token columns per TMEM read round
+        const float* sg_i = sigw + 32 * ((i - 1) & 1);
+#pragma unroll
+        for (int c0 = 0; c0 < MT; c0 += kW) {
+          float a1[kW], a2[kW];
+          if constexpr (kShift) {
+            float a[16];
+            tc::ld_x16(acc1, a);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) { a1[k] = a[k]; a2[k] = a[8 + k]; }
+          } else if constexpr (kW == 8) {
+            tc::ld_x8(acc1 + c0, a1);
+            if constexpr (kTwo) tc::ld_x8(acc2 + c0, a2);
+          } else {
+            tc::ld_x16(acc1 + c0, a1);
+            if constexpr (kTwo) tc::ld_x16(acc2 + c0, a2);
+          }
+          tc::wait_ld();
+#pragma unroll
+          for (int k = 0; k < kW; k += 4) {
+            const float4 sg = *reinterpret_cast<const float4*>(sg_i + c0 + k);
+            const float sgk[4] = {sg.x, sg.y, sg.z, sg.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if constexpr (kTwo) y[c0 + k + u] = fmaf(sgk[u], fmaf(sx, a1[k + u], sy * a2[k + u]), y[c0 + k + u]);
+              else y[c0 + k + u] = fmaf(sx * sgk[u], a1[k + u], y[c0 + k + u]);
+            }
+          }
+        }
+        // hard tokens: their accumulator columns are exactly 0; add their CUDA-core sums
+        if (hm != 0u) {
+#pragma unroll
+          for (int k = 0; k < MT; ++k)
+            if ((hm >> k) & 1u) y[k] += hard_sum[(i - 1) & 1][k];
+        }
+
+        // ---- end of a chunk: y (this chunk's sum) is added to the task's running sum, or, for a
+        // split task, stored as the chunk's partial.  End of a task: the running
+        // sum goes to Y; a split task counts itself in, and the last split of this (tile, lane
+        // quarter) slice adds every chunk partial of the tile in chunk order.
+        const int e = cur.e, tile = cur.tile, sb = cur.sb;
+        const TcEntry& E = P.e[e];
+        const int nb = E.K >> 8;
+        if ((sb + 1) % kChunkSb == 0 || sb + 1 == nb) {
+          if (E.splits == 1) {
+            if (sb < kChunkSb) {
+#pragma unroll
+              for (int k = 0; k < MT; ++k) ytot(k) = y[k];
+            } else {
+#pragma unroll
+              for (int k = 0; k < MT; ++k) ytot(k) = ytot(k) + y[k];
+            }
+          } else {
+            float* part = E.partial + ((size_t)tile * E.chunks + sb / kChunkSb) * (MPAD * kTileRows) + r;
+#pragma unroll
+            for (int k = 0; k < MT; ++k)
+              if (k < P.M) part[k * kTileRows] = y[k];
+          }
+#pragma unroll
+          for (int k = 0; k < MT; ++k) y[k] = 0.f;
+        }
+        if (task_end) {
+          const int row = tile * kTileRows + r;
+          if constexpr (GATED) {
+            // the feed-forward gating in the epilogue: lane r holds row 2f (gate) or 2f+1 (up) of
+            // the same tile; the even lane forms silu(gate) * up in fp32 and stores its bf16
+            // (round to nearest even), silu(g) = g / (1 + e^-g)
+            uint16_t* H = reinterpret_cast<uint16_t*>(E.Y);
+            if constexpr (kYtotSmem) {
+              gate_store_smem<MT>(ytot_s, r, row, E.N, P.M, H);
+            } else {
+              const int64_t F = E.N >> 1;
+#pragma unroll
+              for (int k = 0; k < MT; ++k) {
+                const float mine = ytot(k);
+                const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                if (k < P.M && !(r & 1) && row < E.N) {
+                  const float h = mine / (1.0f + expf(-mine)) * other;
+                  const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+                  H[(int64_t)k * F + (row >> 1)] = *reinterpret_cast<const uint16_t*>(&hb);
+                }
+              }
+            }
+          } else if (E.splits == 1) {
+            if (row < E.N) {
+#pragma unroll
+              for (int k = 0; k < MT; ++k)
+                if (k < P.M) E.Y[(int64_t)k * E.N + row] = ytot(k);
+            }
+          } else {
+            // the warp's partial stores, then one release of them (the warp barrier orders the
+            // other lanes' stores before lane 0's fence) and the arrival count of this slice
+            __syncwarp();
+            unsigned old = 0;
+            if (lane == 0) {
+              fence_acq_rel_gpu();   // release of the warp's partial sums
+              old = atomicAdd(&E.counters[tile * kGroupWarps + q], 1u);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == (unsigned)(E.splits - 1)) {
+              fence_acq_rel_gpu();   // acquire of the other splits' partial sums
+              reduce_chunks<MPAD, MT>(E.partial + (size_t)tile * E.chunks * (MPAD * kTileRows) + r, E.chunks, P.M,
+                                  row < E.N ? E.Y + row : nullptr, E.N);
+            }
+          }
+        }
+      }
+      if (i >= ng) break;
+      const uint32_t ws = A.ws;
+      const uint4 hd = A.hd;
+      const uint32_t rb = sW + ws * kSB + r * kBlk;   // this row's bytes of the super-block
+      // ---- decode: the row's super-block one K half at a time from the stage (this warp's part
+      // of the stage is released once all is read), each half handed to the MMA warp
+      // (the A slot is free: this group read its previous accumulator above)
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         HalfIn<FMT> in;
         load_half<FMT>(in, rb, h);
@@ -843,7 +1224,10 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         }
-        decode_half<FMT>(in, hd, h, aslot + 64u * h, dc);
+        uint32_t a4[4];   // the half's sub-blocks' precomputed pairs
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) a4[jj] = h ? A.add[4 + jj] : A.add[jj];
+        decode_half<FMT>(in, hd, h, aslot + 64u * h, dc, a4);
         if (h == 0) {   // the first K half goes to the MMA warp now
           tc::wait_st();
           tc::fence_before_sync();
@@ -851,168 +1235,62 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
           if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp));
         }
       }
-      // INT4: the scales of this row's two K halves, from the scale plane (read now, used by
-      // the epilogue once the MMAs are done)
-      // Q6K: the row's super-block scale d, from its plane
+      // INT4: the scales of this row's two K halves, from the scale plane; Q6K: the row's
+      // super-block scale d, from its plane (read now, used by the epilogue)
+      const int row0 = nx.tile * kTileRows + r;
       uint32_t int4_scales = 0;
       if constexpr (FMT == kFmtINT4) {
-        const TcEntry& E0 = P.e[cur.e];
-        const int row0 = cur.tile * kTileRows + r;
+        const TcEntry& E0 = P.e[nx.e];
         if (row0 < E0.N)
-          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux[cur.e]) +
-                                                                (int64_t)row0 * (E0.K >> 7)) + cur.sb);
+          int4_scales = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux[nx.e]) +
+                                                                (int64_t)row0 * (E0.K >> 7)) + nx.sb);
       } else if constexpr (FMT == kFmtQ6K) {
-        const TcEntry& E0 = P.e[cur.e];
-        const int row0 = cur.tile * kTileRows + r;
+        const TcEntry& E0 = P.e[nx.e];
         if (row0 < E0.N)
-          int4_scales = __ldg(static_cast<const unsigned short*>(P.aux[cur.e]) + (int64_t)row0 * (E0.K >> 8) + cur.sb);
+          int4_scales = __ldg(static_cast<const unsigned short*>(P.aux[nx.e]) + (int64_t)row0 * (E0.K >> 8) + nx.sb);
       }
       if constexpr (has_min(FMT)) {
-        // A_ext: (m_0..m_7) at k = 0..7 and again at k = 8..15
-        const __half2 k1024 = dc.k1024;
-        const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 (bits 0..47)
-        const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 (bits 16..63)
-        uint32_t mm[8];
+        // A_ext: the pair (hi_j, lo_j) of rho_j T twice per sub-block (against B_ext rows
+        // (X_hi, X_hi) and (X_lo, X_lo)); where it reuses the first K half's columns, after
+        // that half's MMAs have completed
+        if constexpr (kExtInA) {
+          if (!wait_w(bar(kBarH0Done + grp), (uint32_t)i & 1u)) break;
+          tc::fence_after_sync();
+        }
+        uint32_t cols[16];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-          mm[jj] = (uint32_t)((jj < 4 ? (G >> (12 * jj)) : (H >> (16 + 12 * (jj - 4)))) >> 6) & 63u;
-        uint32_t ext[8];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          ext[cc] = ext[cc + 4] =
-              h2bits(__hsub2(bits2h((mm[2 * cc] | 0x6400u) | ((mm[2 * cc + 1] | 0x6400u) << 16)), k1024));
-        tc::st_x8(aslot + 128u, ext);
+        for (int jj = 0; jj < 8; ++jj) cols[2 * jj] = cols[2 * jj + 1] = A.ext[jj];
+        tc::st_x16(aext, cols);
       }
       // ---- hand the second K half (and A_ext) to the MMA warp
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarAFull + 2 * grp + 1));
-      if constexpr (kFetchEarly) {
-        if (i + 1 < n[grp]) {
-          ws_n = su_of<NG>(n, grp, i + 1) % kS;
-          if (!wait_w(gfull(grp, ws_n), (sbits >> ws_n) & 1u)) break;
-          sbits ^= 1u << ws_n;
-          hd_n = FMT == kFmtINT4 ? make_uint4(0, 0, 0, 0) : lds128(sW + ws_n * kSB + r * kBlk);
-          sigma_n = lds_f32(sW + ws_n * kSB + kWSB + MPAD * 544);
-        }
-      }
 
-      // ---- the accumulator of this super-block into y (MT token columns)
-      if (!wait_w(bar(kBarGDone + grp), (uint32_t)i & 1u)) break;
-      tc::fence_after_sync();
-      // the factors of the two accumulator blocks:
-      //   k-quants  y += (D 2^s) acc - (Dm 2^s 64) acc_ext
-      //   NVFP4     y += (g 2^s) acc
-      //   INT4      y += (s_0 2^s) acc_half0 + (s_1 2^s) acc_half1
-      //   Q6K       y += (d 2^s) acc
-      float sx, sy;
+      // the factors of the accumulator blocks (sigma_k = 2^(s_k + 14) of token k applied last):
+      //   k-quants  y += sigma (D acc + fe acc_ext)          (A = (sc q - k) 2^-14)
+      //   NVFP4     y += sigma (g 2^-14) acc
+      //   INT4      y += sigma 2^-14 (s_0 acc_half0 + s_1 acc_half1)
+      //   Q6K       y += sigma (d 2^-14) acc
       if constexpr (has_min(FMT)) {
         const float2 dd = __half22float2(bits2h(hd.x));   // (D, Dm) of this row
-        sx = dd.x * sigma;
-        sy = -(dd.y * sigma * 64.f);
+        sx = dd.x;
+        sy = fold_ext_factor(dd.y);
       } else if constexpr (FMT == kFmtNVFP4) {
-        sx = __ldg(static_cast<const float*>(P.aux[cur.e])) * sigma;
+        sx = __ldg(static_cast<const float*>(P.aux[nx.e])) * 0x1p-14f;
         sy = 0.f;
       } else if constexpr (FMT == kFmtQ6K) {
-        sx = __half2float(__ushort_as_half((unsigned short)int4_scales)) * sigma;
+        sx = __half2float(__ushort_as_half((unsigned short)int4_scales)) * 0x1p-14f;
         sy = 0.f;
       } else {
         const float2 ss = __half22float2(bits2h(int4_scales));
-        sx = ss.x * sigma;
-        sy = ss.y * sigma;
+        sx = ss.x * 0x1p-14f;
+        sy = ss.y * 0x1p-14f;
       }
-      constexpr bool kTwo = FMT != kFmtNVFP4 && FMT != kFmtQ6K;   // a second accumulator block to read
-      constexpr int kW = MT == 16 ? 16 : 8;   // token columns per TMEM read round
-#pragma unroll
-      for (int c0 = 0; c0 < MT; c0 += kW) {
-        float a1[kW], a2[kW];
-        if constexpr (kW == 8) {
-          tc::ld_x8(acc1 + c0, a1);
-          if constexpr (kTwo) tc::ld_x8(acc2 + c0, a2);
-        } else {
-          tc::ld_x16(acc1 + c0, a1);
-          if constexpr (kTwo) tc::ld_x16(acc2 + c0, a2);
-        }
-        tc::wait_ld();
-#pragma unroll
-        for (int k = 0; k < kW; ++k) {
-          y[c0 + k] = fmaf(sx, a1[k], y[c0 + k]);
-          if constexpr (kTwo) y[c0 + k] = fmaf(sy, a2[k], y[c0 + k]);
-        }
-      }
-
-      // ---- end of a chunk: y (this chunk's sum) is added to the task's running sum, or, for a
-      // split task, stored as the chunk's partial.  End of a task: the running
-      // sum goes to Y; a split task counts itself in, and the last split of this (tile, lane
-      // quarter) slice adds every chunk partial of the tile in chunk order.
-      const int e = cur.e, tile = cur.tile, sb = cur.sb;
-      const TcEntry& E = P.e[e];
-      const int nb = E.K >> 8;
-      const bool task_end = cur.advance(P);
-      if ((sb + 1) % kChunkSb == 0 || sb + 1 == nb) {
-        if (E.splits == 1) {
-          if (sb < kChunkSb) {
-#pragma unroll
-            for (int k = 0; k < MT; ++k) ytot(k) = y[k];
-          } else {
-#pragma unroll
-            for (int k = 0; k < MT; ++k) ytot(k) = ytot(k) + y[k];
-          }
-        } else {
-          float* part = E.partial + ((size_t)tile * E.chunks + sb / kChunkSb) * (MPAD * kTileRows) + r;
-#pragma unroll
-          for (int k = 0; k < MT; ++k)
-            if (k < P.M) part[k * kTileRows] = y[k];
-        }
-#pragma unroll
-        for (int k = 0; k < MT; ++k) y[k] = 0.f;
-      }
-      if (task_end) {
-        const int row = tile * kTileRows + r;
-        if constexpr (GATED) {
-          // the feed-forward gating in the epilogue: lane r holds row 2f (gate) or 2f+1 (up) of
-          // the same tile; the even lane forms silu(gate) * up in fp32 and stores its bf16
-          // (round to nearest even), silu(g) = g / (1 + e^-g)
-          uint16_t* H = reinterpret_cast<uint16_t*>(E.Y);
-          if constexpr (kYtotSmem) {
-            gate_store_smem<MT>(ytot_s, r, row, E.N, P.M, H);
-          } else {
-            const int64_t F = E.N >> 1;
-#pragma unroll
-            for (int k = 0; k < MT; ++k) {
-              const float mine = ytot(k);
-              const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-              if (k < P.M && !(r & 1) && row < E.N) {
-                const float h = mine / (1.0f + expf(-mine)) * other;
-                const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-                H[(int64_t)k * F + (row >> 1)] = *reinterpret_cast<const uint16_t*>(&hb);
-              }
-            }
-          }
-        } else if (E.splits == 1) {
-          if (row < E.N) {
-#pragma unroll
-            for (int k = 0; k < MT; ++k)
-              if (k < P.M) E.Y[(int64_t)k * E.N + row] = ytot(k);
-          }
-        } else {
-          // the warp's partial stores, then one release of them (the warp barrier orders the
-          // other lanes' stores before lane 0's fence) and the arrival count of this slice
-          __syncwarp();
-          unsigned old = 0;
-          if (lane == 0) {
-            fence_acq_rel_gpu();   // release of the warp's partial sums
-            old = atomicAdd(&E.counters[tile * kGroupWarps + q], 1u);
-          }
-          old = __shfl_sync(0xffffffffu, old, 0);
-          if (old == (unsigned)(E.splits - 1)) {
-            fence_acq_rel_gpu();   // acquire of the other splits' partial sums
-            reduce_chunks<MPAD, MT>(E.partial + (size_t)tile * E.chunks * (MPAD * kTileRows) + r, E.chunks, P.M,
-                                row < E.N ? E.Y + row : nullptr, E.N);
-          }
-        }
-      }
+      hm = A.hmask;
+      cur = nx;
+      task_end = nx.advance(P);
     }
   }
 
@@ -1030,13 +1308,11 @@ __global__ void __launch_bounds__(threads(MPAD, FMT), 1)
 class Workspace {
  public:
   static cudaError_t get(cudaStream_t stream, size_t bytes, void** out) {
-    static std::mutex mu;
-    static std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> pool;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    std::lock_guard<std::mutex> g(mu);
-    auto& slot = pool[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    std::lock_guard<std::mutex> g(mu());
+    auto& slot = pool()[{dev, reinterpret_cast<uintptr_t>(stream)}];
     if (slot.second < bytes) {
       if (slot.first) {
         err = cudaFree(slot.first);
@@ -1051,6 +1327,36 @@ class Workspace {
     }
     *out = slot.first;
     return cudaSuccess;
+  }
+  // Free every workspace (each with its device current; cudaFree waits for the work that may
+  // still use it).  The calling thread's current device is restored.
+  static cudaError_t release() {
+    std::lock_guard<std::mutex> g(mu());
+    if (pool().empty()) return cudaSuccess;
+    int cur = 0;
+    cudaError_t first = cudaGetDevice(&cur);
+    for (auto& kv : pool()) {
+      if (!kv.second.first) continue;
+      cudaError_t err = cudaSetDevice(kv.first.first);
+      if (err == cudaSuccess) err = cudaFree(kv.second.first);
+      if (err != cudaSuccess && first == cudaSuccess) first = err;
+    }
+    pool().clear();
+    const cudaError_t e2 = cudaSetDevice(cur);
+    return first != cudaSuccess ? first : e2;
+  }
+  static size_t held_bytes() {
+    std::lock_guard<std::mutex> g(mu());
+    size_t b = 0;
+    for (auto& kv : pool()) b += kv.second.second;
+    return b;
+  }
+
+ private:
+  static std::mutex& mu() { static std::mutex m; return m; }
+  static std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>>& pool() {
+    static std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> p;
+    return p;
   }
 };
 
@@ -1195,7 +1501,7 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)std::min(tasks, num_sms()));
-  cfg.blockDim = dim3(threads(MPAD, FMT));
+  cfg.blockDim = dim3(0);   // set with the instance below
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1209,12 +1515,14 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
           cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE, true>();
           if (err != cudaSuccess) return err;
           cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
+          cfg.blockDim = dim3(cta_threads(MPAD, FMT, 8));
           return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE, true>, par);
         }
       }
       cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE, true>();
       if (err != cudaSuccess) return err;
       cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
+      cfg.blockDim = dim3(cta_threads(MPAD, FMT, MPAD));
       return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE, true>, par);
     }
   } else {
@@ -1225,12 +1533,14 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
       cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE, false>();
       if (err != cudaSuccess) return err;
       cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
+      cfg.blockDim = dim3(cta_threads(MPAD, FMT, 8));
       return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE, false>, par);
     }
   }
   cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE, false>();
   if (err != cudaSuccess) return err;
   cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
+  cfg.blockDim = dim3(cta_threads(MPAD, FMT, MPAD));
   return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE, false>, par);
 }
 
@@ -1242,6 +1552,7 @@ cudaError_t launch_prep_n(const std::vector<std::pair<const uint16_t*, int64_t>>
   prep.M = M;
   prep.zero = zero;
   prep.zero_words = (int)zero_words;
+  prep.shift_ext = (MPAD == 16 && M <= 8) ? 1 : 0;   // the 8-token kernels read the min term from columns 8..15
   int blocks = 0;
   for (size_t u = 0; u < xs.size(); ++u) {
     prep.e[u] = PrepEntry{xs[u].first, outs[u], (int)xs[u].second, blocks};
@@ -1355,6 +1666,9 @@ cudaError_t launch_tc_noalloc_t(const Job& job, int M, cudaStream_t stream, uint
 }
 
 }  // namespace
+
+cudaError_t release_workspaces() { return Workspace::release(); }
+size_t workspace_bytes_held() { return Workspace::held_bytes(); }
 
 cudaError_t read_and_clear_tc_status(unsigned* out) {
   unsigned v = 0, zero = 0;

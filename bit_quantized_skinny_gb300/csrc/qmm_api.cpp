@@ -377,6 +377,13 @@ int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M) 
   return select_variant_jobs(jobs, count, M);
 }
 
+qmm_status qmm_release(void) {
+  const cudaError_t e = q4k::release_workspaces();
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
+size_t qmm_workspace_bytes_held(void) { return q4k::workspace_bytes_held(); }
+
 qmm_status qmm_device_status(unsigned* status_out) {
   if (!status_out) return QMM_ERR_NULL;
   unsigned a = 0, b = 0;

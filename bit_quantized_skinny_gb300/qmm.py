@@ -35,7 +35,7 @@ EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_de
            "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
            "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed",
            "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant", "qmm_fmt_run_batched",
-           "qmm_ffn_fused_workspace_bytes", "qmm_run_ffn_fused"]
+           "qmm_ffn_fused_workspace_bytes", "qmm_run_ffn_fused", "qmm_release", "qmm_workspace_bytes_held"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -82,6 +82,10 @@ def load(path: str | None = None):
     lib.qmm_run_variant.restype = i32
     lib.qmm_run_noalloc.argtypes = [vp, i64, i64, vp, vp, i32, vp]
     lib.qmm_run_noalloc.restype = i32
+    lib.qmm_release.argtypes = []
+    lib.qmm_release.restype = i32
+    lib.qmm_workspace_bytes_held.argtypes = []
+    lib.qmm_workspace_bytes_held.restype = ctypes.c_size_t
     lib.qmm_run_batched.argtypes = [ctypes.POINTER(_Entry), i32, i32, vp]
     lib.qmm_run_batched.restype = i32
     lib.qmm_dequant.argtypes = [vp, i64, i64, vp, vp]
@@ -302,6 +306,16 @@ def select_variant(M: int, N: int, K: int) -> int:
 
 def select_variant_batched(entries, M: int) -> int:
     return load().qmm_select_variant_batched(entries, len(entries), M)
+
+
+def release() -> None:
+    """qmm_release: free every tensor-core workspace the library holds (synchronous)."""
+    _check(load().qmm_release(), "qmm_release")
+
+
+def workspace_bytes_held() -> int:
+    """qmm_workspace_bytes_held: device bytes the tensor-core workspaces hold now."""
+    return int(load().qmm_workspace_bytes_held())
 
 
 def device_status() -> int:

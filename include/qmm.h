@@ -64,9 +64,13 @@
  *     before anything is enqueued.  A launch failure returns QMM_ERR_CUDA (the CUDA error
  *     text is available from qmm_last_cuda_error).  Faults that happen while a kernel runs
  *     surface at the caller's next synchronization, as for any CUDA kernel.
- *   - The library allocates no device memory on any call.  Calls on different streams may
- *     run concurrently; the only mutable global state is a per-device cache of launch
- *     attributes, written once under a lock.
+ *   - Device memory: the tensor-core kernel keeps a workspace per (device, stream) for its
+ *     prepared activations and K-split partial sums.  The first call on a stream that runs that
+ *     kernel, and any later call that needs more room, allocates it with cudaMalloc (growing it
+ *     frees the smaller one, which synchronizes the device); qmm_release frees every such
+ *     workspace.  Every other buffer is the caller's.  qmm_run_noalloc allocates nothing.
+ *   - Calls on different streams may run concurrently; the mutable global state (the workspace
+ *     pool, a per-device cache of launch attributes and of tensor maps) is guarded by locks.
  */
 #ifndef QMM_H
 #define QMM_H
@@ -175,8 +179,8 @@ int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M);
  * never does: it computes the same product with the tensor-core kernel and keeps the prepared
  * activations in a fixed buffer of QMM_NOALLOC_SCRATCH_BYTES (4 MiB) that is part of the
  * library's device image, held by every GPU that loads the library until the process exits.
- *   - Limit: (K/256) * (Mpad*544 + 16) bytes must fit, Mpad = 16 for M <= 16 and 32 above:
- *     K <= 61440 for M > 16, K <= 122880 for M <= 16.  Larger problems return QMM_ERR_SCRATCH
+ *   - Limit: (K/256) * (Mpad*580 + 16) bytes must fit, Mpad = 16 for M <= 16 and 32 above:
+ *     K <= 57600 for M > 16, K <= 115456 for M <= 16.  Larger problems return QMM_ERR_SCRATCH
  *     before anything is enqueued.
  *   - The first call on each device looks up the buffer's device address (cudaGetSymbolAddress)
  *     with that device current; make that first call before any stream capture.
@@ -337,6 +341,17 @@ qmm_status qmm_fmt_run_batched(const qmm_fmt_entry* entries_host, int count, int
  * with the decode steps of the product kernel.  Bit-exact to the definitions above. */
 qmm_status qmm_fmt_dequant(int fmt, const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
                            cudaStream_t stream);
+
+/* Free every tensor-core workspace the library holds (one per device and stream that ran the
+ * tensor-core kernel; see "Device memory" above).  A synchronous call: cudaFree waits for the
+ * work that may still use a workspace.  Later calls allocate again as needed.  Do not call it
+ * while a stream that the library uses is being captured into a CUDA graph, or while a graph
+ * that recorded a call of this library may still be launched (the graph refers to the freed
+ * workspace).  Errors: QMM_ERR_CUDA. */
+qmm_status qmm_release(void);
+
+/* Bytes of device memory the tensor-core workspaces hold now (0 after qmm_release). */
+size_t qmm_workspace_bytes_held(void);
 
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the

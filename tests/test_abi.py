@@ -222,3 +222,9 @@ def test_packed_weights_fmt_replicates_rows(qmm, fmt_name):
     if fmt == qmm.FMT_NVFP4:
         assert np.array_equal(out[-16:], chunk[-16:])
     assert out.size == qmm.fmt_packed_bytes(fmt, N, K)
+
+
+def test_release_without_workspaces_needs_no_gpu(qmm):
+    """qmm_release with nothing allocated touches no device; nothing is held afterwards."""
+    assert qmm.load().qmm_release() == 0
+    assert qmm.workspace_bytes_held() == 0

@@ -1,7 +1,7 @@
 """The C ABI under CUDA-graph capture: a call made while its stream is being captured records its
 launches (with their programmatic dependencies) into the graph, and replaying the graph gives
 the eager call's bits.  The calls that keep a workspace are made once before capture (it is
-sized then; capture cannot allocate), qmm_run_noalloc needs no such call.
+sized then; capture cannot allocate).
 """
 import numpy as np
 import pytest
@@ -96,23 +96,3 @@ def test_ffn_chain_in_a_graph(qmm, oracle_lib, M):
     Y = torch.empty((M, K), dtype=torch.float32, device="cuda")
     ws = torch.empty(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
     capture_and_compare(qmm, lambda: qmm.run_ffn(Wgu, Wdn, F, K, X, Y, ws, M=M), [Y])
-
-
-def test_noalloc_in_a_graph_without_a_warm_up_call(qmm, oracle_lib):
-    """qmm_run_noalloc can be the first call on the capturing stream (it allocates nothing)."""
-    N, K, M = 1001, 2304, 9
-    Wq = oracle_lib.pack(inputs.weights_f32(N, K, 61))
-    W, X = dev_bytes(Wq), dev_x(inputs.activations_bf16_bits(M, K, 62))
-    Y = torch.full((M, N), np.nan, dtype=torch.float32, device="cuda")
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            qmm.run_noalloc(W, N, K, X, Y, M=M, stream=s)
-    torch.cuda.current_stream().wait_stream(s)
-    g.replay()
-    torch.cuda.synchronize()
-    assert qmm.device_status() == 0
-    Yref, S = oracle_lib.matmul(Wq, N, K, inputs.activations_bf16_bits(M, K, 62))
-    assert np.all(np.abs(Y.cpu().numpy().astype(np.float64) - Yref) <= 1e-4 * S)

@@ -246,6 +246,25 @@ def test_misaligned_pointers_rejected(qmm):
     torch.cuda.synchronize()
 
 
+def test_release_frees_the_workspaces_and_calls_allocate_again(qmm, oracle_lib):
+    """After qmm_release the tensor-core workspaces are gone (0 bytes held, the device memory
+    back); the next call allocates again and computes the same bits."""
+    N, K, M = 1001, 5120, 8
+    Wq = _cached_pack(oracle_lib, N, K, 19)
+    X = inputs.activations_bf16_bits(M, K, 20)
+    Wd, Xd = dev_bytes(Wq), dev_x(X)
+    Y1 = gpu_run(qmm, Wd, N, K, Xd, M, variant=TC)
+    assert qmm.workspace_bytes_held() > 0
+    free_before = torch.cuda.mem_get_info()[0]
+    held = qmm.workspace_bytes_held()
+    qmm.release()
+    assert qmm.workspace_bytes_held() == 0
+    assert torch.cuda.mem_get_info()[0] >= free_before + held - (2 << 20)
+    Y2 = gpu_run(qmm, Wd, N, K, Xd, M, variant=TC)
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    assert qmm.workspace_bytes_held() > 0
+
+
 # ------------------------------------------------------------------ full sizes --------------
 
 FULL = [

@@ -64,9 +64,39 @@ def test_noalloc_matches_qmm_run_on_two_calls_in_a_row(qmm, oracle_lib):
         assert np.all(np.abs(y_new - Yref) <= TOL * S)
 
 
+def _limit_k(mpad):
+    """Largest K the fixed buffer takes: (K/256) prepared blocks of Mpad * 580 + 16 bytes."""
+    return (4 << 20) // (mpad * 580 + 16) * 256
+
+
 def test_noalloc_rejects_problems_larger_than_its_buffer(qmm):
     lib = qmm.load()
     p = ctypes.c_void_p(256)   # never dereferenced: the size check comes before any GPU work
-    assert lib.qmm_run_noalloc(p, 8, 65536, p, p, 32, None) == 10       # 256 super-blocks at Mpad 32
-    assert lib.qmm_run_noalloc(p, 8, 123136, p, p, 16, None) == 10      # 481 super-blocks at Mpad 16
+    assert lib.qmm_run_noalloc(p, 8, _limit_k(32) + 256, p, p, 32, None) == 10   # one super-block too many, Mpad 32
+    assert lib.qmm_run_noalloc(p, 8, _limit_k(16) + 256, p, p, 16, None) == 10   # and at Mpad 16
     assert lib.qmm_strerror(10).startswith(b"qmm_run_noalloc")
+
+
+@pytest.mark.parametrize("M", [32, 16])
+def test_noalloc_accepts_the_largest_problem_its_buffer_holds(qmm, oracle_lib, M):
+    """At exactly the limit the call runs, and agrees with qmm_run within the tolerance."""
+    lib = qmm.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    N, K = 40, _limit_k(32 if M > 16 else 16)
+    Wq = oracle_lib.pack(inputs.weights_f32(N, K, 71))
+    X = inputs.activations_bf16_bits(M, K, 72)
+    Wd, Xd = _dev(Wq), _dev_x(X)
+    Y_new = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    Y_old = torch.full((M, N), -7.0, dtype=torch.float32, device="cuda")
+    st = lib.qmm_run_noalloc(ctypes.c_void_p(Wd.data_ptr()), N, K, ctypes.c_void_p(Xd.data_ptr()),
+                             ctypes.c_void_p(Y_new.data_ptr()), M, ctypes.c_void_p(stream))
+    assert st == 0, qmm.QmmError(st, "qmm_run_noalloc")
+    st = lib.qmm_run(ctypes.c_void_p(Wd.data_ptr()), N, K, ctypes.c_void_p(Xd.data_ptr()),
+                     ctypes.c_void_p(Y_old.data_ptr()), M, ctypes.c_void_p(stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert qmm.device_status() == 0
+    Yref, S = oracle_lib.matmul(Wq, N, K, X)
+    y_new = Y_new.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(y_new - Y_old.cpu().numpy().astype(np.float64)) <= TOL * S)
+    assert np.all(np.abs(y_new - Yref) <= TOL * S)
