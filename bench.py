@@ -232,15 +232,230 @@ def time_steps(fn, steps: int, warmup: int, stream, sync_ranks):
     return e0.elapsed_time(e1) / steps
 
 
-def cpu_baseline(info, M: int, budget_s: float = 12.0):
+def time_trials(fn, steps: int, warmup: int, stream, sync_ranks, trials: int = 5):
+    """`trials` timed regions of exactly `steps` steps each (the warm-up before the first):
+    the per-step times of the trials."""
+    out = [time_steps(fn, steps, warmup, stream, sync_ranks)]
+    for _ in range(trials - 1):
+        out.append(time_steps(fn, steps, 0, stream, sync_ranks))
+    return out
+
+
+class RooflineGuard:
+    """A result that implies reading HBM faster than the memory system can is a bug ("sixi-asi
+    0.9", section "The patch": a pass faster than the bandwidth floor was a bug, not a win).  The
+    ceiling is the read-only probe of this run (qmm_stream_read), 3 % slack; before it is measured,
+    the measured copy bandwidth plus 15 % (a read-only stream can beat a copy), else the
+    8 TB/s spec."""
+
+    def __init__(self):
+        self.read_gbps = None
+
+    def ceiling(self):
+        if self.read_gbps:
+            return 1.03 * self.read_gbps
+        mp = measured_peaks()
+        if mp and mp.get("hbm_gbs"):
+            return 1.15 * float(mp["hbm_gbs"])
+        return SPEC_HBM_GBS
+
+    def check(self, gbps: float, where: str):
+        if gbps > self.ceiling():
+            raise SystemExit(f"roofline guard: {where}: {gbps:.0f} GB/s exceeds the {self.ceiling():.0f} GB/s "
+                             f"ceiling; a benchmark that beats the roofline is a bug report")
+        return gbps
+
+
+GUARD = RooflineGuard()
+
+
+def peak_probes(device: str):
+    """HBM peak probes on this GPU (FlashRT issue #153: the device-to-device bandwidth check and the
+    sustained-read microtest): the read-only streaming kernel qmm_stream_read over a 4 GiB buffer
+    (burst: one pass, median of 5; sustained: back-to-back passes for about 100 ms) and a 1 GiB
+    device-to-device copy (read + write bytes, median of 5)."""
+    import torch
+    from bit_quantized_skinny_gb300 import qmm
+
+    stream = torch.cuda.current_stream()
+    nbytes = 4 << 30
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device=device)
+    sink = torch.empty(qmm.stream_read_sink_words(), dtype=torch.int32, device=device)
+    rd = lambda: qmm.stream_read(buf, sink)
+    burst = statistics.median(time_trials(rd, 1, 3, stream, lambda: None, trials=5))
+    passes = max(3, int(100.0 / burst))
+    sustained = time_steps(rd, passes, 1, stream, lambda: None)
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    cp = lambda: dst.copy_(src)
+    copy_ms = statistics.median(time_trials(cp, 1, 3, stream, lambda: None, trials=5))
+    del buf, sink, src, dst
+    torch.cuda.empty_cache()
+    out = {"read_burst_gbps": round(weight_gbps(nbytes, burst), 1),
+           "read_sustained_gbps": round(weight_gbps(nbytes, sustained), 1),
+           "read_sustained_ms": round(passes * sustained, 1),
+           "d2d_copy_gbps_read_plus_write": round(weight_gbps(2 << 30, copy_ms), 1),
+           "d2d_copy_payload_gbps": round(weight_gbps(1 << 30, copy_ms), 1),
+           "how": "qmm_stream_read (this library's read-only streaming kernel) over 4 GiB; torch copy_ of 1 GiB"}
+    GUARD.read_gbps = max(out["read_burst_gbps"], out["read_sustained_gbps"])
+    return out
+
+
+def graph_launch_us(fns, stream, trials: int = 5, min_launches: int = 20):
+    """Device time per launch under CUDA-graph replay: the launches (one per weight copy, the list
+    repeated to at least min_launches) captured once into a graph on a side stream (after one
+    eager pass there, which sizes the tensor-core workspace), replayed once, then CUDA events on
+    the launching stream around `reps` replays per trial; the median over the trials, in us."""
+    import torch
+    seq = list(fns)
+    while len(seq) < min_launches:
+        seq += list(fns)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for f in seq:
+                f()
+    stream.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 3
+    times = []
+    for _ in range(trials):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / (reps * len(seq)))
+    del graph
+    return statistics.median(times) * 1e3
+
+
+SWITCH_MS = [1, 2, 3, 4, 7, 8, 9, 12, 16]
+
+
+def config_timings(device: str):
+    """The configurations other than the pass, device-timed under CUDA-graph replay, weights
+    cycled over copies totalling at least 4x L2 (each launch reads HBM):
+      ffn_decode_m1  single FFN layer at M = 1: the gate/up product 34816 x 5120, the down product
+                     5120 x 17408, and the block (qmm_run_ffn, qmm_run_ffn_fused)
+      lm_head        N = 248320, K = 5120 at M = 1 and M = 7
+      switch_point   gate_up, down, q (5120 x 5120), k (1024 x 5120) at M in SWITCH_MS, both kernel
+                     families, and the family the dispatcher picks
+    Each figure: us per launch, GB/s of packed weights, fraction of the read probe."""
+    import torch
+    from bit_quantized_skinny_gb300 import inputs, qmm, workloads
+
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    peak = GUARD.read_gbps or hbm_peak()[0]
+
+    def weights(N, K, seed, min_bytes=4 * l2):
+        w = workloads.packed_weights_fmt(qmm.FMT_Q4K, N, K, seed)
+        return [w] + [w.clone() for _ in range(max(1, -(-min_bytes // w.numel())) - 1)]
+
+    def fig(us, wbytes, where):
+        g = GUARD.check(weight_gbps(wbytes, us * 1e-3), where)
+        return {"us": round(us, 2), "gbps": round(g, 1), "frac_of_read_peak": round(g / peak, 4)}
+
+    out = {}
+    # FFN layer decode, M = 1
+    F, K = 17408, 5120
+    gu = weights(2 * F, K, inputs.seed_for(2, 0))
+    dn = weights(K, F, inputs.seed_for(2, 1))
+    M = 1
+    X, _ = workloads.activations(M, K, inputs.seed_for(2, 51), device=device)
+    Xd, _ = workloads.activations(M, F, inputs.seed_for(2, 52), device=device)
+    Yg = torch.empty((M, 2 * F), device=device)
+    Yd = torch.empty((M, K), device=device)
+    ffn = {"gate_up": fig(graph_launch_us([lambda w=w: qmm.run(w, 2 * F, K, X, Yg, M=M) for w in gu], stream),
+                          gu[0].numel(), "ffn gate_up M=1"),
+           "down": fig(graph_launch_us([lambda w=w: qmm.run(w, K, F, Xd, Yd, M=M) for w in dn], stream),
+                       dn[0].numel(), "ffn down M=1")}
+    ffn["gate_up"]["variant"] = qmm.VARIANT_NAMES[qmm.select_variant(M, 2 * F, K)]
+    ffn["down"]["variant"] = qmm.VARIANT_NAMES[qmm.select_variant(M, K, F)]
+    ws = torch.empty(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device=device)
+    wsf = torch.empty(qmm.ffn_fused_workspace_bytes(M, F), dtype=torch.uint8, device=device)
+    pairs = list(zip(gu, dn))[:max(4, -(-4 * l2 // (gu[0].numel() + dn[0].numel())))]
+    blk = gu[0].numel() + dn[0].numel()
+    ffn["block"] = fig(graph_launch_us([lambda g=g, d=d: qmm.run_ffn(g, d, F, K, X, Yd, ws, M=M) for g, d in pairs],
+                                       stream), blk, "ffn block M=1")
+    ffn["block_fused"] = fig(graph_launch_us([lambda g=g, d=d: qmm.run_ffn_fused(g, d, F, K, X, Yd, wsf, M=M)
+                                              for g, d in pairs], stream), blk, "ffn fused block M=1")
+    out["ffn_decode_m1"] = ffn
+    # the switch-point table (gate_up and down reuse the copies above)
+    qw = weights(5120, 5120, inputs.seed_for(3, 2))
+    kw = weights(1024, 5120, inputs.seed_for(3, 3))
+    table = {}
+    for name, ws_, N, Kk in (("gate_up", gu, 2 * F, K), ("down", dn, K, F), ("q", qw, 5120, 5120), ("k", kw, 1024, 5120)):
+        rows = {}
+        for m in SWITCH_MS:
+            Xm, _ = workloads.activations(m, Kk, inputs.seed_for(3, 60 + m), device=device)
+            Ym = torch.empty((m, N), device=device)
+            row = {"picks": qmm.VARIANT_NAMES[qmm.select_variant(m, N, Kk)]}
+            for v in (qmm.VARIANT_FMA, qmm.VARIANT_TC):
+                us = graph_launch_us([lambda w=w, v=v: qmm.run(w, N, Kk, Xm, Ym, M=m, variant=v) for w in ws_], stream)
+                f = fig(us, ws_[0].numel(), f"switch {name} M={m} {qmm.VARIANT_NAMES[v]}")
+                row[qmm.VARIANT_NAMES[v]] = {"us": f["us"], "gbps": f["gbps"]}
+            rows[str(m)] = row
+        table[name] = {"N": N, "K": Kk, "weight_bytes": ws_[0].numel(), "copies": len(ws_), "per_M": rows}
+    out["switch_point"] = table
+    del gu, dn, qw, kw, pairs
+    torch.cuda.empty_cache()
+    # lm_head
+    N, K = 248320, 5120
+    lw = weights(N, K, inputs.seed_for(5, 0))
+    lm = {}
+    for m in (1, 7):
+        Xm, _ = workloads.activations(m, K, inputs.seed_for(5, 70 + m), device=device)
+        Ym = torch.empty((m, N), device=device)
+        f = fig(graph_launch_us([lambda w=w: qmm.run(w, N, K, Xm, Ym, M=m) for w in lw], stream), lw[0].numel(),
+                f"lm_head M={m}")
+        f["variant"] = qmm.VARIANT_NAMES[qmm.select_variant(m, N, K)]
+        lm[f"M{m}"] = f
+    out["lm_head"] = lm
+    del lw
+    torch.cuda.empty_cache()
+    if qmm.device_status() != 0:
+        raise RuntimeError("kernel reported a device-side error")
+    out["how"] = ("CUDA-graph replay of >= 20 launches (one per weight copy, copies >= 4x L2), CUDA events "
+                  "on the launching stream, median of 5 trials; us per launch")
+    return out
+
+
+def oracle_packed_layers():
+    """Host copies of the six distinct layer matrices packed by the oracle's packer (the bytes
+    qmm_pack writes, by the packers' byte-equality test), for the host-side baselines."""
+    import numpy as np
+    import oracle
+    from bit_quantized_skinny_gb300 import inputs, workloads
+
+    hosts = []
+    for idx, (name, N, K) in enumerate(workloads.LAYER_SHAPES):
+        buf = np.empty(N * (K // 256) * 144, dtype=np.uint8)
+        rowbytes = (K // 256) * 144
+        for row0, w in inputs.weight_chunks(N, K, inputs.seed_for(4, idx)):
+            buf[row0 * rowbytes:(row0 + w.shape[0]) * rowbytes] = oracle.pack(w)
+        hosts.append(buf)
+    return hosts
+
+
+def cpu_baseline(M: int, budget_s: float = 12.0):
     """The oracle as it stands, timed on the host cores over a bounded sample of the pass:
-    evenly spaced rows of each of the six distinct matrices, M activation rows, repeated until
-    at least ~10 s of CPU work has run."""
+    evenly spaced rows of each of the six distinct matrices (packed by the oracle's packer), M
+    activation rows, repeated until at least ~10 s of CPU work has run."""
     import numpy as np
     import oracle
     from bit_quantized_skinny_gb300 import inputs, workloads
 
     oracle.build()
+    info = {"hosts": oracle_packed_layers()}
     cores = oracle.max_threads()
     shapes = workloads.LAYER_SHAPES
     xs = {K: inputs.activations_bf16_bits(M, K, 9) for K in {K for _, _, K in shapes}}
@@ -295,6 +510,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
     qmm.load()
     stream = torch.cuda.current_stream()
     M = args.M
+    probes = peak_probes(device) if rank == 0 else None
     entries, info = layer_pass_setup(M, device)
 
     variant = qmm.select_variant_batched(entries, M)
@@ -308,16 +524,15 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
     if qmm.device_status() != 0:
         raise RuntimeError("kernel reported a device-side error")
 
+    # five timed regions of exactly `steps` steps each; the step time is their median
     with ClockSampler(local_rank) as clocks:
-        ms = time_steps(step, args.steps, args.warmup, stream, sync)
+        trials = time_trials(step, args.steps, args.warmup, stream, sync, trials=5)
+    ms = statistics.median(trials)
     if qmm.device_status() != 0:
         raise RuntimeError("kernel reported a device-side error")
     wb = info["weight_bytes"]
     ms_max, wb_all = aggregate_ranks(ms, wb, dist_ok, device)
-    per_gpu_gbps = weight_gbps(wb, ms)
-    if per_gpu_gbps > SPEC_HBM_GBS:
-        raise SystemExit(f"roofline guard: {per_gpu_gbps:.0f} GB/s exceeds the {SPEC_HBM_GBS:.0f} GB/s HBM "
-                         f"peak; a benchmark that beats the roofline is a bug report")
+    per_gpu_gbps = GUARD.check(weight_gbps(wb, ms), "64-layer pass")
     value = weight_gbps(wb_all, ms_max)
 
     # ---- end to end through the C ABI with host buffers: H2D of X, the pass, D2H of Y
@@ -348,8 +563,9 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
                 pin_y[lo:hi].copy_(info["y_arena"][lo:hi], non_blocking=True)
         stream.wait_stream(copy_stream)   # the step ends when every output is on the host
 
-    ms_e2e = time_steps(e2e_step, args.steps, args.warmup, stream, sync)
+    ms_e2e = statistics.median(time_trials(e2e_step, args.steps, args.warmup, stream, sync, trials=3))
     ms_e2e, _ = aggregate_ranks(ms_e2e, wb, dist_ok, device)
+    GUARD.check(weight_gbps(wb, ms_e2e), "end-to-end pass")
 
     # ---- per-M sweep on the same pass (context for the switch point; same timing rules)
     per_m = {}
@@ -357,8 +573,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
         for m in args.sweep:
             ents_m, info_m = (entries, info) if m == M else layer_pass_setup(m, device)
             f = (lambda e=ents_m, mm=m: qmm.run_batched(e, mm))
-            msm = time_steps(f, max(3, args.steps // 2), 3, stream, lambda: None)
-            g = weight_gbps(info_m["weight_bytes"], msm)
+            msm = statistics.median(time_trials(f, max(3, args.steps // 2), 3, stream, lambda: None, trials=3))
+            g = GUARD.check(weight_gbps(info_m["weight_bytes"], msm), f"pass M={m}")
             per_m[str(m)] = {"gbps": round(g, 1), "ms_per_15.8GB_pass": round(ms_per_pass(g), 4),
                              "frac_of_measured_hbm": round(g / hbm_peak()[0], 4),
                              "frac_of_spec_8TBps": round(g / SPEC_HBM_GBS, 4),
@@ -369,6 +585,15 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
 
     peak, peak_kind = hbm_peak()
     achieved = info["algo_bytes"] / (ms * 1e-3) / 1e9
+    algo_bytes = info["algo_bytes"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(M)
+    # the other configurations, after the pass's buffers are released
+    del entries, parts, pin_x, pin_y
+    info_items = len(info["items"])
+    info.clear()
+    torch.cuda.empty_cache()
+    configs = config_timings(device) if (rank == 0 and not args.no_configs) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
@@ -378,7 +603,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
             "workload": "64-layer Q4K weight pass: per layer q 5120x5120, k 1024x5120, v 1024x5120, "
                         "o 5120x5120, gate_up 34816x5120, down 5120x17408 (384 matrices), "
                         f"M={M} bf16 rows, one qmm_run_batched launch per pass",
-            "M": M, "matrices": len(info["items"]), "weight_bytes_per_step": wb,
+            "M": M, "matrices": info_items, "weight_bytes_per_step": wb,
             "ms_per_15.8GB_pass": round(ms_per_pass(per_gpu_gbps), 4),
             "frac_of_spec_8TBps": round(per_gpu_gbps / SPEC_HBM_GBS, 4),
             "l2": "inputs larger than L2: 11.9 GB of weights per step vs 129 MB L2, no flush",
@@ -391,7 +616,8 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
                      "timed": "whole step on the launching stream (the product launches plus the "
                               "activation-prep launch, 0.15% of the step by ncu)" if variant == qmm.VARIANT_TC
                               else "whole step on the launching stream (one kernel)",
-                     "algorithmic_bytes_per_step": info["algo_bytes"],
+                     "algorithmic_bytes_per_step": algo_bytes,
+                     "frac_of_read_probe": round(achieved / GUARD.read_gbps, 4) if GUARD.read_gbps else None,
                      "unit_of_measure": "one step = one qmm_run_batched call over the 384 matrices: one "
                                         "activation-prep launch and ceil(384/160) = 3 product launches; "
                                         "achieved and traffic are per step"},
@@ -404,12 +630,16 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
                         "back on a second stream while the next call computes; the weights are "
                         "resident model parameters"},
         "gpu_launches": args.steps * launches_per_step,
+        "timing": {"trials_ms_per_step": [round(t, 5) for t in trials], "statistic": "median of 5 timed regions "
+                   "of exactly `steps` steps each (warm-up before the first)"},
+        "peak_probes": probes,
+        "configs": configs,
         "variant": qmm.VARIANT_NAMES.get(variant, str(variant)),
         "clocks": clocks.summary(),
         "per_M": per_m,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(info, M)
+        line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -657,17 +887,13 @@ def run_reference(args, rank: int):
         return
     import numpy as np
     import oracle
-    from bit_quantized_skinny_gb300 import inputs, qmm, build_lib, workloads
+    from bit_quantized_skinny_gb300 import inputs, workloads
 
-    build_lib.build()
     oracle.build()
     cores = oracle.max_threads()
     M = args.M
     shapes = workloads.LAYER_SHAPES
-    hosts = []
-    for idx, (name, N, K) in enumerate(shapes):
-        _, Wh = workloads.packed_weights(N, K, inputs.seed_for(4, idx), device=None, keep_host=True)
-        hosts.append(Wh)
+    hosts = oracle_packed_layers()   # the oracle's packer: this arm loads nothing of the library
     xs = {K: inputs.activations_bf16_bits(M, K, 9) for K in {K for _, _, K in shapes}}
     # one step: a fixed, evenly spaced sample of rows from each distinct matrix (~1.5 s of work)
     N5, K5 = shapes[5][1], shapes[5][2]
@@ -716,6 +942,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 4, 8, 16, 32])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' graph-replay timings")
     ap.add_argument("--single", choices=list(SINGLE_SHAPES) + ["all"], default=None)
     ap.add_argument("--Ms", type=lambda s: [int(v) for v in s.split(",") if v], default=[1, 2, 3, 4, 7, 8, 9, 12, 16])
     ap.add_argument("--variant", choices=["fma", "tc", "auto", "both"], default="both")

@@ -158,24 +158,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 // that compute); after `limit` polls the wait gives up and returns false.
 constexpr uint32_t kSuspendNs = 20000;
 
-// One poll without a suspend hint: the cheap test for a phase that has most likely completed.
+// One non-blocking test: the cheap check for a phase that has most likely completed.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(done) : "r"(bar), "r"(parity) : "memory");
   return done != 0;
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit,
+                                          uint32_t suspend_ns = kSuspendNs) {
   for (uint32_t it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n"
         " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
+        : "=r"(done) : "r"(bar), "r"(parity), "r"(suspend_ns) : "memory");
     if (done) return true;
   }
   return false;

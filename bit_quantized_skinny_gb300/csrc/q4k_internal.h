@@ -63,6 +63,15 @@ cudaError_t launch_dequant_fmt(int fmt, const void* W, int64_t N, int64_t K, flo
 cudaError_t release_workspaces();
 size_t workspace_bytes_held();
 
+// Failure-detection hook: bound the tensor-core kernel's pipeline waits to `polls` polls of at
+// most suspend_ns each (0, 0: the kernel's own bound) in launches made from now on.
+void set_wait_limit(uint32_t polls, uint32_t suspend_ns);
+
+// The read-only streaming probe: read `bytes` (a multiple of 16) at buf once; sink holds
+// stream_read_grid() words.
+cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream);
+int stream_read_grid();
+
 // Device status words of the kernel files: read and clear (synchronous; 0 = no error).
 cudaError_t read_and_clear_fma_status(unsigned* out);
 cudaError_t read_and_clear_tc_status(unsigned* out);

@@ -65,6 +65,7 @@
 // in fp16 unless it is below 2^-32 of that largest value (such values are rounded to fp16's
 // 2^-24 step of the scaled range), and writes B, B_ext and 2^s into a per-stream workspace.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <map>
@@ -269,6 +270,8 @@ struct TcParams {
   int M;
   int tasks_total;
   int gated;   // one product whose row pairs (2f, 2f+1) are (gate f, up f): Y holds bf16 H[M x N/2]
+  uint32_t wait_polls;   // bound of the pipeline waits: polls (0: kWaitLimit) of at most
+  uint32_t wait_ns;      // wait_ns each (0: kSuspendNs); set only by the failure-detection hook
   const void* aux[NAUX];
 };
 __host__ __device__ constexpr int naux(int f, int maxe) { return f == kFmtQ4K ? 1 : maxe; }
@@ -607,7 +610,7 @@ __device__ __forceinline__ float fold_ext_factor(float Dm) {
   return eb ? -__uint_as_float(eb - (16u << 23)) : 0.f;
 }
 
-// The per-sub-block constants of the folded decode, computed ahead of it (12-bit group
+// The per-sub-block constants of the folded decode (12-bit group
 // gr = sc_j | m_j << 6): cm = the fp16 pair (-k_j 2^-14, sc_j 2^10) -- the decode's addend and
 // its first multiplier -- and ext = the A_ext pair (hi, lo) of rho_j T.
 __device__ __forceinline__ void fold_k(uint32_t gr, const Fold& fd, const DecodeConsts& C, uint32_t& cm,
@@ -625,18 +628,11 @@ __device__ __forceinline__ void fold_k(uint32_t gr, const Fold& fd, const Decode
 
 // The 12-bit (sc_j, m_j) group of sub-block j from a super-block's first 16 bytes.
 __device__ __forceinline__ uint32_t kq_group(const uint4& hd, int j) {
-  const uint64_t G = (uint64_t)hd.z << 32 | hd.y;   // groups 0..3 at bits 0..47
-  const uint64_t H = (uint64_t)hd.w << 32 | hd.z;   // groups 4..7 at bits 16..63
-  return (uint32_t)(j < 4 ? (G >> (12 * j)) : (H >> (16 + 12 * (j - 4)))) & 0xFFFu;
-}
-
-// All fold constants of a row's super-block (computed ahead of its decode).
-__device__ __forceinline__ void fold_consts(const uint4& hd, const DecodeConsts& C, uint32_t (&add)[8],
-                                            uint32_t (&ext)[8]) {
-  const float2 dd = __half22float2(bits2h(hd.x));
-  const Fold fd = make_fold(dd.x, dd.y);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) fold_k(kq_group(hd, j), fd, C, add[j], ext[j]);
+  // bit 12j of the 96-bit field held in hd.y (bits 0..31), hd.z (32..63), hd.w (64..95)
+  const int b = 12 * j;
+  const uint32_t lo = b < 32 ? hd.y : (b < 64 ? hd.z : hd.w);
+  const uint32_t hi = b < 32 ? hd.z : hd.w;
+  return __funnelshift_r(lo, hi, b & 31) & 0xFFFu;
 }
 
 template <int FMT>
@@ -900,7 +896,8 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
   auto wait = [&](uint32_t b, uint32_t parity) -> bool {
     if (mbar_try(b, parity)) return true;
     if (*abort_flag) return false;
-    if (mbar_wait(b, parity, kWaitLimit)) return true;
+    if (mbar_wait(b, parity, P.wait_polls ? P.wait_polls : kWaitLimit, P.wait_ns ? P.wait_ns : kSuspendNs))
+      return true;
     atomicOr(&g_status, kErrWaitTimeout);
     *abort_flag = 1;
     return false;
@@ -1003,9 +1000,9 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
     // Software-pipelined over the group's super-blocks: once super-block i is handed to the
-    // MMA warp, the group waits for the stage of super-block i+1 and computes what does not
-    // need tensor memory (its per-token scales, hard tokens, the k-quant fold constants) while
-    // the MMAs of i run; then it reads i's accumulator, and decodes i+1.
+    // MMA warp, the group waits for the stage of super-block i+1 and takes what does not need
+    // tensor memory (its header, per-token scales, hard tokens) while the MMAs of i run; then it
+    // reads i's accumulator, and decodes i+1.
     const int grp = warp >> 2;       // dequant group: the CTA's local tasks j % NG == grp
     const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
     const int r = 32 * q + lane;     // row inside the tile
@@ -1040,8 +1037,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       uint32_t ws;        // its stage
       uint4 hd;           // this row's first 16 bytes
       uint32_t hmask;     // its hard tokens
-      uint32_t add[8];    // k-quants: the pairs (-k_j 2^-14, sc_j 2^10) of the decode
-      uint32_t ext[8];    //           the A_ext pairs of rho_j T
+      uint32_t ext[8];    // k-quants: the A_ext pairs of rho_j T (filled by the decode)
     };
     // Wait for the i-th super-block of the group (task position c) and prepare it.
     auto ahead = [&](int i, const GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG>& c, Ahead& A) -> bool {
@@ -1076,7 +1072,6 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
         const uint16_t* X = reinterpret_cast<const uint16_t*>((uint64_t)tr.z | ((uint64_t)tr.w << 32));
         hard_dot<FMT, MT>(rb, X, (int)tr.y, c.sb, A.hd, a0, a1, A.hmask, hard_sum[i & 1]);
       }
-      if constexpr (has_min(FMT)) fold_consts(A.hd, dc, A.add, A.ext);
       return true;
     };
 
@@ -1213,10 +1208,15 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       const uint32_t ws = A.ws;
       const uint4 hd = A.hd;
       const uint32_t rb = sW + ws * kSB + r * kBlk;   // this row's bytes of the super-block
+      Fold fd{0.f, 0.f, 0.f};                          // k-quants: the row's fold factors
+      if constexpr (has_min(FMT)) {
+        const float2 dd = __half22float2(bits2h(hd.x));
+        fd = make_fold(dd.x, dd.y);
+      }
       // ---- decode: the row's super-block one K half at a time from the stage (this warp's part
       // of the stage is released once all is read), each half handed to the MMA warp
       // (the A slot is free: this group read its previous accumulator above)
-#pragma unroll 1
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         HalfIn<FMT> in;
         load_half<FMT>(in, rb, h);
@@ -1224,9 +1224,11 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         }
-        uint32_t a4[4];   // the half's sub-blocks' precomputed pairs
+        uint32_t a4[4];   // the half's sub-blocks' fold constants
+        if constexpr (has_min(FMT)) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) a4[jj] = h ? A.add[4 + jj] : A.add[jj];
+          for (int jj = 0; jj < 4; ++jj) fold_k(kq_group(hd, 4 * h + jj), fd, dc, a4[jj], A.ext[4 * h + jj]);
+        }
         decode_half<FMT>(in, hd, h, aslot + 64u * h, dc, a4);
         if (h == 0) {   // the first K half goes to the MMA warp now
           tc::wait_st();
@@ -1257,10 +1259,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
           if (!wait_w(bar(kBarH0Done + grp), (uint32_t)i & 1u)) break;
           tc::fence_after_sync();
         }
-        uint32_t cols[16];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) cols[2 * jj] = cols[2 * jj + 1] = A.ext[jj];
-        tc::st_x16(aext, cols);
+        tc::st_x16_pairs(aext, A.ext);   // column 2j and 2j+1: ext[j]
       }
       // ---- hand the second K half (and A_ext) to the MMA warp
       tc::wait_st();
@@ -1359,6 +1358,9 @@ class Workspace {
     return p;
   }
 };
+
+// The failure-detection hook's wait bound (0, 0: the kernels' own bound).
+std::atomic<uint32_t> g_wait_polls{0}, g_wait_ns{0};
 
 int num_sms() {
   int dev = 0, sms = 0;
@@ -1496,6 +1498,8 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   }
   par.tasks_total = tasks;
   par.gated = (count == 1 && jobs[0].gated) ? 1 : 0;
+  par.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
+  par.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   for (int k = 0; k < naux(FMT, MAXE) && k < count; ++k) par.aux[k] = jobs[k].aux;
   // Programmatic dependent launch: the kernel may start while the preparation kernel before it
   // in the stream still runs; it waits (griddepcontrol.wait) before it reads the prepared data.
@@ -1668,6 +1672,11 @@ cudaError_t launch_tc_noalloc_t(const Job& job, int M, cudaStream_t stream, uint
 }  // namespace
 
 cudaError_t release_workspaces() { return Workspace::release(); }
+
+void set_wait_limit(uint32_t polls, uint32_t suspend_ns) {
+  g_wait_polls.store(polls, std::memory_order_relaxed);
+  g_wait_ns.store(suspend_ns, std::memory_order_relaxed);
+}
 size_t workspace_bytes_held() { return Workspace::held_bytes(); }
 
 cudaError_t read_and_clear_tc_status(unsigned* out) {

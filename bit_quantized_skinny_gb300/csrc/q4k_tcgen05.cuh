@@ -112,6 +112,14 @@ __device__ __forceinline__ void st_x16(uint32_t taddr, const uint32_t (&v)[16]) 
       : "memory");
 }
 
+// Columns 2j and 2j+1 both take v[j] (j = 0..7).
+__device__ __forceinline__ void st_x16_pairs(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %2, %2, %3, %3, %4, %4, %5, %5, %6, %6, %7, %7, %8, %8};"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void ld_x8(uint32_t taddr, float (&v)[8]) {

@@ -377,6 +377,21 @@ int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M) 
   return select_variant_jobs(jobs, count, M);
 }
 
+size_t qmm_stream_read_sink_words(void) {
+  const int g = q4k::stream_read_grid();
+  return g > 0 ? (size_t)g : 0;
+}
+
+qmm_status qmm_stream_read(const void* buf_dev, size_t bytes, uint32_t* sink_dev, cudaStream_t stream) {
+  if (!buf_dev || !sink_dev) return QMM_ERR_NULL;
+  if (bytes == 0 || bytes % 16 != 0) return QMM_ERR_SHAPE;
+  if (!aligned(buf_dev, 16) || !aligned(sink_dev, 4)) return QMM_ERR_ALIGN;
+  const cudaError_t e = q4k::launch_stream_read(buf_dev, bytes, sink_dev, stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
+void qmm_set_wait_limit(uint32_t polls, uint32_t suspend_ns) { q4k::set_wait_limit(polls, suspend_ns); }
+
 qmm_status qmm_release(void) {
   const cudaError_t e = q4k::release_workspaces();
   return e == cudaSuccess ? QMM_OK : cuda_fail(e);

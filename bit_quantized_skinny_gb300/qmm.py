@@ -35,7 +35,8 @@ EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_de
            "qmm_last_cuda_error", "qmm_run_noalloc", "qmm_select_variant_batched",
            "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed",
            "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant", "qmm_fmt_run_batched",
-           "qmm_ffn_fused_workspace_bytes", "qmm_run_ffn_fused", "qmm_release", "qmm_workspace_bytes_held"]
+           "qmm_ffn_fused_workspace_bytes", "qmm_run_ffn_fused", "qmm_release", "qmm_workspace_bytes_held",
+           "qmm_stream_read", "qmm_stream_read_sink_words", "qmm_set_wait_limit"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -82,6 +83,12 @@ def load(path: str | None = None):
     lib.qmm_run_variant.restype = i32
     lib.qmm_run_noalloc.argtypes = [vp, i64, i64, vp, vp, i32, vp]
     lib.qmm_run_noalloc.restype = i32
+    lib.qmm_stream_read.argtypes = [vp, ctypes.c_size_t, vp, vp]
+    lib.qmm_stream_read.restype = i32
+    lib.qmm_stream_read_sink_words.argtypes = []
+    lib.qmm_stream_read_sink_words.restype = ctypes.c_size_t
+    lib.qmm_set_wait_limit.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+    lib.qmm_set_wait_limit.restype = None
     lib.qmm_release.argtypes = []
     lib.qmm_release.restype = i32
     lib.qmm_workspace_bytes_held.argtypes = []
@@ -306,6 +313,23 @@ def select_variant(M: int, N: int, K: int) -> int:
 
 def select_variant_batched(entries, M: int) -> int:
     return load().qmm_select_variant_batched(entries, len(entries), M)
+
+
+def stream_read(buf, sink, stream=None) -> None:
+    """qmm_stream_read: read every byte of the device tensor `buf` once (the read-bandwidth probe);
+    `sink` is a device uint32 tensor of at least qmm_stream_read_sink_words() words."""
+    st = load().qmm_stream_read(ctypes.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size(),
+                                ctypes.c_void_p(sink.data_ptr()), _stream_handle(stream))
+    _check(st, "qmm_stream_read")
+
+
+def stream_read_sink_words() -> int:
+    return int(load().qmm_stream_read_sink_words())
+
+
+def set_wait_limit(polls: int = 0, suspend_ns: int = 0) -> None:
+    """qmm_set_wait_limit: the tensor-core kernel's wait bound for later launches (0, 0: default)."""
+    load().qmm_set_wait_limit(polls, suspend_ns)
 
 
 def release() -> None:

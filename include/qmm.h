@@ -342,6 +342,17 @@ qmm_status qmm_fmt_run_batched(const qmm_fmt_entry* entries_host, int count, int
 qmm_status qmm_fmt_dequant(int fmt, const void* Wq_dev, int64_t N, int64_t K, float* out_dev,
                            cudaStream_t stream);
 
+/* Measurement probe: read bytes (a multiple of 16) of device memory at buf_dev exactly once,
+ * with 16-byte loads that bypass L1 and are marked evict-first in L2, and write one word per CTA
+ * (an XOR of what it read) to sink_dev, which holds qmm_stream_read_sink_words() words.  Timed
+ * over a buffer much larger than L2, it gives the HBM read bandwidth this GPU reaches from a
+ * kernel that only reads: the ceiling of the weight stream, against which the products' GB/s are
+ * compared (the pages check their kernels' GB/s against the memory system's own numbers: FlashRT
+ * issue #153, the device-to-device bandwidth check and the sustained-read microtest).
+ * Enqueued on `stream`; errors: QMM_ERR_NULL, QMM_ERR_SHAPE, QMM_ERR_ALIGN, QMM_ERR_CUDA. */
+size_t qmm_stream_read_sink_words(void);
+qmm_status qmm_stream_read(const void* buf_dev, size_t bytes, uint32_t* sink_dev, cudaStream_t stream);
+
 /* Free every tensor-core workspace the library holds (one per device and stream that ran the
  * tensor-core kernel; see "Device memory" above).  A synchronous call: cudaFree waits for the
  * work that may still use a workspace.  Later calls allocate again as needed.  Do not call it
@@ -352,6 +363,17 @@ qmm_status qmm_release(void);
 
 /* Bytes of device memory the tensor-core workspaces hold now (0 after qmm_release). */
 size_t qmm_workspace_bytes_held(void);
+
+/* Failure-detection hook.  Every wait inside the tensor-core kernel (for its weight copies, for
+ * its tensor-core work, between its warps) is bounded: by default 2^17 polls of at most 20 us.
+ * When a bound runs out the kernel sets bit 0 of the device status word (qmm_device_status),
+ * stops its other warps at their next wait, waits for the copies and tensor-core operations it
+ * has already issued (with the default bound), releases its tensor memory and returns; the
+ * outputs of that call are invalid and the context stays usable.  This call sets the bound of
+ * the launches made from now on to `polls` polls of at most `suspend_ns` nanoseconds each
+ * (0, 0 restores the default), for every thread and stream of the process: a test hook, which
+ * with a bound far below a memory access's latency makes the first wait run out. */
+void qmm_set_wait_limit(uint32_t polls, uint32_t suspend_ns);
 
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the

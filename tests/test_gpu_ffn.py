@@ -145,3 +145,53 @@ def test_fused_ffn_argument_errors(qmm):
     assert ei.value.status == 5
     assert qmm.ffn_fused_workspace_bytes(M, 100) == 0
     assert qmm.ffn_fused_workspace_bytes(M, F) == M * F * 2
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_full_size_ffn_chain_and_fused(qmm, oracle_lib, M):
+    """The configurations' FFN layer (gate/up 34816 x 5120, down 5120 x 17408) through qmm_run_ffn
+    and qmm_run_ffn_fused, on sampled rows: G within 1e-4 * sum|w x| of the oracle; H within one
+    bf16 step of the oracle's SwiGLU of the GPU's G (and of the fused block's own H: identical
+    when both gate/up products run on the tensor cores); Y within 1e-4 * sum|w x| of the oracle's
+    down product of the GPU's H.  The sampled rows' packed bytes equal the oracle packer's."""
+    from bit_quantized_skinny_gb300 import workloads
+    F, K = 17408, 5120
+    Wgu_d, Wgu = workloads.packed_weights(2 * F, K, inputs.seed_for(2, 0), device="cuda", keep_host=True)
+    Wdn_d, Wdn = workloads.packed_weights(K, F, inputs.seed_for(2, 1), device="cuda", keep_host=True)
+    rowbytes = (K // 256) * 144
+    W0 = inputs.weights_f32(64, K, inputs.seed_for(2, 0))          # the first rows of the same draw
+    assert np.array_equal(oracle_lib.pack(W0), Wgu[:64 * rowbytes])
+    Wint_d = _dev_bytes(_interleave_rows(Wgu, F, K))
+    rng = np.random.default_rng(M)
+    fs = np.unique(np.concatenate([[0, F - 1], rng.integers(0, F, 62)])).astype(np.int64)
+    ys = np.unique(np.concatenate([[0, K - 1], rng.integers(0, K, 62)])).astype(np.int64)
+    X = inputs.activations_bf16_bits(M, K, 950 + M)
+    Xd = _dev_x(X)
+    Y = torch.full((M, K), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(qmm.ffn_workspace_bytes(M, F), dtype=torch.uint8, device="cuda")
+    qmm.run_ffn(Wgu_d, Wdn_d, F, K, Xd, Y, ws, M=M)
+    Yf = torch.full((M, K), 7.0, dtype=torch.float32, device="cuda")
+    wsf = torch.full((qmm.ffn_fused_workspace_bytes(M, F),), 255, dtype=torch.uint8, device="cuda")
+    qmm.run_ffn_fused(Wint_d, Wdn_d, F, K, Xd, Yf, wsf, M=M)
+    torch.cuda.synchronize()
+    assert qmm.device_status() == 0
+    wsh = ws.cpu().numpy()
+    g_bytes = (M * 2 * F * 4 + 15) // 16 * 16
+    G = wsh[:M * 2 * F * 4].view(np.float32).reshape(M, 2 * F)
+    H = wsh[g_bytes:g_bytes + M * F * 2].view(np.uint16).reshape(M, F)
+    Hf = wsf.cpu().numpy()[:M * F * 2].view(np.uint16).reshape(M, F)
+    rows = np.concatenate([fs, F + fs])
+    Gref, SG = oracle_lib.matmul(Wgu, 2 * F, K, X, rows=rows)
+    _within(G[:, rows], Gref, SG, f"full gate/up M={M}")
+    href = oracle_lib.swiglu(G[:, rows].astype(np.float64), len(fs))
+    step = np.ldexp(1.0, np.frexp(np.abs(href))[1] - 8)
+    for what, HH in (("chained", H), ("fused", Hf)):
+        assert np.all(np.abs(_bf16_to_f64(HH[:, fs]) - href) <= step), f"{what} H off by more than one bf16 step"
+    assert np.mean(H[:, fs] == oracle_lib.bf16_round(href)) > 0.99
+    if qmm.select_variant(M, 2 * F, K) == qmm.VARIANT_TC:
+        assert np.array_equal(H, Hf), "fused and chained H differ"
+    for what, HH, YY in (("chained", H, Y), ("fused", Hf, Yf)):
+        Yref, SY = oracle_lib.matmul(Wdn, K, F, HH, rows=ys)
+        _within(YY.cpu().numpy()[:, ys], Yref, SY, f"full {what} down M={M}")
+    del Wgu_d, Wdn_d, Wint_d
+    torch.cuda.empty_cache()
