@@ -566,9 +566,9 @@ __device__ __forceinline__ void load_half(HalfIn<FMT>& in, uint32_t rb, int h) {
 
 // fp16 constants of the decodes, made once per thread (outside the super-block loop)
 struct DecodeConsts {
-  __half2 k1024, k0_1024, kn1024_1024, k1o16, kn1032, kn72;
+  __half2 k1024, kn1024, k64, k1o16, kn1032, kn72;
   __device__ __forceinline__ DecodeConsts()
-      : k1024(bits2h(0x64006400u)), k0_1024(bits2h(0x64000000u)), kn1024_1024(bits2h(0x6400E400u)),
+      : k1024(bits2h(0x64006400u)), kn1024(bits2h(0xE400E400u)), k64(__float2half2_rn(64.f)),
         k1o16(__float2half2_rn(0.0625f)), kn1032(__float2half2_rn(-1032.f)), kn72(__float2half2_rn(-72.f)) {}
 };
 
@@ -587,20 +587,23 @@ struct DecodeConsts {
 //     hi + lo is exact or within 2^-22 of rho_j T.
 // The min-term MMAs take A_ext columns (hi_j, lo_j) twice per sub-block against the B_ext rows
 // (X_hi, X_hi) and (X_lo, X_lo), so that the accumulator receives (hi + lo)(X_hi + X_lo).
+// The sub-block's fields enter the fp32 steps as 64 m_j (exact), so the factors are kept divided
+// by 64: (64 m) (R / 64) is m R exactly whenever R / 64 is a normal number, and below that
+// m R < 2^-114 rounds to k = 0 either way; (64 m) (Dm T / 64) = m Dm T exactly.
 struct Fold {
-  float R;     // Dm / D when >= 0, else 0 (+inf when D = 0: every k_j then clamps; D A_t vanishes)
-  float DT;    // D * T
-  float DmT;   // Dm * T, in [2^8, 2^9) (0 when Dm = 0, T = 1)
+  float R64;     // Dm / D / 64 when >= 0, else 0 (+inf when D = 0: every k_j then clamps; D A_t vanishes)
+  float DT;      // D * T
+  float DmT64;   // Dm * T / 64, Dm T in [2^8, 2^9) (0 when Dm = 0, T = 1)
 };
 __device__ __forceinline__ Fold make_fold(float D, float Dm) {
   Fold f;
   float rD;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rD) : "f"(D));
-  f.R = fmaxf(Dm * rD, 0.f);   // opposite signs (and D = 0 with Dm = 0): k = 0
+  f.R64 = fmaxf(Dm * rD, 0.f) * 0.015625f;   // opposite signs (and D = 0 with Dm = 0): k = 0
   const uint32_t eb = __float_as_uint(Dm) & 0x7F800000u;
   const float T = eb ? __uint_as_float((262u << 23) - eb) : 1.0f;
   f.DT = D * T;
-  f.DmT = Dm * T;
+  f.DmT64 = Dm * T * 0.015625f;
   return f;
 }
 // The factor of the min-term accumulator: y += sigma (D acc + fe(Dm) acc_ext), fe = -2^(e-16)
@@ -610,47 +613,85 @@ __device__ __forceinline__ float fold_ext_factor(float Dm) {
   return eb ? -__uint_as_float(eb - (16u << 23)) : 0.f;
 }
 
-// The per-sub-block constants of the folded decode (12-bit group
-// gr = sc_j | m_j << 6): cm = the fp16 pair (-k_j 2^-14, sc_j 2^10) -- the decode's addend and
-// its first multiplier -- and ext = the A_ext pair (hi, lo) of rho_j T.
-__device__ __forceinline__ void fold_k(uint32_t gr, const Fold& fd, const DecodeConsts& C, uint32_t& cm,
-                                       uint32_t& ext) {
-  const float mf = (float)(gr >> 6);
-  const float tk = fmaf(mf, fd.R, 12582912.0f);               // 1.5 2^23 + rint(m R) while m R < 2^22
-  const uint32_t k = min(__float_as_uint(tk) - 0x4B400000u, 2047u);
-  // (k 2^-24, 1024 + sc): k 2^-24 has the bit pattern of k; minus (0, 1024), times (-1024, 1024)
-  const uint32_t v = ((gr & 63u) | 0x6400u) * 0x10000u + k;
-  cm = h2bits(__hmul2(__hsub2(bits2h(v), C.k0_1024), C.kn1024_1024));
-  const float rt = fmaf(-fd.DT, (float)k, mf * fd.DmT);       // (Dm m - D k) T
-  const float rhi = __uint_as_float(__float_as_uint(rt) & 0xFFFFE000u);
-  ext = h2bits(__floats2half2_rn(rhi, rt - rhi));
-}
-
-// The 12-bit (sc_j, m_j) group of sub-block j from a super-block's first 16 bytes.
-__device__ __forceinline__ uint32_t kq_group(const uint4& hd, int j) {
-  // bit 12j of the 96-bit field held in hd.y (bits 0..31), hd.z (32..63), hd.w (64..95)
-  const int b = 12 * j;
+// 32 bits of the 96-bit scale field (hd.y bits 0..31, hd.z 32..63, hd.w 64..95) from bit b on
+// (the bits past 95 are not defined; callers mask them off).
+__device__ __forceinline__ uint32_t field_at(const uint4& hd, int b) {
   const uint32_t lo = b < 32 ? hd.y : (b < 64 ? hd.z : hd.w);
   const uint32_t hi = b < 32 ? hd.z : hd.w;
-  return __funnelshift_r(lo, hi, b & 31) & 0xFFFu;
+  return __funnelshift_r(lo, hi, b & 31);
+}
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));   // (a & mask) | bits
+  return d;
+}
+
+// The decode constants of one sub-block: the fp16 pairs (-k 2^-14, -k 2^-14) (the addend),
+// (sc 2^10, sc 2^10) and (sc 2^6, sc 2^6) (the multipliers of the two nibble positions), and
+// the A_ext pair (hi, lo) of rho T.
+struct SbConst {
+  __half2 add, mlo, mhi;
+  uint32_t ext;
+};
+
+// The constants of sub-blocks J and J + 1, whose 12-bit groups (sc | m << 6) start at bits 12J
+// and 12J + 12 of the field; the fp32 steps of the two run as pairs (f32x2).
+//   k = rint(m R) clamped to 2047: 1.5 2^23 + m R rounds to the integer in its low bits
+//   rho T = (Dm m - D k) T = fma(-D T, k, m Dm T), exact or one rounding
+template <int J>
+__device__ __forceinline__ void fold_pair(const uint4& hd, const Fold& fd, const DecodeConsts& C, SbConst& c0,
+                                          SbConst& c1) {
+  constexpr float kMagic = 12582912.0f;                              // 1.5 2^23
+  constexpr uint32_t kKK = 0u - 0x4B400000u * 0x10001u;              // bits(1.5 2^23 + k) * 0x10001 + kKK = k * 0x10001
+  const uint32_t g0 = field_at(hd, 12 * J), g1 = field_at(hd, 12 * J + 12);
+  // 64 m: 2^23 + 64 m has the bit pattern 0x4B000000 | (m << 6)
+  const float2 m64 = __fadd2_rn(make_float2(__uint_as_float(lop_and_or(g0, 0xFC0u, 0x4B000000u)),
+                                            __uint_as_float(lop_and_or(g1, 0xFC0u, 0x4B000000u))),
+                                make_float2(-8388608.0f, -8388608.0f));
+  const float2 tk = __ffma2_rn(m64, make_float2(fd.R64, fd.R64), make_float2(kMagic, kMagic));
+  const float2 tc = make_float2(fminf(tk.x, kMagic + 2047.0f), fminf(tk.y, kMagic + 2047.0f));   // NaN (0 x inf) too
+  const float2 kf = __fadd2_rn(tc, make_float2(-kMagic, -kMagic));
+  const float2 rt = __ffma2_rn(make_float2(-fd.DT, -fd.DT), kf,
+                               __fmul2_rn(m64, make_float2(fd.DmT64, fd.DmT64)));
+  const float2 rhi = make_float2(__uint_as_float(__float_as_uint(rt.x) & 0xFFFFE000u),
+                                 __uint_as_float(__float_as_uint(rt.y) & 0xFFFFE000u));   // 11 significant bits
+  const float2 rlo = __ffma2_rn(rhi, make_float2(-1.0f, -1.0f), rt);
+  c0.ext = h2bits(__floats2half2_rn(rhi.x, rlo.x));
+  c1.ext = h2bits(__floats2half2_rn(rhi.y, rlo.y));
+  // (k 2^-24, k 2^-24) has the bit pattern k * 0x10001; times -1024
+  c0.add = __hmul2(bits2h(__float_as_uint(tc.x) * 0x10001u + kKK), C.kn1024);
+  c1.add = __hmul2(bits2h(__float_as_uint(tc.y) * 0x10001u + kKK), C.kn1024);
+  // (1024 + sc, 1024 + sc) has the bit pattern (0x6400 | sc) * 0x10001; minus 1024
+  const __half2 sc0 = __hsub2(bits2h(lop_and_or(g0, 0x3Fu, 0x6400u) * 0x10001u), C.k1024);
+  const __half2 sc1 = __hsub2(bits2h(lop_and_or(g1, 0x3Fu, 0x6400u) * 0x10001u), C.k1024);
+  c0.mlo = __hmul2(sc0, C.k1024);
+  c0.mhi = __hmul2(sc0, C.k64);
+  c1.mlo = __hmul2(sc1, C.k1024);
+  c1.mhi = __hmul2(sc1, C.k64);
 }
 
 template <int FMT>
 __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& hd, int h, uint32_t aaddr,
-                                            const DecodeConsts& C, const uint32_t (&add4)[4]) {
+                                            const DecodeConsts& C, const Fold& fd, uint32_t* ext4) {
   if constexpr (FMT == kFmtQ4K || FMT == kFmtQ5K) {
     // the addend (-k 2^-14) and multipliers (sc 2^10, sc 2^6) of the two nibble positions of
-    // sub-blocks 4h .. 4h+3, from the precomputed pairs (-k 2^-14, sc 2^10)
+    // sub-blocks 4h .. 4h+3, and their A_ext pairs
+    SbConst sbc[4];
+    if (h == 0) {
+      fold_pair<0>(hd, fd, C, sbc[0], sbc[1]);
+      fold_pair<2>(hd, fd, C, sbc[2], sbc[3]);
+    } else {
+      fold_pair<4>(hd, fd, C, sbc[0], sbc[1]);
+      fold_pair<6>(hd, fd, C, sbc[2], sbc[3]);
+    }
     __half2 mlo[4], mhi[4], add[4];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t cm = add4[jj];
-      uint32_t lo2, hi2;
-      asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(lo2) : "r"(cm));
-      asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(hi2) : "r"(cm));
-      add[jj] = bits2h(lo2);
-      mlo[jj] = bits2h(hi2);
-      mhi[jj] = __hmul2(mlo[jj], C.k1o16);
+      add[jj] = sbc[jj].add;
+      mlo[jj] = sbc[jj].mlo;
+      mhi[jj] = sbc[jj].mhi;
+      ext4[jj] = sbc[jj].ext;
     }
     // A = (sc q - k) 2^-14 as fp16 pairs, 16 columns per sub-block.  The quants enter as fp16
     // subnormals: q 2^-24 (bits 0..3 of a half) or 16 q 2^-24 (bits 4..7).
@@ -761,10 +802,11 @@ __device__ __forceinline__ void decode_half(const HalfIn<FMT>& in, const uint4& 
 // ------------------------------------------------------------------------------------------
 // Hard tokens (q4k_xprep_kernel): their part of a super-block's outputs in fp32 on CUDA cores:
 // this row's packed bytes from the stage at rb (the first 16 in hd), the activations from X
-// (super-block sb of each token's row of K).  Each weight is its format's definition (one
-// rounding of the exact value, as the dequantization hook computes it); the 256 products are
-// summed in order of k.  aux0 / aux1: Q6K d; INT4 the scales of the two K halves; NVFP4 the
-// tensor scale g.
+// (super-block sb of each token's row of K; X and K from the trailer of the prepared block at
+// xblk).  Each weight is its format's definition (one rounding of the exact value, as the
+// dequantization hook computes it); the 256 products are summed in order of k.  aux: what the
+// format keeps outside its row blocks (Q6K's d plane, INT4's scale plane, NVFP4's tensor scale
+// g), for row `row` of the product's N.
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -813,9 +855,26 @@ __device__ __forceinline__ float weight_at(uint32_t rb, const uint4& hd, int t, 
   }
 }
 
-template <int FMT, int MT>
-__device__ __noinline__ void hard_dot(uint32_t rb, const uint16_t* X, int K, int sb, uint4 hd, float aux0, float aux1,
+template <int FMT, int MPAD, int MT>
+__device__ __noinline__ void hard_dot(uint32_t rb, uint32_t xblk, const void* aux, int N, int row, int sb, uint4 hd,
                                       uint32_t mask, float* out) {
+  const uint4 tr = lds128(xblk + mask_off(MPAD));   // (mask, K, address of X)
+  const int K = (int)tr.y;
+  const uint16_t* X = reinterpret_cast<const uint16_t*>((uint64_t)tr.z | ((uint64_t)tr.w << 32));
+  float aux0 = 0.f, aux1 = 0.f;
+  if constexpr (FMT == kFmtQ6K) {
+    if (row < N)
+      aux0 = __half2float(__ushort_as_half(__ldg(static_cast<const unsigned short*>(aux) + (int64_t)row * (K >> 8) + sb)));
+  } else if constexpr (FMT == kFmtINT4) {
+    if (row < N) {
+      const uint32_t sc2 =
+          __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(aux) + (int64_t)row * (K >> 7)) + sb);
+      aux0 = __low2float(bits2h(sc2));
+      aux1 = __high2float(bits2h(sc2));
+    }
+  } else if constexpr (FMT == kFmtNVFP4) {
+    aux0 = __ldg(static_cast<const float*>(aux));
+  }
   for (int k = 0; k < MT; ++k) out[k] = 0.f;
   for (int t = 0; t < 256; ++t) {
     const float w = weight_at<FMT>(rb, hd, t, aux0, aux1);
@@ -1001,8 +1060,9 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     // ------------------------------------------------------------------ dequant + epilogue
     // Software-pipelined over the group's super-blocks: once super-block i is handed to the
     // MMA warp, the group waits for the stage of super-block i+1 and takes what does not need
-    // tensor memory (its header, per-token scales, hard tokens) while the MMAs of i run; then it
-    // reads i's accumulator, and decodes i+1.
+    // tensor memory (its header, per-token scales, the mask of hard tokens) while the MMAs of i
+    // run; then it reads i's accumulator, and decodes i+1 (the hard tokens' part of i+1, if
+    // any, just before the stage is released).
     const int grp = warp >> 2;       // dequant group: the CTA's local tasks j % NG == grp
     const int q = warp & 3;          // TMEM lane quarter / row quarter of the tile
     const int r = 32 * q + lane;     // row inside the tile
@@ -1028,7 +1088,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     const uint32_t acc2 = tl + acc2_col(MPAD, grp, FMT, MT);
     // this warp's copies of the per-token scales of two super-blocks in flight (by parity)
     float* sigw = reinterpret_cast<float*>(smem + L::kSig) + warp * 64;
-    float hard_sum[2][MT];   // the hard tokens' sums of the super-blocks in flight (rarely used)
+    float hard_sum[MT];   // the hard tokens' sums of the super-block being finished (rarely used)
     asm volatile("griddepcontrol.wait;" ::: "memory");   // split counters zeroed, activations written
     uint32_t sbits = 0;   // parity of this group's full barrier of each stage
 
@@ -1039,8 +1099,9 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       uint32_t hmask;     // its hard tokens
       uint32_t ext[8];    // k-quants: the A_ext pairs of rho_j T (filled by the decode)
     };
-    // Wait for the i-th super-block of the group (task position c) and prepare it.
-    auto ahead = [&](int i, const GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG>& c, Ahead& A) -> bool {
+    // Wait for the i-th super-block of the group and take its header, per-token scales and hard
+    // tokens.
+    auto ahead = [&](int i, Ahead& A) -> bool {
       A.ws = su_of<NG>(n, grp, i, nmin) % kS;
       if (!wait_w(gfull(grp, A.ws), (sbits >> A.ws) & 1u)) return false;
       sbits ^= 1u << A.ws;
@@ -1050,28 +1111,6 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       float* sg = sigw + 32 * (i & 1);
       if (lane < MT / 4) *reinterpret_cast<uint4*>(sg + 4 * lane) = lds128(xblk + sig_off(MPAD) + 16 * lane);
       A.hmask = lds_u32(xblk + mask_off(MPAD)) & (MT == 32 ? 0xFFFFFFFFu : ((1u << MT) - 1u));
-      if (A.hmask != 0u) {   // uniform over the CTA: the mask belongs to the super-block of X
-        float a0 = 0.f, a1 = 0.f;
-        const TcEntry& E0 = P.e[c.e];
-        const int row0 = c.tile * kTileRows + r;
-        if constexpr (FMT == kFmtQ6K) {
-          if (row0 < E0.N)
-            a0 = __half2float(__ushort_as_half(
-                __ldg(static_cast<const unsigned short*>(P.aux[c.e]) + (int64_t)row0 * (E0.K >> 8) + c.sb)));
-        } else if constexpr (FMT == kFmtINT4) {
-          if (row0 < E0.N) {
-            const uint32_t sc2 = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.aux[c.e]) +
-                                                                         (int64_t)row0 * (E0.K >> 7)) + c.sb);
-            a0 = __low2float(bits2h(sc2));
-            a1 = __high2float(bits2h(sc2));
-          }
-        } else if constexpr (FMT == kFmtNVFP4) {
-          a0 = __ldg(static_cast<const float*>(P.aux[c.e]));
-        }
-        const uint4 tr = lds128(xblk + mask_off(MPAD));   // (mask, K, address of X)
-        const uint16_t* X = reinterpret_cast<const uint16_t*>((uint64_t)tr.z | ((uint64_t)tr.w << 32));
-        hard_dot<FMT, MT>(rb, X, (int)tr.y, c.sb, A.hd, a0, a1, A.hmask, hard_sum[i & 1]);
-      }
       return true;
     };
 
@@ -1090,7 +1129,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     float sx = 0.f, sy = 0.f;              // the accumulator factors of super-block i - 1
     uint32_t hm = 0;                       // its hard tokens
     for (int i = 0;; ++i) {
-      if (i < ng && !ahead(i, nx, A)) break;
+      if (i < ng && !ahead(i, A)) break;
       if (i >= 1) {
         // ---- the accumulator of super-block i - 1 into y (MT token columns)
         if (!wait_w(bar(kBarGDone + grp), (uint32_t)(i - 1) & 1u)) break;
@@ -1130,7 +1169,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
         if (hm != 0u) {
 #pragma unroll
           for (int k = 0; k < MT; ++k)
-            if ((hm >> k) & 1u) y[k] += hard_sum[(i - 1) & 1][k];
+            if ((hm >> k) & 1u) y[k] += hard_sum[k];
         }
 
         // ---- end of a chunk: y (this chunk's sum) is added to the task's running sum, or, for a
@@ -1208,6 +1247,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       const uint32_t ws = A.ws;
       const uint4 hd = A.hd;
       const uint32_t rb = sW + ws * kSB + r * kBlk;   // this row's bytes of the super-block
+      const uint32_t xblk = sW + ws * kSB + kWSB;      // its prepared activation block
       Fold fd{0.f, 0.f, 0.f};                          // k-quants: the row's fold factors
       if constexpr (has_min(FMT)) {
         const float2 dd = __half22float2(bits2h(hd.x));
@@ -1221,15 +1261,15 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
         HalfIn<FMT> in;
         load_half<FMT>(in, rb, h);
         if (h == 1) {
+          // hard tokens: this row's part of their outputs on CUDA cores (added after the
+          // accumulator in the epilogue of this super-block)
+          if (A.hmask != 0u)   // uniform over the CTA: the mask belongs to the super-block of X
+            hard_dot<FMT, MPAD, MT>(rb, xblk, P.aux[nx.e], P.e[nx.e].N, nx.tile * kTileRows + r, nx.sb, hd, A.hmask,
+                                    hard_sum);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         }
-        uint32_t a4[4];   // the half's sub-blocks' fold constants
-        if constexpr (has_min(FMT)) {
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) fold_k(kq_group(hd, 4 * h + jj), fd, dc, a4[jj], A.ext[4 * h + jj]);
-        }
-        decode_half<FMT>(in, hd, h, aslot + 64u * h, dc, a4);
+        decode_half<FMT>(in, hd, h, aslot + 64u * h, dc, fd, A.ext + 4 * h);
         if (h == 0) {   // the first K half goes to the MMA warp now
           tc::wait_st();
           tc::fence_before_sync();
