@@ -440,10 +440,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 // line: it runs once per split tile and would otherwise take registers from the hot loop.
 template <int MPAD, int MT>
 __device__ __noinline__ void reduce_chunks(const float* part, int chunks, int M, float* y, int N) {
+  constexpr int kB = MT >= 32 ? 1 : (MT >= 16 ? 2 : 4);   // chunk partials loaded together (added in chunk order)
   float v[MT];
 #pragma unroll
   for (int k = 0; k < MT; ++k) v[k] = (k < M) ? __ldcg(&part[k * kTileRows]) : 0.f;
-  for (int ch = 1; ch < chunks; ++ch) {
+  int ch = 1;
+  for (; ch + kB <= chunks; ch += kB) {
+    float t[kB][MT];
+#pragma unroll
+    for (int c = 0; c < kB; ++c)
+#pragma unroll
+      for (int k = 0; k < MT; ++k) t[c][k] = (k < M) ? __ldcg(&part[((size_t)(ch + c) * MPAD + k) * kTileRows]) : 0.f;
+#pragma unroll
+    for (int c = 0; c < kB; ++c)
+#pragma unroll
+      for (int k = 0; k < MT; ++k) v[k] = v[k] + t[c][k];
+  }
+  for (; ch < chunks; ++ch) {
 #pragma unroll
     for (int k = 0; k < MT; ++k)
       if (k < M) v[k] = v[k] + __ldcg(&part[((size_t)ch * MPAD + k) * kTileRows]);
@@ -494,22 +507,30 @@ struct TaskView {
   }
 };
 
-// Walk over the tasks of one dequant group: the CTA's local tasks j = g, g + NG, ... (task index
-// blockIdx.x + j * gridDim.x), each super-block of each task in order.
+// Walk over the tasks of one dequant group.  The launch's tasks are dealt to the NG x gridDim.x
+// (group, CTA) slots in rounds, slot s = g * gridDim.x + blockIdx.x taking task r * S + s in even
+// rounds r and r * S + (S - 1 - s) in odd ones (S slots; the host orders a launch's products by
+// decreasing K, so the back-and-forth order evens out the slots' work); each super-block of each
+// task in order.
 template <class PT, int NG>
 struct GroupCursor {
-  int j, t, e, tile, split, sb, end;
+  int r, slot, t, e, tile, split, sb, end;
   __device__ __forceinline__ void load(const PT& P) {
-    t = (int)blockIdx.x + j * (int)gridDim.x;
+    const int S = NG * (int)gridDim.x;
+    t = r * S + ((r & 1) ? S - 1 - slot : slot);
     if (t >= P.tasks_total) { t = -1; return; }
     const TaskView<PT> T(P, t);
     e = T.e; tile = T.tile; split = T.split; sb = T.sb0; end = T.sb1;
   }
-  __device__ __forceinline__ void start(const PT& P, int g) { j = g; load(P); }
+  __device__ __forceinline__ void start(const PT& P, int g) {
+    r = 0;
+    slot = g * (int)gridDim.x + (int)blockIdx.x;
+    load(P);
+  }
   // after the current super-block: true if it was the last of its task
   __device__ __forceinline__ bool advance(const PT& P) {
     if (++sb < end) return false;
-    j += NG;
+    ++r;
     load(P);
     return true;
   }
@@ -936,7 +957,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur;
     cur.start(P, lane);
     int cnt = 0;
-    while (cur.t >= 0) { cnt += cur.end - cur.sb; cur.j += NG; cur.load(P); }
+    while (cur.t >= 0) { cnt += cur.end - cur.sb; ++cur.r; cur.load(P); }
     group_sbs[lane] = cnt;
   }
   if (warp == kMmaWarp) {
@@ -967,8 +988,9 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     // Per super-block one TMA copy of the weights (rows row0 .. row0+127, rows past N read as
     // zeros; bytes 144 sb .. 144 sb + 143 of each row) and one bulk copy of the prepared
     // activation block, into the same stage, completing on that stage's barrier of the owning
-    // group.  The ring runs kS - 1 super-blocks ahead, in the CTA's super-block order.
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // the prepared activations are written
+    // group.  The ring runs kS - 1 super-blocks ahead, in the CTA's super-block order.  The
+    // weights of the first kS super-blocks are requested before the preparation grid has finished
+    // (they do not depend on it); their activation blocks once it has.
     if (elect_one()) {
       const uint64_t pol = policy_evict_first();
       GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur[NG];
@@ -978,9 +1000,23 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       uint32_t gbits = 0;    // parity of the next phase of each (group, stage) full barrier
       uint32_t owner = 0;    // group of the copies last issued into each stage, 2 bits a stage
       bool ok = true;
+      // activation-block copies held back until the preparation grid is complete: those of the
+      // super-blocks su < kS (in stage su), entry and super-block packed as e << 16 | sb
+      uint32_t pend[kS];
+      bool prepped = false;
+      auto release_pending = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the prepared activations are written
+        for (uint32_t k = 0; k < su && k < (uint32_t)kS; ++k) {
+          const uint32_t g = (owner >> (2 * k)) & 3u;
+          bulk_g2s(sW + k * kSB + kWSB, P.e[pend[k] >> 16].B + (int64_t)(pend[k] & 0xFFFFu) * kBB, kBB,
+                   gfull((int)g, k), 0ull);
+        }
+        prepped = true;
+      };
       for (int i = 0; i < nmax && ok; ++i) {
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
+          if (ok && i < n[g] && !prepped && su == (uint32_t)kS) release_pending();   // before a stage is reused
           if (ok && i < n[g]) ok = wait(bar(kBarWEmpty + su % kS), ((su / kS) & 1u) ^ 1u);
           if (ok && i < n[g]) {
             const uint32_t ws = su % kS;
@@ -990,12 +1026,14 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
             const int e = cur[g].e, sb = cur[g].sb;
             mbar_arrive_expect_tx(gfull(g, ws), kWSB + kBB);
             tma_load_2d(st, &P.maps[e], sb * kBlk, cur[g].tile * kTileRows, gfull(g, ws), pol);
-            bulk_g2s(st + kWSB, P.e[e].B + (int64_t)sb * kBB, kBB, gfull(g, ws), 0ull);
+            if (prepped) bulk_g2s(st + kWSB, P.e[e].B + (int64_t)sb * kBB, kBB, gfull(g, ws), 0ull);
+            else pend[su] = (uint32_t)e << 16 | (uint32_t)sb;
             cur[g].advance(P);
             ++su;
           }
         }
       }
+      if (!prepped) release_pending();
       // copies still in flight land before the CTA can end: wait for the last phase armed on
       // each stage's full barrier (complete already, or once its bytes have arrived)
       for (uint32_t k = (su > (uint32_t)kS ? su - kS : 0u); k < su; ++k) {
@@ -1471,11 +1509,15 @@ cudaError_t set_smem_attr() {
 // K split of a product: the number of splits of every 128-row tile and the super-blocks per
 // split (a multiple of kChunkSb, so that the split does not change the summation order).  A
 // batched launch has work enough for every SM and does not split; a single product picks the
-// split that minimizes
-//   (tasks per SM, rounded up) x (super-blocks per task) + 0.5 x (split tasks per SM)
-//     + 0.25 x (chunks summed by the last split)
-// in units of one super-block of a tile: the busiest SM's work, the cost of publishing a split
-// task's partial sums, and the final reduction's chain of partial-sum loads.
+// split with the least time on the busiest dequant group,
+//   pace x (its tasks) x (super-blocks per task) + 2.5 x (its tasks, if split)
+//     + 0.05 x (chunks summed by the last split)
+// in units of one super-block of a tile at the pace of a CTA whose ng groups all work (the
+// tasks are dealt to the SMs' (CTA, group) slots, GroupCursor).  An SM with fewer tasks than
+// groups runs fewer groups, each faster: pace 0.65 for one group, 0.92 for two of three.  The
+// constants are a least-squares fit to GB300 graph-replay timings of 5120 x 5120, 34816 x 5120
+// and 5120 x 17408 products at 1 to 17 splits (a split task costs its partial-sum stores, a
+// device-scope fence and an atomic on the busiest group).
 struct Split {
   int splits;
   int chunk;
@@ -1483,23 +1525,35 @@ struct Split {
 
 int chunks_of(int64_t K) { return (int)((K / 256 + kChunkSb - 1) / kChunkSb); }
 
-Split split_for(int64_t N, int64_t K, int sms, bool batched) {
+struct SplitCost {
+  Split split;
+  double units;   // busiest group's time, in super-blocks of a tile at the full pace
+};
+
+SplitCost split_cost(int64_t N, int64_t K, int sms, int ng, bool batched) {
   const int64_t tiles = (N + kTileRows - 1) / kTileRows;
   const int nb = (int)(K / 256);
   const int nch = chunks_of(K);
-  Split best{1, nb};
+  auto cost_of = [&](int splits, int chunk_sb) {
+    const double per_cta = std::ceil((double)(tiles * splits) / (double)std::max(1, sms));
+    const double per_group = std::ceil(per_cta / ng);
+    const int active = (int)std::min<double>(ng, per_cta);
+    const double pace = active >= ng ? 1.0 : (active == 1 ? (ng >= 3 ? 0.65 : 0.75) : 0.92);
+    return pace * per_group * chunk_sb + (splits > 1 ? 2.5 * per_group + 0.05 * nch : 0.0);
+  };
+  SplitCost best{Split{1, nb}, cost_of(1, nb)};
   if (batched) return best;
-  double best_cost = 1e300;
-  for (int cps = nch; cps >= 1; --cps) {   // chunks per split
+  for (int cps = nch - 1; cps >= 1; --cps) {   // chunks per split
     const int splits = (nch + cps - 1) / cps;
-    if (cps != nch && (nch + splits - 1) / splits != cps) continue;   // same splits, larger chunk seen
-    const double per_sm = std::ceil((double)(tiles * splits) / (double)std::max(1, sms));
+    if ((nch + splits - 1) / splits != cps) continue;   // same splits, larger chunk seen
     const int chunk_sb = std::min(nb, cps * kChunkSb);
-    const double cost = per_sm * chunk_sb + (splits > 1 ? 0.5 * per_sm + 0.25 * nch : 0.0);
-    if (cost < best_cost - 1e-9) { best_cost = cost; best = Split{splits, splits == 1 ? nb : chunk_sb}; }
+    const double c = cost_of(splits, chunk_sb);
+    if (c < best.units - 1e-9) best = SplitCost{Split{splits, chunk_sb}, c};
   }
   return best;
 }
+
+Split split_for(int64_t N, int64_t K, int sms, int ng, bool batched) { return split_cost(N, K, sms, ng, batched).split; }
 
 // Bytes of split workspace (partials, then counters) that a job needs.
 struct SplitSpace {
@@ -1642,9 +1696,29 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
   cudaError_t err = launch_prep<MPAD, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream);
   if (err != cudaSuccess) return err;
   if (count == 1) return launch_main<FMT, MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M, stream);
-  for (int k0 = 0; k0 < count; k0 += kMaxEBatch) {
-    err = launch_main<FMT, MPAD, kMaxEBatch>(jobs + k0, bsrc.data() + k0, sp.data() + k0, part.data() + k0,
-                                             ctr.data() + k0, std::min(kMaxEBatch, count - k0), M, stream);
+  // Launches of near-equal size, each with its products ordered by decreasing K (the kernel deals
+  // tasks back and forth over its slots: large tasks first, then the small ones even them out).
+  const int launches = (count + kMaxEBatch - 1) / kMaxEBatch;
+  const int per = (count + launches - 1) / launches;
+  std::vector<int> ord(count);
+  for (int k = 0; k < count; ++k) ord[k] = k;
+  std::vector<Job> pj(count);
+  std::vector<const uint8_t*> pb(count);
+  std::vector<Split> ps(count);
+  std::vector<float*> pp(count);
+  std::vector<unsigned*> pc(count);
+  for (int k0 = 0; k0 < count; k0 += per) {
+    const int n = std::min(per, count - k0);
+    std::stable_sort(ord.begin() + k0, ord.begin() + k0 + n, [&](int a, int b) { return jobs[a].K > jobs[b].K; });
+    for (int k = k0; k < k0 + n; ++k) {
+      pj[k] = jobs[ord[k]];
+      pb[k] = bsrc[ord[k]];
+      ps[k] = sp[ord[k]];
+      pp[k] = part[ord[k]];
+      pc[k] = ctr[ord[k]];
+    }
+    err = launch_main<FMT, MPAD, kMaxEBatch>(pj.data() + k0, pb.data() + k0, ps.data() + k0, pp.data() + k0,
+                                             pc.data() + k0, n, M, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
@@ -1675,7 +1749,7 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
   std::vector<Split> sp(count);
   size_t split_bytes = 0, zero_words = 0;
   for (int k = 0; k < count; ++k) {
-    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, count > 1 || jobs[k].gated);   // gating needs whole rows
+    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, groups(MPAD, FMT), count > 1 || jobs[k].gated);   // gating needs whole rows
     const SplitSpace s = split_space<MPAD>(jobs[k].N, jobs[k].K, sp[k]);
     split_bytes += s.partial_bytes;
     zero_words += s.counter_words;
@@ -1728,24 +1802,24 @@ cudaError_t read_and_clear_tc_status(unsigned* out) {
   return e;
 }
 
-// Time model of a tensor-core launch over jobs[0 .. count), fitted to GB300 timings: a fixed
-// ~10 us (two launches, pipeline fill), the busiest SM's super-blocks of a tile at 0.53 / 0.60 /
-// 0.79 us each for M <= 8 / 16 / 32, and ~1.5 us per split task on it (partial sums, fences).
+// Time model of a Q4K tensor-core launch over jobs[0 .. count), fitted to GB300 graph-replay
+// timings: a fixed ~6 us (two launches, pipeline fill and drain) and the busiest dequant group's
+// work (split_cost) at a full-CTA pace of 1.385 / 1.49 / 1.5 us per super-block of a tile for
+// M <= 8 / 16 / 32 (three groups, three, two).  A batched launch (no splits) counts its tasks
+// over all slots.
 double tc_estimate_us(const Job* jobs, int count, int M) {
   const int sms = std::max(1, num_sms());
-  double tasks = 0, sbs = 0, split_tasks = 0;
+  const int ng = groups(M <= 16 ? 16 : 32);
+  const double pace_us = M <= 8 ? 1.385 : (M <= 16 ? 1.49 : 1.5);
+  if (count == 1) return 6.0 + pace_us * split_cost(jobs[0].N, jobs[0].K, sms, ng, false).units;
+  double tasks = 0, sbs = 0;
   for (int k = 0; k < count; ++k) {
-    const Split sp = split_for(jobs[k].N, jobs[k].K, sms, count > 1);
     const double tiles = std::ceil((double)jobs[k].N / kTileRows);
-    tasks += tiles * sp.splits;
+    tasks += tiles;
     sbs += tiles * (double)(jobs[k].K / 256);
-    if (sp.splits > 1) split_tasks += tiles * sp.splits;
   }
-  // whole tasks per SM, each of the average size
-  const double per_sm_tasks = std::ceil(tasks / sms);
-  const double per_sm_sbs = per_sm_tasks * (sbs / std::max(1.0, tasks));
-  const double rate = M <= 8 ? 0.53 : (M <= 16 ? 0.60 : 0.79);
-  return 10.0 + per_sm_sbs * rate + 1.5 * std::ceil(split_tasks / sms);
+  const double per_group_tasks = std::ceil(std::ceil(tasks / sms) / ng);
+  return 6.0 + pace_us * per_group_tasks * (sbs / std::max(1.0, tasks));
 }
 
 bool tc_supports(int M, int64_t N, int64_t K) {
