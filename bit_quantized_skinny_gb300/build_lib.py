@@ -23,7 +23,8 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompil
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-fno-fast-math",
              "-I" + INCLUDE, "-I" + CSRC, "-I" + os.path.join(CUDA_HOME, "include")]
 
-CU_SOURCES = ["q4k_fma.cu", "q4k_dequant.cu", "q4k_tc.cu", "q4k_ffn.cu", "q4k_gather.cu", "qmm_probe.cu"]
+CU_SOURCES = ["q4k_fma.cu", "q4k_dequant.cu", "q4k_tc.cu", "q4k_ffn.cu", "q4k_gather.cu", "qmm_probe.cu",
+              "q4k_pack_dev.cu"]
 CXX_SOURCES = ["qmm_api.cpp", "qmm_pack.cpp"]
 
 

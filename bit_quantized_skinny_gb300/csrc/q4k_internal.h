@@ -73,6 +73,11 @@ cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cu
 int stream_read_grid();
 
 // Device status words of the kernel files: read and clear (synchronous; 0 = no error).
+// Device-side packer: fp32 W (device) -> Q4K super-blocks (device), the host packer's bytes; a
+// super-block with a non-finite weight or an fp16 scale overflow is written as zeros and sets
+// bit 1 of the pack status word.
+cudaError_t launch_pack_dev(const float* W, int64_t N, int64_t K, void* out, cudaStream_t stream);
+cudaError_t read_and_clear_pack_status(unsigned* out);
 cudaError_t read_and_clear_fma_status(unsigned* out);
 cudaError_t read_and_clear_tc_status(unsigned* out);
 

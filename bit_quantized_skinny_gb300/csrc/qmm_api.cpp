@@ -125,6 +125,17 @@ qmm_status qmm_pack(const float* W_host, int64_t N, int64_t K, void* out_host, s
   return rc == 0 ? QMM_OK : QMM_ERR_NONFINITE;
 }
 
+qmm_status qmm_pack_dev(const float* W_dev, int64_t N, int64_t K, void* out_dev, size_t out_bytes,
+                        cudaStream_t stream) {
+  if (!W_dev || !out_dev) return QMM_ERR_NULL;
+  qmm_status s = check_shape(N, K);
+  if (s != QMM_OK) return s;
+  if (out_bytes < qmm_packed_bytes(N, K)) return QMM_ERR_BUFSIZE;
+  if (!aligned(W_dev, 16) || !aligned(out_dev, 16)) return QMM_ERR_ALIGN;
+  const cudaError_t e = q4k::launch_pack_dev(W_dev, N, K, out_dev, stream);
+  return e == cudaSuccess ? QMM_OK : cuda_fail(e);
+}
+
 qmm_status qmm_run_variant(const void* Wq_dev, int64_t N, int64_t K, const uint16_t* X_dev,
                            float* Y_dev, int M, int variant, cudaStream_t stream) {
   qmm_status s = check_job(Wq_dev, N, K, X_dev, Y_dev);
@@ -401,10 +412,11 @@ size_t qmm_workspace_bytes_held(void) { return q4k::workspace_bytes_held(); }
 
 qmm_status qmm_device_status(unsigned* status_out) {
   if (!status_out) return QMM_ERR_NULL;
-  unsigned a = 0, b = 0;
+  unsigned a = 0, b = 0, c = 0;
   cudaError_t e = q4k::read_and_clear_fma_status(&a);
   if (e == cudaSuccess) e = q4k::read_and_clear_tc_status(&b);
-  *status_out = a | b;
+  if (e == cudaSuccess) e = q4k::read_and_clear_pack_status(&c);
+  *status_out = a | b | c;
   return e == cudaSuccess ? QMM_OK : cuda_fail(e);
 }
 

@@ -36,7 +36,7 @@ EXPORTS = ["qmm_packed_bytes", "qmm_pack", "qmm_run", "qmm_run_batched", "qmm_de
            "qmm_ffn_workspace_bytes", "qmm_run_ffn", "qmm_indexed_workspace_bytes", "qmm_run_indexed",
            "qmm_fmt_packed_bytes", "qmm_fmt_pack", "qmm_fmt_run", "qmm_fmt_dequant", "qmm_fmt_run_batched",
            "qmm_ffn_fused_workspace_bytes", "qmm_run_ffn_fused", "qmm_release", "qmm_workspace_bytes_held",
-           "qmm_stream_read", "qmm_stream_read_sink_words", "qmm_set_wait_limit"]
+           "qmm_stream_read", "qmm_stream_read_sink_words", "qmm_set_wait_limit", "qmm_pack_dev"]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -77,6 +77,8 @@ def load(path: str | None = None):
     lib.qmm_packed_bytes.restype = ctypes.c_size_t
     lib.qmm_pack.argtypes = [vp, i64, i64, vp, ctypes.c_size_t, i32]
     lib.qmm_pack.restype = i32
+    lib.qmm_pack_dev.argtypes = [vp, i64, i64, vp, ctypes.c_size_t, vp]
+    lib.qmm_pack_dev.restype = i32
     lib.qmm_run.argtypes = [vp, i64, i64, vp, vp, i32, vp]
     lib.qmm_run.restype = i32
     lib.qmm_run_variant.argtypes = [vp, i64, i64, vp, vp, i32, i32, vp]
@@ -161,6 +163,23 @@ def pack(W: np.ndarray, threads: int = 0, out: np.ndarray | None = None) -> np.n
         out = np.empty(nbytes, dtype=np.uint8)
     _check(load().qmm_pack(W.ctypes.data_as(ctypes.c_void_p), N, K, out.ctypes.data_as(ctypes.c_void_p),
                            out.nbytes, threads), "qmm_pack")
+    return out
+
+
+def pack_dev(W, out=None, stream=None):
+    """qmm_pack_dev: pack an N x K fp32 CUDA tensor into Q4K bytes on the GPU (a uint8 CUDA
+    tensor of packed_bytes(N, K) bytes, allocated when `out` is None), asynchronous on `stream`
+    (default: torch's current stream).  Non-finite super-blocks come out as zeros and set bit 1
+    of device_status()."""
+    import torch
+    N, K = W.shape
+    nbytes = packed_bytes(N, K)
+    if nbytes == 0:
+        raise QmmError(2, "qmm_pack_dev")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check(load().qmm_pack_dev(ctypes.c_void_p(W.data_ptr()), N, K, ctypes.c_void_p(out.data_ptr()),
+                               out.numel() * out.element_size(), _stream_handle(stream)), "qmm_pack_dev")
     return out
 
 

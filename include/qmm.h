@@ -115,6 +115,18 @@ size_t qmm_packed_bytes(int64_t N, int64_t K);
 qmm_status qmm_pack(const float* W_host, int64_t N, int64_t K, void* out_host, size_t out_bytes,
                     int threads);
 
+/* The same packing on the GPU: W_dev (N x K row-major fp32, device memory, 16-byte aligned)
+ * into the caller's device buffer out_dev (16-byte aligned, out_bytes >= qmm_packed_bytes(N, K)),
+ * enqueued on `stream`.  Every super-block is byte-identical to what qmm_pack writes (the
+ * quantizer above, each step the same IEEE fp32 operation).  A super-block that holds a
+ * non-finite weight, or whose d or dmin overflows binary16, is written as 144 zero bytes and
+ * sets bit 1 of the device status word (qmm_device_status); qmm_pack instead rejects the whole
+ * matrix with QMM_ERR_NONFINITE.  The weights are read once and not modified.  Errors (before
+ * anything is enqueued): QMM_ERR_NULL, QMM_ERR_SHAPE, QMM_ERR_BUFSIZE, QMM_ERR_ALIGN;
+ * QMM_ERR_CUDA if the launch fails. */
+qmm_status qmm_pack_dev(const float* W_dev, int64_t N, int64_t K, void* out_dev, size_t out_bytes,
+                        cudaStream_t stream);
+
 /* Y_dev[M x N] = X_dev[M x K] * dequant(Wq_dev)^T, enqueued on `stream`.
  * Wq_dev: packed weights on the device (qmm_packed_bytes(N, K) bytes, 16-byte aligned).
  * X_dev: bf16 activations; Y_dev: fp32 result (overwritten).  The kernel variant is chosen
@@ -378,7 +390,8 @@ void qmm_set_wait_limit(uint32_t polls, uint32_t suspend_ns);
 /* Read and clear the status word that the kernels of this library keep on the current device
  * (a synchronous call: it waits for the device).  0: no kernel reported a problem since the
  * last read.  Bit 0: a kernel stopped waiting for its own weight copies after a bounded number
- * of polls; the outputs of the calls since the last read are then invalid. */
+ * of polls; the outputs of the calls since the last read are then invalid.  Bit 1: qmm_pack_dev
+ * met a non-finite weight or an fp16 scale overflow and wrote zeros for that super-block. */
 qmm_status qmm_device_status(unsigned* status_out);
 
 /* Human-readable text of a status code (static storage). */

@@ -59,6 +59,12 @@ def test_argument_errors_need_no_gpu(qmm):
     assert lib.qmm_run_batched(ents, 513, 1, None) == 8
     assert lib.qmm_dequant(p, 4, 100, p, None) == 2
     assert lib.qmm_strerror(3) == b"M must be in [1, 32]"
+    # the device packer validates on the host before anything is enqueued
+    assert lib.qmm_pack_dev(None, 4, 256, p, 4 * 144, None) == 1
+    assert lib.qmm_pack_dev(p, 4, 255, p, 4 * 144, None) == 2
+    assert lib.qmm_pack_dev(p, 4, 256, p, 4 * 144 - 1, None) == 5
+    assert lib.qmm_pack_dev(ctypes.c_void_p(24), 4, 256, p, 4 * 144, None) == 4
+    assert lib.qmm_pack_dev(p, 4, 256, ctypes.c_void_p(40), 4 * 144, None) == 4
 
 
 @pytest.mark.parametrize("shape", [(256, 512), (37, 2304), (5, 256), (64, 5120)])
