@@ -12,6 +12,8 @@ larger than L2 (129 MB), so no flush is needed between steps.
   python bench.py --single gate_up|down|q|k|lm_head|all [--Ms 1,2,...] [--variant fma|tc|auto|both]
   python bench.py --ffn [--Ms 1,2,...]     (one feed-forward block per call: gate/up, gate, down)
   python bench.py --indexed [--Ms 1,2,...] (indexed-expert product over 16 experts)
+  python bench.py --profile-pass L [--M 8] (a few untimed steps over the first L layers: the small
+                                           case that DRAM-traffic captures run on)
 
 `--single` times one matrix product per launch instead (weights cycled over copies totalling
 more than 4x the L2 size), for the switch-point sweep between the two kernel families and as
@@ -71,11 +73,15 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the library's sources with // comments and blank space removed (a comment edit
+    does not change the kernels whose counters a profile recorded)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_quantized_skinny_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            code = re.sub(r"//[^\n]*", "", fh.read())
+        h.update(name.encode() + " ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -162,10 +168,11 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workload --
 
-def layer_pass_setup(M: int, device: str):
-    """Device buffers for the 64-layer pass: each distinct matrix is packed once and copied
-    into 64 distinct device buffers (content does not change the speed; every buffer is
-    read from HBM).  Returns (entries, info) with info holding the host-side copies."""
+def layer_pass_setup(M: int, device: str, layers: int = LAYERS):
+    """Device buffers for the 64-layer pass (or its first `layers` layers): each distinct matrix
+    is packed once and copied into one distinct device buffer per layer (content does not change
+    the speed; every buffer is read from HBM).  Returns (entries, info) with info holding the
+    host-side copies."""
     import torch
     from bit_quantized_skinny_gb300 import inputs, qmm, workloads
 
@@ -179,11 +186,11 @@ def layer_pass_setup(M: int, device: str):
         xs[K] = workloads.activations(M, K, inputs.seed_for(4, 100 + K % 97), device=device)
     # the outputs of a pass live in one arena (one result buffer per step, as a model runtime
     # keeps them), each product's Y a slice of it
-    y_arena = torch.empty(LAYERS * sum(M * N for _, N, _ in workloads.LAYER_SHAPES), dtype=torch.float32,
+    y_arena = torch.empty(layers * sum(M * N for _, N, _ in workloads.LAYER_SHAPES), dtype=torch.float32,
                           device=device)
     items, ys, ws = [], [], []
     off = 0
-    for layer in range(LAYERS):
+    for layer in range(layers):
         for idx, (name, N, K) in enumerate(workloads.LAYER_SHAPES):
             w = bases[idx] if layer == 0 else bases[idx].clone()
             y = y_arena[off:off + M * N].view(M, N)
@@ -648,6 +655,29 @@ SINGLE_SHAPES = {"gate_up": (34816, 5120), "down": (5120, 17408), "q": (5120, 51
                  "lm_head": (248320, 5120), "tiny": (256, 512)}
 
 
+def run_profile_pass(args):
+    """The small case that profiling captures: `--steps` steps of the pass over the first
+    `--profile-pass` layers (one activation-prep launch and ceil(6 L / 160) product launches per
+    step, all of them after `--warmup` warm-up steps), no timing.  Prints one JSON line."""
+    import torch
+    from bit_quantized_skinny_gb300 import build_lib, qmm
+
+    build_lib.build()
+    qmm.load()
+    torch.cuda.set_device(0)
+    layers = args.profile_pass
+    entries, info = layer_pass_setup(args.M, "cuda", layers)
+    for _ in range(args.warmup + args.steps):
+        qmm.run_batched(entries, args.M)
+    torch.cuda.synchronize()
+    if qmm.device_status() != 0:
+        raise RuntimeError("kernel reported a device-side error")
+    print(json.dumps({"profile_pass": {"layers": layers, "matrices": len(entries), "M": args.M,
+                                       "weight_bytes": info["weight_bytes"], "algorithmic_bytes": info["algo_bytes"],
+                                       "steps": args.warmup + args.steps,
+                                       "product_launches_per_step": -(-len(entries) // 160)}}), flush=True)
+
+
 def run_single(args):
     """One product per launch, per shape x M x variant, weights cycled over copies totalling
     more than 4x L2 so every launch reads HBM.  Prints one JSON line."""
@@ -951,6 +981,8 @@ def main(argv=None):
     ap.add_argument("--fmt", default=None, help="with --formats: only these formats (comma list)")
     ap.add_argument("--pass-formats", default=None,
                     help="time the 64-layer pass in these weight formats instead (comma list, 'mix_q4k_q6k' or 'all')")
+    ap.add_argument("--profile-pass", type=int, default=0,
+                    help="run warmup + steps steps of the first L layers' pass, untimed (the small case for ncu)")
     ap.add_argument("--formats", default=None,
                     help="time the weight formats on these shapes instead (comma list of gate_up,down,q,k,lm_head or 'all')")
     args = ap.parse_args(argv)
@@ -962,6 +994,10 @@ def main(argv=None):
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.profile_pass:
+        if rank == 0:
+            run_profile_pass(args)
         return
     if args.single:
         if rank == 0:

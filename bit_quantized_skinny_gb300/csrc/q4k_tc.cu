@@ -10,45 +10,53 @@
 // pages (a matrix kernel from a few rows on, section "The patch") done with GB300's units.
 //
 // Operands ("swap AB": the 128-row MMA dimension runs over weight rows), described for Q4K:
-//   A[128 rows x 16 k] fp16 in tensor memory (TMEM): A = sc_j * q_t, an integer <= 945, exact.
-//     Written by the dequant warps with tcgen05.st, one thread per weight row (lane).
-//   B[16 k x Mpad] fp16 in shared memory: the activations of one super-block, x * 2^-s with one
-//     power-of-two s per super-block so that every bf16 value is exact in fp16 (see below).
+//   A[128 rows x 16 k] fp16 in tensor memory (TMEM): A = (sc_j q_t - k_j) 2^-14 with the min
+//     term folded in (k_j = rint(m_j Dm / D), see Fold below): an integer times 2^-14, exact,
+//     and exactly zero for a weight that is exactly zero.  Written by the dequant warps with
+//     tcgen05.st, one thread per weight row (lane).
+//   B[16 k x Mpad] fp16 in shared memory: the activations of one super-block, x * 2^-s_i with one
+//     power of two per token i so that its bf16 values are exact in fp16 (see the preparation).
 //   D[128 x Mpad] fp32 in TMEM, one accumulator per 256-weight super-block.
-//   One more K=16 MMA per super-block multiplies A_ext = (m_0..m_7, m_0..m_7) with
-//   B_ext = (hi_0..hi_7, lo_0..lo_7), the fp16 halves of the sub-block sums of x, so the
-//   dmin term also comes from the tensor cores.  The epilogue forms, per super-block,
-//     y += (D*2^s) * acc - (Dm*2^s*64) * acc_ext
+//   Two more K=16 MMAs per super-block multiply A_ext (the fp16 pair (hi, lo) of the residual
+//   rho_j T of each sub-block, twice) with B_ext (the fp16 pair of the sub-block sums of x as
+//   rows (hi, hi, lo, lo)): the residual of the min term also comes from the tensor cores.  The
+//   epilogue forms, per super-block and token i,
+//     y_i += sigma_i (D acc_i + f_e acc_ext_i),   sigma_i = 2^(s_i + 14), f_e = -2^(e - 16)
 //   in fp32 registers.  Products in the MMAs are exact; only fp32 accumulation rounds.
-//   The other formats keep A exact in fp16 too (Q5K sc*q <= 1953; Q6K sc*(q-32) <= 2048 with
+//   The other formats keep A exact in fp16 too (Q5K sc*q - k <= 1953; Q6K sc*(q-32) <= 2048 with
 //   7-bit scales; NVFP4 s*v, at most 6 significant bits; INT4 q itself) and differ in the
-//   epilogue: NVFP4 and Q6K have one accumulator (factor g*2^s or d*2^s), INT4 one per K half
+//   epilogue: NVFP4 and Q6K have one accumulator (factor g 2^-14 or d 2^-14), INT4 one per K half
 //   (its two scale groups), Q5K the Q4K pair.
 //
-// K order inside a super-block: the nibble trick below yields the quants of one 32-bit word as
+// K order inside a super-block: the nibble masks below yield the quants of one 32-bit word as
 // fp16 pairs (q0,q4) (q1,q5) (q2,q6) (q3,q7); TMEM column 4w+c holds k = 8w+c (low half) and
 // 8w+c+4 (high half), and the activations are laid out in B with the same permutation.
 //
 // Work: a task is one 128-row tile of one product over a range of its super-blocks (a K split).
+// A launch's tasks are dealt to its (dequant group, CTA) slots in back-and-forth rounds.
 // Summation order: a row's super-blocks are summed in chunks of 4 (each chunk from zero, in order
 // of k) and the chunk sums are added in chunk order; splits cut only at chunk boundaries, so a
 // product's bits depend neither on M nor on how its work is split or batched.  One CTA per SM.
 //
-// Roles (448 threads at Mpad 16, 320 at Mpad 32; 448 for the one-accumulator formats):
-//   dequant groups (3 at Mpad 16, 2 at Mpad 32 -- 3 for NVFP4 and Q6K, whose groups own one
-//                accumulator block instead of two; 4 warps each, warp q <-> TMEM lanes 32q..32q+31,
-//                the rows of the tile).  The CTA's tasks are dealt to the groups round robin; a
-//                group walks its tasks' super-blocks in order.  Each group owns one A slot and
-//                one accumulator in TMEM.  Per super-block: read the stage, write the A slot one
-//                K half at a time (each half handed to the MMA lane as soon as it is written),
-//                wait for the MMAs, read the accumulator and scale it into y.
+// Roles (512 threads; 352 at 32 token columns for the two-accumulator formats):
+//   dequant groups (3; 2 at 32 token columns except for NVFP4 and Q6K, whose groups own one
+//                accumulator block instead of two; 4 warps each, warp q <-> TMEM lanes
+//                32q..32q+31, the rows of the tile).  Each group owns one A slot and its
+//                accumulators in TMEM and walks its tasks' super-blocks, software-pipelined:
+//                while the MMAs of super-block i run it waits for the stage of i+1 and takes its
+//                header, per-token scales and hard-token mask; then it reads i's accumulator and
+//                decodes i+1 one K half at a time, each half handed to its MMA warp as soon as it
+//                is written; hard tokens (see the preparation) are summed on CUDA cores just
+//                before the stage is released.
 //   copy warp    per super-block one 2D TMA tile copy of the weights (128 rows x the format's
 //                bytes per 256 weights) and one bulk copy of the prepared activation block into
 //                a stage of the ring (8 stages for 8 token columns, 7 for 16, 5 for 32; fewer for
-//                the wider formats), in the CTA's super-block order: rounds over the groups.
-//   MMA warp     owns TMEM; one elected lane issues each super-block's MMAs (8 per K half, and
-//                one for the dmin term of the k-quants) in the same order.  Issuing from an elect.sync branch
-//                keeps the operands in uniform registers (~14 cycles per MMA).
+//                the wider formats), in the CTA's super-block order (rounds over the groups).
+//                The first ring's weights are requested before the preparation grid finishes.
+//   MMA warps    one per group (the first owns TMEM); one elected lane issues its group's MMAs
+//                (8 per K half, and two for the min term of the k-quants) and commits them to the
+//                group's completion barrier and the stage's empty barrier.  Issuing from an
+//                elect.sync branch keeps the operands in uniform registers (~14 cycles per MMA).
 // Every barrier is waited on only by threads that see all of its phases in order (a parity wait
 // is exact only then): full barriers per (group, stage), handoff and completion barriers per
 // group.  Every wait is bounded; on timeout the kernel records an error in the status word, the
@@ -60,10 +68,12 @@
 // slice, zeroed by the preparation kernel of the same call) adds all chunk sums of the tile in
 // chunk order and writes Y.
 //
-// Activation preparation (q4k_xprep_kernel, one CTA per super-block of each distinct X): picks
-// s so that the largest |x| of the super-block lands in [2^14, 2^15); a bf16 value is then exact
-// in fp16 unless it is below 2^-32 of that largest value (such values are rounded to fp16's
-// 2^-24 step of the scaled range), and writes B, B_ext and 2^s into a per-stream workspace.
+// Activation preparation (q4k_xprep_kernel, one CTA per super-block of each distinct X): per
+// token a power of two s_i that puts its largest |x| in [2^14, 2^15); B, B_ext, sigma_i and a
+// trailer (hard-token mask, K, the address of X) go to a per-stream workspace.  A token whose
+// staging would not be exact (a value below fp16's range after scaling, or a sub-block sum too
+// small for its (hi, lo) pair) is "hard": its B and B_ext rows are zero and the product kernel
+// computes its part of that super-block from X on CUDA cores.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -94,9 +104,9 @@ constexpr int kTileRows = 128;
 constexpr int kGroupWarps = 4;     // a dequant group: one warp per TMEM lane quarter (32 rows)
 constexpr int kMaxGroups = 3;
 // Dequant groups: three at Mpad 16, two at Mpad 32 (what tensor memory holds, below) -- three
-// for the formats with one accumulator block per group.  With the copy and MMA warps that is at
-// most 14 warps, at most 4 per SM sub-partition, which leaves each thread 128 registers (a
-// sub-partition holds 16384).
+// for the formats with one accumulator block per group.  With the copy warp and one MMA warp per
+// group that is 16 warps (11 for two groups), four per SM sub-partition, which leaves each thread
+// 128 registers (a sub-partition holds 16384; 168 with two groups).
 // The formats with one accumulator block per group (no dmin term, one scale group per
 // super-block).
 __host__ __device__ constexpr bool single_acc(int f) { return f == kFmtNVFP4 || f == kFmtQ6K; }
@@ -109,8 +119,8 @@ constexpr int kSmemLimit = 232448; // shared memory per CTA (227 KB)
 
 // Bytes of one row's 256 weights in the streamed weight plane (one TMA box column), per format:
 // Q4K and NVFP4 144 (NVFP4: 16 E4M3 scales + 128 bytes of codes), Q5K 176, Q6K 208, INT4 128
-// (INT4's scales and Q6K's super-block scales live in separate planes).  The dmin term (an extra
-// MMA and a second accumulator column block) belongs to Q4K and Q5K only.
+// (INT4's scales and Q6K's super-block scales live in separate planes).  The min term (an extra
+// MMA pair and a second accumulator column block) belongs to Q4K and Q5K only.
 __host__ __device__ constexpr int blk_bytes(int f) {
   return f == kFmtQ5K ? 176 : (f == kFmtQ6K ? 208 : (f == kFmtINT4 ? 128 : 144));
 }
@@ -1466,7 +1476,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Map of a packed matrix's weight plane as a 2D byte array: inner dimension the bytes of a row
 // (K/256 blocks of blk_bytes(fmt)), outer dimension the N rows; the box is one 256-weight block
-// of 128 rows.  INT4 boxes (128 bytes) are copied with the 128-byte swizzle.
+// of 128 rows.  INT4 boxes (128 bytes) are copied with the 128-byte swizzle.  L2 promotion to
+// 128 bytes: with 256-byte promotion the evict-first rows of a 144-byte box pulled in bytes of
+// the next super-block that were often gone again when it was copied (DRAM traffic 1.038x of
+// lm_head's bytes against 1.017x, measured on GB300).
 cudaError_t weight_map(const void* W, int64_t N, int64_t K, int fmt, CUtensorMap* out) {
   static std::mutex mu;
   static std::map<std::tuple<const void*, int64_t, int64_t, int>, CUtensorMap> cache;
@@ -1485,7 +1498,7 @@ cudaError_t weight_map(const void* W, int64_t N, int64_t K, int fmt, CUtensorMap
   const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         fmt == kFmtINT4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   if (cache.size() >= 4096) cache.clear();
   cache.emplace(key, m);
