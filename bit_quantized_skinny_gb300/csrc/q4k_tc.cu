@@ -38,9 +38,9 @@
 // of k) and the chunk sums are added in chunk order; splits cut only at chunk boundaries, so a
 // product's bits depend neither on M nor on how its work is split or batched.  One CTA per SM.
 //
-// Roles (512 threads; 352 at 32 token columns for the two-accumulator formats):
-//   dequant groups (3; 2 at 32 token columns except for NVFP4 and Q6K, whose groups own one
-//                accumulator block instead of two; 4 warps each, warp q <-> TMEM lanes
+// Roles (512 threads; 352 for INT4 at 32 token columns):
+//   dequant groups (3; 2 for INT4 at 32 token columns, whose groups own two accumulator blocks
+//                next to the slot; 4 warps each, warp q <-> TMEM lanes
 //                32q..32q+31, the rows of the tile).  Each group owns one A slot and its
 //                accumulators in TMEM and walks its tasks' super-blocks, software-pipelined:
 //                while the MMAs of super-block i run it waits for the stage of i+1 and takes its
@@ -50,8 +50,8 @@
 //                before the stage is released.
 //   copy warp    per super-block one 2D TMA tile copy of the weights (128 rows x the format's
 //                bytes per 256 weights) and one bulk copy of the prepared activation block into
-//                a stage of the ring (8 stages for 8 token columns, 7 for 16, 5 for 32; fewer for
-//                the wider formats), in the CTA's super-block order (rounds over the groups).
+//                a stage of the ring (8 stages for 8 token columns, 7 for 16, 4 or 5 for 32; fewer
+//                for the wider formats), in the CTA's super-block order (rounds over the groups).
 //                The first ring's weights are requested before the preparation grid finishes.
 //   MMA warps    one per group (the first owns TMEM); one elected lane issues its group's MMAs
 //                (8 per K half, and two for the min term of the k-quants) and commits them to the
@@ -103,14 +103,14 @@ __device__ unsigned g_status;   // this file's kernels' status word
 constexpr int kTileRows = 128;
 constexpr int kGroupWarps = 4;     // a dequant group: one warp per TMEM lane quarter (32 rows)
 constexpr int kMaxGroups = 3;
-// Dequant groups: three at Mpad 16, two at Mpad 32 (what tensor memory holds, below) -- three
-// for the formats with one accumulator block per group.  With the copy warp and one MMA warp per
-// group that is 16 warps (11 for two groups), four per SM sub-partition, which leaves each thread
-// 128 registers (a sub-partition holds 16384; 168 with two groups).
+// Dequant groups: three, except for INT4 at Mpad 32 (two: what tensor memory holds, below).  With
+// the copy warp and one MMA warp per group that is 16 warps (11 for two groups), four per SM
+// sub-partition, which leaves each thread 128 registers (a sub-partition holds 16384; 168 with
+// two groups).
 // The formats with one accumulator block per group (no dmin term, one scale group per
 // super-block).
 __host__ __device__ constexpr bool single_acc(int f) { return f == kFmtNVFP4 || f == kFmtQ6K; }
-__host__ __device__ constexpr int groups(int mpad, int f = kFmtQ4K) { return (mpad <= 16 || single_acc(f)) ? 3 : 2; }
+__host__ __device__ constexpr int groups(int mpad, int f = kFmtQ4K) { return (mpad <= 16 || f != kFmtINT4) ? 3 : 2; }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
@@ -159,16 +159,19 @@ constexpr int kMaxStages = 8;
 //   128 columns.  With 8 token columns (M <= 8) the min-term MMAs accumulate into columns 8..15
 //   of the product's own 16-column accumulator (their B_ext has the tokens in columns 8..15,
 //   the product's B zeros there); otherwise the min term has its own Mpad-column accumulator.
-//   With 16 token columns three such groups do not fit: there A_ext reuses the slot's first 16
-//   columns once the first K half's MMAs have completed, and each group has its own MMA warp
-//   (with one MMA warp for all groups, a group waiting for its first half's MMAs would hold up
-//   the other groups' MMAs, issued in order).
+//   With 16 or 32 token columns three such groups do not fit: there A_ext reuses the slot's
+//   first 16 columns once the first K half's MMAs have completed (their own commit), and each
+//   group has its own MMA warp (with one MMA warp for all groups, a group waiting for its first
+//   half's MMAs would hold up the other groups' MMAs, issued in order).  At 32 token columns the
+//   min term's accumulator also lives in the slot, in columns 16..47: the min-term MMAs are
+//   issued after that wait, so no MMA still reads those columns, and the group reads the
+//   accumulator before it writes the slot again.
 //   INT4: two accumulators (one per K half, its two scale groups); NVFP4, Q6K: one.
-//     Q4K, Q5K   8 tokens: 3 x (144 + 16) = 480;  16 tokens: 3 x (128 + 32) = 480;  Mpad 32: 2 x (144 + 64)
+//     Q4K, Q5K   8 tokens: 3 x (144 + 16) = 480;  16 tokens: 3 x (128 + 32) = 480;  Mpad 32: 3 x (128 + 32)
 //     INT4       3 x (128 + 32) = 480 at Mpad 16;  2 x (128 + 64) at Mpad 32
 //     NVFP4, Q6K 3 x (128 + Mpad): 432 / 480
-__host__ __device__ constexpr bool ext_in_a(int f, int mt) { return has_min(f) && mt == 16; }
-__host__ __device__ constexpr uint32_t acols(int f, int mt) { return (has_min(f) && mt != 16) ? 144u : 128u; }
+__host__ __device__ constexpr bool ext_in_a(int f, int mt) { return has_min(f) && mt >= 16; }
+__host__ __device__ constexpr uint32_t acols(int f, int mt) { return (has_min(f) && mt == 8) ? 144u : 128u; }
 // MMA-issuing warps: one per group.  (With one MMA warp serving the groups in order, its wait
 // for one group's handoff held up the MMAs of the others: measured on GB300 with clock stamps,
 // the groups then advanced one at a time.)
@@ -183,12 +186,14 @@ __host__ __device__ constexpr int cta_threads(int mpad, int f, int mt) {
 constexpr int kChunkSb = 4;
 __host__ __device__ constexpr uint32_t a_col(int g, int f, int mt) { return acols(f, mt) * g; }
 __host__ __device__ constexpr uint32_t acc_cols(int mpad, int f, int mt) {
-  return single_acc(f) ? mpad : ((has_min(f) && mt == 8) ? mpad : 2u * mpad);
+  return single_acc(f) ? mpad : ((has_min(f) && mt != 16) ? mpad : 2u * mpad);
 }
 __host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f, int mt) {
   return 512u - acc_cols(mpad, f, mt) * groups(mpad, f) + acc_cols(mpad, f, mt) * g;
 }
-__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f, int mt) { return acc1_col(mpad, g, f, mt) + mpad; }
+__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f, int mt) {
+  return (has_min(f) && mt == 32) ? a_col(g, f, mt) + 16u : acc1_col(mpad, g, f, mt) + mpad;
+}
 __host__ __device__ constexpr bool tmem_fits(int mpad, int f, int mt) {
   return a_col(groups(mpad, f), f, mt) <= acc1_col(mpad, 0, f, mt);
 }
@@ -221,7 +226,8 @@ __host__ __device__ constexpr int ytot_bytes(int mpad, int mt, int f = kFmtQ4K) 
 // that brought them is released before the epilogue needs them): 32 floats for each of the
 // two super-blocks in flight, per warp.
 constexpr int kSigBytes = kMaxGroups * kGroupWarps * 64 * 4;
-// Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens).
+// Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens, 4
+// for 32 with three groups' running sums in shared memory).
 __host__ __device__ constexpr int stages_fit(int mpad, int f, int mt) {
   return (kSmemLimit - ytot_bytes(mpad, mt, f) - kSigBytes - kNumBars * 8 - 32) / stage_bytes(mpad, f);
 }
@@ -245,7 +251,7 @@ constexpr bool smem_fits() {
 }
 static_assert(smem_fits<kFmtQ4K>() && smem_fits<kFmtQ5K>() && smem_fits<kFmtNVFP4>() && smem_fits<kFmtINT4>() &&
               smem_fits<kFmtQ6K>(), "shared memory");
-static_assert(stages(16, kFmtQ4K, 8) == 8 && stages(16, kFmtQ4K, 16) == 7 && stages(32, kFmtQ4K, 32) == 5 &&
+static_assert(stages(16, kFmtQ4K, 8) == 8 && stages(16, kFmtQ4K, 16) == 7 && stages(32, kFmtQ4K, 32) >= 4 &&
               stages(16, kFmtQ5K, 16) >= 4 && stages(32, kFmtQ5K, 32) >= 3 && stages(32, kFmtINT4, 32) >= 3 &&
               stages(16, kFmtQ6K, 16) >= 4 && stages(32, kFmtQ6K, 32) >= 3, "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
@@ -1817,13 +1823,13 @@ cudaError_t read_and_clear_tc_status(unsigned* out) {
 
 // Time model of a Q4K tensor-core launch over jobs[0 .. count), fitted to GB300 graph-replay
 // timings: a fixed ~6 us (two launches, pipeline fill and drain) and the busiest dequant group's
-// work (split_cost) at a full-CTA pace of 1.385 / 1.49 / 1.5 us per super-block of a tile for
-// M <= 8 / 16 / 32 (three groups, three, two).  A batched launch (no splits) counts its tasks
-// over all slots.
+// work (split_cost) at a full-CTA pace of 1.385 / 1.49 / 2.3 us per super-block of a tile for
+// M <= 8 / 16 / 32 (three groups each).  A batched launch (no splits) counts its tasks over all
+// slots.
 double tc_estimate_us(const Job* jobs, int count, int M) {
   const int sms = std::max(1, num_sms());
   const int ng = groups(M <= 16 ? 16 : 32);
-  const double pace_us = M <= 8 ? 1.385 : (M <= 16 ? 1.49 : 1.5);
+  const double pace_us = M <= 8 ? 1.385 : (M <= 16 ? 1.49 : 2.3);
   if (count == 1) return 6.0 + pace_us * split_cost(jobs[0].N, jobs[0].K, sms, ng, false).units;
   double tasks = 0, sbs = 0;
   for (int k = 0; k < count; ++k) {
