@@ -158,20 +158,20 @@ constexpr int kMaxStages = 8;
 //   k-quants (Q4K, Q5K) have the min-term MMAs: A_ext, 16 columns (K = 32), after the slot's
 //   128 columns.  With 8 token columns (M <= 8) the min-term MMAs accumulate into columns 8..15
 //   of the product's own 16-column accumulator (their B_ext has the tokens in columns 8..15,
-//   the product's B zeros there); otherwise the min term has its own Mpad-column accumulator.
-//   With 16 or 32 token columns three such groups do not fit: there A_ext reuses the slot's
-//   first 16 columns once the first K half's MMAs have completed (their own commit), and each
-//   group has its own MMA warp (with one MMA warp for all groups, a group waiting for its first
-//   half's MMAs would hold up the other groups' MMAs, issued in order).  At 32 token columns the
-//   min term's accumulator also lives in the slot, in columns 16..47: the min-term MMAs are
-//   issued after that wait, so no MMA still reads those columns, and the group reads the
-//   accumulator before it writes the slot again.
+//   the product's B zeros there).  With 16 or 32 token columns the min term's accumulator lives
+//   in the slot itself, in columns 16..15+Mpad: the min-term MMAs are issued only after the first
+//   K half's MMAs (the slot's readers of those columns) have completed (their own commit), and
+//   the group reads that accumulator before it writes the slot again.  With 32 token columns
+//   A_ext too reuses the slot's first 16 columns, written by the group after that same commit.
+//   Each group has its own MMA warp (with one MMA warp for all groups, a group waiting for its
+//   first half's MMAs would hold up the other groups' MMAs, issued in order).
 //   INT4: two accumulators (one per K half, its two scale groups); NVFP4, Q6K: one.
-//     Q4K, Q5K   8 tokens: 3 x (144 + 16) = 480;  16 tokens: 3 x (128 + 32) = 480;  Mpad 32: 3 x (128 + 32)
+//     Q4K, Q5K   8 tokens: 3 x (144 + 16) = 480;  16 tokens: 3 x (144 + 16) = 480;  Mpad 32: 3 x (128 + 32)
 //     INT4       3 x (128 + 32) = 480 at Mpad 16;  2 x (128 + 64) at Mpad 32
 //     NVFP4, Q6K 3 x (128 + Mpad): 432 / 480
-__host__ __device__ constexpr bool ext_in_a(int f, int mt) { return has_min(f) && mt >= 16; }
-__host__ __device__ constexpr uint32_t acols(int f, int mt) { return (has_min(f) && mt == 8) ? 144u : 128u; }
+__host__ __device__ constexpr bool ext_in_a(int f, int mt) { return has_min(f) && mt == 32; }
+__host__ __device__ constexpr bool acc_in_a(int f, int mt) { return has_min(f) && mt >= 16; }
+__host__ __device__ constexpr uint32_t acols(int f, int mt) { return (has_min(f) && mt <= 16) ? 144u : 128u; }
 // MMA-issuing warps: one per group.  (With one MMA warp serving the groups in order, its wait
 // for one group's handoff held up the MMAs of the others: measured on GB300 with clock stamps,
 // the groups then advanced one at a time.)
@@ -186,13 +186,13 @@ __host__ __device__ constexpr int cta_threads(int mpad, int f, int mt) {
 constexpr int kChunkSb = 4;
 __host__ __device__ constexpr uint32_t a_col(int g, int f, int mt) { return acols(f, mt) * g; }
 __host__ __device__ constexpr uint32_t acc_cols(int mpad, int f, int mt) {
-  return single_acc(f) ? mpad : ((has_min(f) && mt != 16) ? mpad : 2u * mpad);
+  return single_acc(f) ? mpad : (has_min(f) ? mpad : 2u * mpad);
 }
 __host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f, int mt) {
   return 512u - acc_cols(mpad, f, mt) * groups(mpad, f) + acc_cols(mpad, f, mt) * g;
 }
 __host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f, int mt) {
-  return (has_min(f) && mt == 32) ? a_col(g, f, mt) + 16u : acc1_col(mpad, g, f, mt) + mpad;
+  return acc_in_a(f, mt) ? a_col(g, f, mt) + 16u : acc1_col(mpad, g, f, mt) + mpad;
 }
 __host__ __device__ constexpr bool tmem_fits(int mpad, int f, int mt) {
   return a_col(groups(mpad, f), f, mt) <= acc1_col(mpad, 0, f, mt);
@@ -208,7 +208,8 @@ static_assert(tmem_fits(16, kFmtQ4K, 8) && tmem_fits(16, kFmtQ4K, 16) && tmem_fi
 //   WEmpty[s]    stage s consumed (the group's 4 warps + the MMA commit); copy lane
 //   AFull[g][h]  K half h of group g's A slot written; MMA lane
 //   H0Done[g]    the first K half's MMAs of group g's latest super-block completed; group g
-//                (only where A_ext reuses the first K half's columns)
+//                where A_ext reuses the first K half's columns (32 token columns), else the MMA
+//                lane before the min-term MMAs that write into those columns (16)
 //   GDone[g]     the MMAs of group g's latest super-block completed; group g
 //   Drain        the last MMAs of the CTA completed; MMA lane
 enum : int {
@@ -1084,7 +1085,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
         const uint32_t bslot = sW + ws * kSB + kWSB;
         const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
         tc::mma_f16_ts_x8(d1, abase, bdesc, 16, idesc, 0);
-        if constexpr (kExtInA) tc::commit(bar(kBarH0Done + g));   // the group may reuse these A columns
+        if constexpr (acc_in_a(FMT, MT)) tc::commit(bar(kBarH0Done + g));   // the group may reuse these A columns
         if (!wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u)) break;
         tc::fence_after_sync();
         if constexpr (FMT == kFmtINT4) {
@@ -1099,6 +1100,10 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
           constexpr bool kShiftExt = MT == 8;   // the min term in columns 8..15 of d1
           const uint64_t edesc = tc::smem_desc_kmajor(bslot + bext_off(MPAD), 128, 512);
           const uint32_t ea = abase + (kExtInA ? 0u : 128u);
+          if constexpr (acc_in_a(FMT, MT) && !kExtInA) {
+            if (!wait(bar(kBarH0Done + g), (uint32_t)i & 1u)) break;   // no MMA still reads d2's columns
+            tc::fence_after_sync();
+          }
           tc::mma_f16_ts(kShiftExt ? d1 : d2, ea, edesc, idesc, kShiftExt ? 1u : 0u);
           tc::mma_f16_ts(kShiftExt ? d1 : d2, ea + 8, edesc + 16, idesc, 1u);
         }
