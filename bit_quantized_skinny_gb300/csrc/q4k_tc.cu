@@ -103,14 +103,20 @@ __device__ unsigned g_status;   // this file's kernels' status word
 constexpr int kTileRows = 128;
 constexpr int kGroupWarps = 4;     // a dequant group: one warp per TMEM lane quarter (32 rows)
 constexpr int kMaxGroups = 3;
-// Dequant groups: three, except for INT4 at Mpad 32 (two: what tensor memory holds, below).  With
-// the copy warp and one MMA warp per group that is 16 warps (11 for two groups), four per SM
-// sub-partition, which leaves each thread 128 registers (a sub-partition holds 16384; 168 with
-// two groups).
 // The formats with one accumulator block per group (no dmin term, one scale group per
 // super-block).
 __host__ __device__ constexpr bool single_acc(int f) { return f == kFmtNVFP4 || f == kFmtQ6K; }
-__host__ __device__ constexpr int groups(int mpad, int f = kFmtQ4K) { return (mpad <= 16 || f != kFmtINT4) ? 3 : 2; }
+__host__ __device__ constexpr bool has_min(int f) { return f == kFmtQ4K || f == kFmtQ5K; }
+// Dequant groups (NG): three at Mpad 16 and for NVFP4 and Q6K at Mpad 32; two for INT4 at Mpad 32
+// (what tensor memory holds, below); two or three for the k-quants at Mpad 32, chosen per launch
+// (`wide`): three stream long task lists faster, two (with more stages: the running sums of
+// fewer groups leave more shared memory) finish short, split products sooner.  With the copy
+// warp and one MMA warp per group that is 16 warps (11 for two groups), four per SM
+// sub-partition, which leaves each thread 128 registers (a sub-partition holds 16384; 168 with
+// two groups).
+__host__ __device__ constexpr int groups(int mpad, int f = kFmtQ4K, bool wide = true) {
+  return (mpad <= 16 || single_acc(f)) ? 3 : ((has_min(f) && wide) ? 3 : 2);
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 17;
 constexpr int kMaxEBatch = 160;    // products per batched launch (their tensor maps ride in the parameters)
@@ -124,7 +130,6 @@ constexpr int kSmemLimit = 232448; // shared memory per CTA (227 KB)
 __host__ __device__ constexpr int blk_bytes(int f) {
   return f == kFmtQ5K ? 176 : (f == kFmtQ6K ? 208 : (f == kFmtINT4 ? 128 : 144));
 }
-__host__ __device__ constexpr bool has_min(int f) { return f == kFmtQ4K || f == kFmtQ5K; }
 __host__ __device__ constexpr int w_stage_bytes(int f) { return kTileRows * blk_bytes(f); }
 
 // Prepared activation block of one super-block (bblock_bytes(MPAD) bytes, written by the
@@ -169,38 +174,35 @@ constexpr int kMaxStages = 8;
 //     Q4K, Q5K   8 tokens: 3 x (144 + 16) = 480;  16 tokens: 3 x (144 + 16) = 480;  Mpad 32: 3 x (128 + 32)
 //     INT4       3 x (128 + 32) = 480 at Mpad 16;  2 x (128 + 64) at Mpad 32
 //     NVFP4, Q6K 3 x (128 + Mpad): 432 / 480
-__host__ __device__ constexpr bool ext_in_a(int f, int mt) { return has_min(f) && mt == 32; }
-__host__ __device__ constexpr bool acc_in_a(int f, int mt) { return has_min(f) && mt >= 16; }
-__host__ __device__ constexpr uint32_t acols(int f, int mt) { return (has_min(f) && mt <= 16) ? 144u : 128u; }
+__host__ __device__ constexpr bool ext_in_a(int f, int mt, int ng) { return has_min(f) && mt == 32 && ng == 3; }
+__host__ __device__ constexpr bool acc_in_a(int f, int mt, int ng) { return has_min(f) && (mt == 16 || (mt == 32 && ng == 3)); }
+__host__ __device__ constexpr uint32_t acols(int f, int mt, int ng) { return (has_min(f) && !ext_in_a(f, mt, ng)) ? 144u : 128u; }
 // MMA-issuing warps: one per group.  (With one MMA warp serving the groups in order, its wait
 // for one group's handoff held up the MMAs of the others: measured on GB300 with clock stamps,
 // the groups then advanced one at a time.)
-__host__ __device__ constexpr int mma_warps(int mpad, int f, int mt) { return groups(mpad, f) + 0 * mt; }
-// Threads of a CTA: the dequant groups, the copy warp and the MMA warp(s).
-__host__ __device__ constexpr int cta_threads(int mpad, int f, int mt) {
-  return 32 * (groups(mpad, f) * kGroupWarps + 1 + mma_warps(mpad, f, mt));
-}
+// Threads of a CTA: the dequant groups, the copy warp and one MMA warp per group.
+__host__ __device__ constexpr int cta_threads(int ng) { return 32 * (ng * kGroupWarps + 1 + ng); }
 // Summation order of a product: the super-blocks of a row are summed in chunks of kChunkSb (each
 // chunk from zero, in order of k), and the chunk sums are then added in chunk order.  A K split
 // only ever cuts at chunk boundaries, so the bits of a product do not depend on the split.
 constexpr int kChunkSb = 4;
-__host__ __device__ constexpr uint32_t a_col(int g, int f, int mt) { return acols(f, mt) * g; }
-__host__ __device__ constexpr uint32_t acc_cols(int mpad, int f, int mt) {
-  return single_acc(f) ? mpad : (has_min(f) ? mpad : 2u * mpad);
+__host__ __device__ constexpr uint32_t a_col(int g, int f, int mt, int ng) { return acols(f, mt, ng) * g; }
+__host__ __device__ constexpr uint32_t acc_cols(int mpad, int f, int mt, int ng) {
+  return single_acc(f) ? mpad : ((has_min(f) && (mt == 8 || acc_in_a(f, mt, ng))) ? mpad : 2u * mpad);
 }
-__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f, int mt) {
-  return 512u - acc_cols(mpad, f, mt) * groups(mpad, f) + acc_cols(mpad, f, mt) * g;
+__host__ __device__ constexpr uint32_t acc1_col(int mpad, int g, int f, int mt, int ng) {
+  return 512u - acc_cols(mpad, f, mt, ng) * ng + acc_cols(mpad, f, mt, ng) * g;
 }
-__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f, int mt) {
-  return acc_in_a(f, mt) ? a_col(g, f, mt) + 16u : acc1_col(mpad, g, f, mt) + mpad;
+__host__ __device__ constexpr uint32_t acc2_col(int mpad, int g, int f, int mt, int ng) {
+  return acc_in_a(f, mt, ng) ? a_col(g, f, mt, ng) + 16u : acc1_col(mpad, g, f, mt, ng) + mpad;
 }
-__host__ __device__ constexpr bool tmem_fits(int mpad, int f, int mt) {
-  return a_col(groups(mpad, f), f, mt) <= acc1_col(mpad, 0, f, mt);
+__host__ __device__ constexpr bool tmem_fits(int mpad, int f, int mt, int ng) {
+  return a_col(ng, f, mt, ng) <= acc1_col(mpad, 0, f, mt, ng);
 }
-static_assert(tmem_fits(16, kFmtQ4K, 8) && tmem_fits(16, kFmtQ4K, 16) && tmem_fits(32, kFmtQ4K, 32) &&
-              tmem_fits(16, kFmtINT4, 8) && tmem_fits(16, kFmtINT4, 16) && tmem_fits(32, kFmtINT4, 32) &&
-              tmem_fits(16, kFmtNVFP4, 16) && tmem_fits(32, kFmtNVFP4, 32) && tmem_fits(32, kFmtQ6K, 32),
-              "TMEM column plan overlaps");
+static_assert(tmem_fits(16, kFmtQ4K, 8, 3) && tmem_fits(16, kFmtQ4K, 16, 3) && tmem_fits(32, kFmtQ4K, 32, 3) &&
+              tmem_fits(32, kFmtQ4K, 32, 2) && tmem_fits(16, kFmtINT4, 8, 3) && tmem_fits(16, kFmtINT4, 16, 3) &&
+              tmem_fits(32, kFmtINT4, 32, 2) && tmem_fits(16, kFmtNVFP4, 16, 3) && tmem_fits(32, kFmtNVFP4, 32, 3) &&
+              tmem_fits(32, kFmtQ6K, 32, 3), "TMEM column plan overlaps");
 
 // Barrier indices inside the barrier block.  Every barrier is waited on by threads that see
 // all of its phases in order (a parity wait is only exact then):
@@ -222,39 +224,41 @@ enum : int {
 // With 16 or 32 token columns each group's running sum of chunk sums (MT tokens x 128 rows of
 // fp32) lives in shared memory, not in registers (there it spilled); it is touched once per
 // chunk of 4 super-blocks.
-__host__ __device__ constexpr int ytot_bytes(int mpad, int mt, int f = kFmtQ4K) { return mt >= 16 ? groups(mpad, f) * mt * kTileRows * 4 : 0; }
+__host__ __device__ constexpr int ytot_bytes(int mt, int ng) { return mt >= 16 ? ng * mt * kTileRows * 4 : 0; }
 // Each dequant warp keeps its own copy of the current super-block's per-token scales (the stage
 // that brought them is released before the epilogue needs them): 32 floats for each of the
 // two super-blocks in flight, per warp.
 constexpr int kSigBytes = kMaxGroups * kGroupWarps * 64 * 4;
 // Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens, 4
 // for 32 with three groups' running sums in shared memory).
-__host__ __device__ constexpr int stages_fit(int mpad, int f, int mt) {
-  return (kSmemLimit - ytot_bytes(mpad, mt, f) - kSigBytes - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+__host__ __device__ constexpr int stages_fit(int mpad, int f, int mt, int ng) {
+  return (kSmemLimit - ytot_bytes(mt, ng) - kSigBytes - kNumBars * 8 - 32) / stage_bytes(mpad, f);
 }
-__host__ __device__ constexpr int stages(int mpad, int f, int mt) {
-  return stages_fit(mpad, f, mt) < (mpad <= 16 ? 8 : 5) ? stages_fit(mpad, f, mt) : (mpad <= 16 ? 8 : 5);
+__host__ __device__ constexpr int stages(int mpad, int f, int mt, int ng) {
+  return stages_fit(mpad, f, mt, ng) < (mpad <= 16 ? 8 : 5) ? stages_fit(mpad, f, mt, ng) : (mpad <= 16 ? 8 : 5);
 }
 
-template <int MPAD, int FMT, int MT>
+template <int MPAD, int FMT, int MT, int NG>
 struct TcSmem {
   static constexpr int kW = 0;
-  static constexpr int kYtot = kW + stages(MPAD, FMT, MT) * stage_bytes(MPAD, FMT);
-  static constexpr int kSig = kYtot + ytot_bytes(MPAD, MT, FMT);
+  static constexpr int kYtot = kW + stages(MPAD, FMT, MT, NG) * stage_bytes(MPAD, FMT);
+  static constexpr int kSig = kYtot + ytot_bytes(MT, NG);
   static constexpr int kBars = kSig + kSigBytes;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 32;   // TMEM address, abort flag, super-blocks per group (<= 4)
 };
 template <int FMT>
 constexpr bool smem_fits() {
-  return TcSmem<16, FMT, 8>::kTotal <= kSmemLimit && TcSmem<16, FMT, 16>::kTotal <= kSmemLimit &&
-         TcSmem<32, FMT, 32>::kTotal <= kSmemLimit;
+  return TcSmem<16, FMT, 8, 3>::kTotal <= kSmemLimit && TcSmem<16, FMT, 16, 3>::kTotal <= kSmemLimit &&
+         TcSmem<32, FMT, 32, groups(32, FMT, false)>::kTotal <= kSmemLimit &&
+         TcSmem<32, FMT, 32, groups(32, FMT, true)>::kTotal <= kSmemLimit;
 }
 static_assert(smem_fits<kFmtQ4K>() && smem_fits<kFmtQ5K>() && smem_fits<kFmtNVFP4>() && smem_fits<kFmtINT4>() &&
               smem_fits<kFmtQ6K>(), "shared memory");
-static_assert(stages(16, kFmtQ4K, 8) == 8 && stages(16, kFmtQ4K, 16) == 7 && stages(32, kFmtQ4K, 32) >= 4 &&
-              stages(16, kFmtQ5K, 16) >= 4 && stages(32, kFmtQ5K, 32) >= 3 && stages(32, kFmtINT4, 32) >= 3 &&
-              stages(16, kFmtQ6K, 16) >= 4 && stages(32, kFmtQ6K, 32) >= 3, "stage counts");
+static_assert(stages(16, kFmtQ4K, 8, 3) == 8 && stages(16, kFmtQ4K, 16, 3) == 7 && stages(32, kFmtQ4K, 32, 3) == 4 &&
+              stages(32, kFmtQ4K, 32, 2) == 5 && stages(16, kFmtQ5K, 16, 3) >= 4 && stages(32, kFmtQ5K, 32, 3) >= 3 &&
+              stages(32, kFmtINT4, 32, 2) >= 3 && stages(16, kFmtQ6K, 16, 3) >= 4 && stages(32, kFmtQ6K, 32, 3) >= 3,
+              "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
 static_assert(stage_bytes(16, kFmtQ4K) % 128 == 0 && stage_bytes(32, kFmtQ5K) % 128 == 0 &&
               stage_bytes(16, kFmtINT4) % 1024 == 0 && w_stage_bytes(kFmtQ5K) % 128 == 0 &&
@@ -929,22 +933,22 @@ __device__ __noinline__ void hard_dot(uint32_t rb, uint32_t xblk, const void* au
 // MT: the token columns the epilogue reads and sums (8 when M <= 8, else MPAD); columns past M
 // hold zeros.  GATED: the feed-forward gating in the epilogue (a separate instance: its code in
 // the regular kernels measured 2.5 % slower at M <= 8).
-template <int FMT, int MPAD, int MT, int MAXE, bool GATED>
-__global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
+template <int FMT, int MPAD, int MT, int MAXE, bool GATED, int NG>
+__global__ void __launch_bounds__(cta_threads(NG), 1)
     q4k_tc_kernel(const __grid_constant__ TcParams<MAXE, naux(FMT, MAXE)> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
-  using L = TcSmem<MPAD, FMT, MT>;
-  constexpr int NG = groups(MPAD, FMT);
+  using L = TcSmem<MPAD, FMT, MT, NG>;
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
   constexpr int kMmaWarp = kProdWarp + 1;       // (first) MMA issue warp; owns TMEM
-  constexpr int kMmaWarps = mma_warps(MPAD, FMT, MT);
+  constexpr int kMmaWarps = NG;                 // one MMA warp per group
   constexpr int kBB = bblock_bytes(MPAD);
-  constexpr int kS = stages(MPAD, FMT, MT);
+  constexpr int kS = stages(MPAD, FMT, MT, NG);
   constexpr int kSB = stage_bytes(MPAD, FMT);
   constexpr int kBlk = blk_bytes(FMT);
   constexpr int kWSB = w_stage_bytes(FMT);
-  constexpr bool kExtInA = ext_in_a(FMT, MT);
+  constexpr bool kExtInA = ext_in_a(FMT, MT, NG);
+  constexpr bool kAccInA = acc_in_a(FMT, MT, NG);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t sW = smem_addr(smem + L::kW);   // stage k: weights at sW + k*kSB, activations kWSB further
@@ -1073,9 +1077,9 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
       int ngl = 0;
 #pragma unroll
       for (int h = 0; h < NG; ++h) if (h == g) ngl = n[h];
-      const uint32_t abase = tmem + a_col(g, FMT, MT);
-      const uint32_t d1 = tmem + acc1_col(MPAD, g, FMT, MT);
-      const uint32_t d2 = tmem + acc2_col(MPAD, g, FMT, MT);
+      const uint32_t abase = tmem + a_col(g, FMT, MT, NG);
+      const uint32_t d1 = tmem + acc1_col(MPAD, g, FMT, MT, NG);
+      const uint32_t d2 = tmem + acc2_col(MPAD, g, FMT, MT, NG);
       uint32_t gbits = 0;   // parity of this group's full barrier of each stage
       for (int i = 0; i < ngl; ++i) {
         const uint32_t ws = su_of<NG>(n, g, i, nmin) % kS;
@@ -1085,7 +1089,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
         const uint32_t bslot = sW + ws * kSB + kWSB;
         const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
         tc::mma_f16_ts_x8(d1, abase, bdesc, 16, idesc, 0);
-        if constexpr (acc_in_a(FMT, MT)) tc::commit(bar(kBarH0Done + g));   // the group may reuse these A columns
+        if constexpr (kAccInA) tc::commit(bar(kBarH0Done + g));   // the group may reuse these A columns
         if (!wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u)) break;
         tc::fence_after_sync();
         if constexpr (FMT == kFmtINT4) {
@@ -1100,7 +1104,7 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
           constexpr bool kShiftExt = MT == 8;   // the min term in columns 8..15 of d1
           const uint64_t edesc = tc::smem_desc_kmajor(bslot + bext_off(MPAD), 128, 512);
           const uint32_t ea = abase + (kExtInA ? 0u : 128u);
-          if constexpr (acc_in_a(FMT, MT) && !kExtInA) {
+          if constexpr (kAccInA && !kExtInA) {
             if (!wait(bar(kBarH0Done + g), (uint32_t)i & 1u)) break;   // no MMA still reads d2's columns
             tc::fence_after_sync();
           }
@@ -1141,10 +1145,10 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
     for (int k = 0; k < (kYtotSmem ? 1 : MT); ++k) ytot_r[k] = 0.f;
     auto ytot = [&](int k) -> float& { if constexpr (kYtotSmem) return ytot_s[k * kTileRows]; else return ytot_r[k]; };
 
-    const uint32_t aslot = tl + a_col(grp, FMT, MT);           // this group's A slot (this warp's lanes)
+    const uint32_t aslot = tl + a_col(grp, FMT, MT, NG);       // this group's A slot (this warp's lanes)
     const uint32_t aext = aslot + (kExtInA ? 0u : 128u);         // its min-term columns
-    const uint32_t acc1 = tl + acc1_col(MPAD, grp, FMT, MT);    // and accumulators
-    const uint32_t acc2 = tl + acc2_col(MPAD, grp, FMT, MT);
+    const uint32_t acc1 = tl + acc1_col(MPAD, grp, FMT, MT, NG);    // and accumulators
+    const uint32_t acc2 = tl + acc2_col(MPAD, grp, FMT, MT, NG);
     // this warp's copies of the per-token scales of two super-blocks in flight (by parity)
     float* sigw = reinterpret_cast<float*>(smem + L::kSig) + warp * 64;
     float hard_sum[MT];   // the hard tokens' sums of the super-block being finished (rarely used)
@@ -1217,10 +1221,22 @@ __global__ void __launch_bounds__(cta_threads(MPAD, FMT, MT), 1)
           for (int k = 0; k < kW; k += 4) {
             const float4 sg = *reinterpret_cast<const float4*>(sg_i + c0 + k);
             const float sgk[4] = {sg.x, sg.y, sg.z, sg.w};
+            // two tokens per f32x2 operation: y += sigma (sx a1 + sy a2), each step rounded as
+            // its scalar form
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if constexpr (kTwo) y[c0 + k + u] = fmaf(sgk[u], fmaf(sx, a1[k + u], sy * a2[k + u]), y[c0 + k + u]);
-              else y[c0 + k + u] = fmaf(sx * sgk[u], a1[k + u], y[c0 + k + u]);
+            for (int u = 0; u < 4; u += 2) {
+              const float2 yy = make_float2(y[c0 + k + u], y[c0 + k + u + 1]);
+              float2 r;
+              if constexpr (kTwo) {
+                const float2 t = __ffma2_rn(make_float2(sx, sx), make_float2(a1[k + u], a1[k + u + 1]),
+                                            __fmul2_rn(make_float2(sy, sy), make_float2(a2[k + u], a2[k + u + 1])));
+                r = __ffma2_rn(make_float2(sgk[u], sgk[u + 1]), t, yy);
+              } else {
+                r = __ffma2_rn(__fmul2_rn(make_float2(sx, sx), make_float2(sgk[u], sgk[u + 1])),
+                               make_float2(a1[k + u], a1[k + u + 1]), yy);
+              }
+              y[c0 + k + u] = r.x;
+              y[c0 + k + u + 1] = r.y;
             }
           }
         }
@@ -1517,17 +1533,34 @@ cudaError_t weight_map(const void* W, int64_t N, int64_t K, int fmt, CUtensorMap
   return cudaSuccess;
 }
 
-template <int FMT, int MPAD, int MT, int MAXE, bool GATED>
+template <int FMT, int MPAD, int MT, int MAXE, bool GATED, int NG>
 cudaError_t set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(q4k_tc_kernel<FMT, MPAD, MT, MAXE, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcSmem<MPAD, FMT, MT>::kTotal);
+  err = cudaFuncSetAttribute(q4k_tc_kernel<FMT, MPAD, MT, MAXE, GATED, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TcSmem<MPAD, FMT, MT, NG>::kTotal);
   if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return err;
+}
+
+// One instance of the kernel: its shared memory attribute, block size and launch.
+template <int FMT, int MPAD, int MT, int MAXE, bool GATED, int NG, class PT>
+cudaError_t launch_instance(cudaLaunchConfig_t& cfg, const PT& par) {
+  cudaError_t err = set_smem_attr<FMT, MPAD, MT, MAXE, GATED, NG>();
+  if (err != cudaSuccess) return err;
+  cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MT, NG>::kTotal;
+  cfg.blockDim = dim3(cta_threads(NG));
+  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MT, MAXE, GATED, NG>, par);
+}
+
+// Tensor-core launches over these products run the k-quants' three-group instance at 32 token
+// columns when their tasks keep every group busy: a batched launch, or a product with at least
+// three 128-row tiles per SM.
+bool wide_launch(const Job* jobs, int count, int sms) {
+  return count > 1 || (jobs[0].N + kTileRows - 1) / kTileRows >= 3 * (int64_t)sms;
 }
 
 // K split of a product: the number of splits of every 128-row tile and the super-blocks per
@@ -1601,7 +1634,7 @@ SplitSpace split_space(int64_t N, int64_t K, const Split& s) {
 // static block under the caller's lock.
 template <int FMT, int MPAD, int MAXE>
 cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split* sp, float* const* part,
-                        unsigned* const* ctr, int count, int M, cudaStream_t stream) {
+                        unsigned* const* ctr, int count, int M, bool wide, cudaStream_t stream) {
   static TcParams<MAXE, naux(FMT, MAXE)> par;
   par.count = count;
   par.M = M;
@@ -1633,37 +1666,24 @@ cudaError_t launch_main(const Job* jobs, const uint8_t* const* bsrc, const Split
   if constexpr (FMT == kFmtQ4K && MAXE == 1) {
     if (par.gated) {   // one product split into no tasks along K (split_for with whole rows)
       if constexpr (MPAD == 16) {
-        if (M <= 8) {
-          cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE, true>();
-          if (err != cudaSuccess) return err;
-          cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
-          cfg.blockDim = dim3(cta_threads(MPAD, FMT, 8));
-          return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE, true>, par);
-        }
+        if (M <= 8) return launch_instance<FMT, MPAD, 8, MAXE, true, 3>(cfg, par);
+        return launch_instance<FMT, MPAD, 16, MAXE, true, 3>(cfg, par);
+      } else {
+        return launch_instance<FMT, MPAD, MPAD, MAXE, true, groups(MPAD, FMT, false)>(cfg, par);
       }
-      cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE, true>();
-      if (err != cudaSuccess) return err;
-      cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
-      cfg.blockDim = dim3(cta_threads(MPAD, FMT, MPAD));
-      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE, true>, par);
     }
   } else {
     if (par.gated) return cudaErrorNotSupported;   // the gated epilogue is Q4K's, single products
   }
   if constexpr (MPAD == 16) {
-    if (M <= 8) {
-      cudaError_t err = set_smem_attr<FMT, MPAD, 8, MAXE, false>();
-      if (err != cudaSuccess) return err;
-      cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, 8>::kTotal;
-      cfg.blockDim = dim3(cta_threads(MPAD, FMT, 8));
-      return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, 8, MAXE, false>, par);
-    }
+    if (M <= 8) return launch_instance<FMT, MPAD, 8, MAXE, false, 3>(cfg, par);
+    return launch_instance<FMT, MPAD, 16, MAXE, false, 3>(cfg, par);
+  } else if constexpr (MAXE > 1 || groups(MPAD, FMT, true) == groups(MPAD, FMT, false)) {
+    return launch_instance<FMT, MPAD, MPAD, MAXE, false, groups(MPAD, FMT, true)>(cfg, par);   // batched: wide
+  } else {
+    if (wide) return launch_instance<FMT, MPAD, MPAD, MAXE, false, groups(MPAD, FMT, true)>(cfg, par);
+    return launch_instance<FMT, MPAD, MPAD, MAXE, false, groups(MPAD, FMT, false)>(cfg, par);
   }
-  cudaError_t err = set_smem_attr<FMT, MPAD, MPAD, MAXE, false>();
-  if (err != cudaSuccess) return err;
-  cfg.dynamicSmemBytes = TcSmem<MPAD, FMT, MPAD>::kTotal;
-  cfg.blockDim = dim3(cta_threads(MPAD, FMT, MPAD));
-  return cudaLaunchKernelEx(&cfg, q4k_tc_kernel<FMT, MPAD, MPAD, MAXE, false>, par);
 }
 
 template <int MPAD, int NX, bool NAT>
@@ -1719,7 +1739,9 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
   std::lock_guard<std::mutex> g(mu);
   cudaError_t err = launch_prep<MPAD, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream);
   if (err != cudaSuccess) return err;
-  if (count == 1) return launch_main<FMT, MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M, stream);
+  if (count == 1)
+    return launch_main<FMT, MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M,
+                                     wide_launch(jobs, 1, num_sms()), stream);
   // Launches of near-equal size, each with its products ordered by decreasing K (the kernel deals
   // tasks back and forth over its slots: large tasks first, then the small ones even them out).
   const int launches = (count + kMaxEBatch - 1) / kMaxEBatch;
@@ -1742,7 +1764,7 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
       pc[k] = ctr[ord[k]];
     }
     err = launch_main<FMT, MPAD, kMaxEBatch>(pj.data() + k0, pb.data() + k0, ps.data() + k0, pp.data() + k0,
-                                             pc.data() + k0, n, M, stream);
+                                             pc.data() + k0, n, M, true, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
@@ -1773,7 +1795,8 @@ cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) 
   std::vector<Split> sp(count);
   size_t split_bytes = 0, zero_words = 0;
   for (int k = 0; k < count; ++k) {
-    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, groups(MPAD, FMT), count > 1 || jobs[k].gated);   // gating needs whole rows
+    sp[k] = split_for(jobs[k].N, jobs[k].K, sms, groups(MPAD, FMT, wide_launch(jobs, count, sms) && !jobs[k].gated),
+                      count > 1 || jobs[k].gated);   // gating needs whole rows
     const SplitSpace s = split_space<MPAD>(jobs[k].N, jobs[k].K, sp[k]);
     split_bytes += s.partial_bytes;
     zero_words += s.counter_words;
@@ -1828,13 +1851,13 @@ cudaError_t read_and_clear_tc_status(unsigned* out) {
 
 // Time model of a Q4K tensor-core launch over jobs[0 .. count), fitted to GB300 graph-replay
 // timings: a fixed ~6 us (two launches, pipeline fill and drain) and the busiest dequant group's
-// work (split_cost) at a full-CTA pace of 1.385 / 1.49 / 2.3 us per super-block of a tile for
-// M <= 8 / 16 / 32 (three groups each).  A batched launch (no splits) counts its tasks over all
-// slots.
+// work (split_cost) at a full-CTA pace of 1.385 / 1.49 us per super-block of a tile for M <= 8 / 16
+// (three groups) and 2.3 / 1.58 us for M <= 32 with three / two groups.  A batched launch (no
+// splits) counts its tasks over all slots.
 double tc_estimate_us(const Job* jobs, int count, int M) {
   const int sms = std::max(1, num_sms());
-  const int ng = groups(M <= 16 ? 16 : 32);
-  const double pace_us = M <= 8 ? 1.385 : (M <= 16 ? 1.49 : 2.3);
+  const int ng = groups(M <= 16 ? 16 : 32, kFmtQ4K, wide_launch(jobs, count, sms));
+  const double pace_us = M <= 8 ? 1.385 : (M <= 16 ? 1.49 : (ng == 3 ? 2.3 : 1.58));
   if (count == 1) return 6.0 + pace_us * split_cost(jobs[0].N, jobs[0].K, sms, ng, false).units;
   double tasks = 0, sbs = 0;
   for (int k = 0; k < count; ++k) {
