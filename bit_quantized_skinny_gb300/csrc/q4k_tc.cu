@@ -132,8 +132,11 @@ __host__ __device__ constexpr int blk_bytes(int f) {
 }
 __host__ __device__ constexpr int w_stage_bytes(int f) { return kTileRows * blk_bytes(f); }
 
-// Prepared activation block of one super-block (bblock_bytes(MPAD) bytes, written by the
-// preparation kernel, read by the product kernel from a stage of its ring):
+// Prepared activation block of one super-block (bblock_bytes(TW) bytes, written by the
+// preparation kernel, read by the product kernel from a stage of its ring).  TW, the token
+// columns it stores, is MPAD, except for the 8-token kernels (M <= 8), whose MMAs (N = 16) take
+// token columns 8..15 of B and 0..7 of B_ext from zero regions of shared memory: their blocks
+// hold 8 columns (TW = 8, half the bytes of every copy).  With MPAD read as TW:
 //   [0, MPAD*512)         B: the 256 activations of every token column i as fp16 x * 2^-s_i,
 //                         K-major core matrices (8 tokens x 8 k, 128 bytes; 32 of them along k
 //                         per group of 8 tokens: 4096 bytes)
@@ -157,7 +160,7 @@ __host__ __device__ constexpr int stage_bytes(int mpad, int f) {
   return f == kFmtINT4 ? (w_stage_bytes(f) + bblock_bytes(mpad) + 1023) / 1024 * 1024
                        : (w_stage_bytes(f) + bblock_bytes(mpad) + 127) / 128 * 128;
 }
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 9;
 // TMEM columns.  Each group owns one A slot (one super-block: 64 columns of fp16 pairs per K
 // half) and one accumulator block at the top of the 512 columns.
 //   k-quants (Q4K, Q5K) have the min-term MMAs: A_ext, 16 columns (K = 32), after the slot's
@@ -221,6 +224,14 @@ enum : int {
   kNumBars = kBarDrain + kMaxGroups
 };
 
+// The 8-token kernels keep two zero regions: 1024 bytes before the stages (token columns 0..7 of
+// the min-term operand B_ext; 1024 keeps the stages 1024-byte aligned) and 4096 bytes after them
+// (token columns 8..15 of B).  An MMA's B descriptor reaches the second group of 8 token columns
+// at its start + SBO, so a stage's descriptor points there with SBO = zero region - stage
+// (forwards for B) or starts in the zero region with SBO = stage - zero region (B_ext).
+constexpr int kZeroExtBytes = 1024;
+constexpr int kZeroMainBytes = 4096;
+__host__ __device__ constexpr int token_width(int mpad, int mt) { return mt == 8 ? 8 : mpad; }
 // With 16 or 32 token columns each group's running sum of chunk sums (MT tokens x 128 rows of
 // fp32) lives in shared memory, not in registers (there it spilled); it is touched once per
 // chunk of 4 super-blocks.
@@ -229,19 +240,24 @@ __host__ __device__ constexpr int ytot_bytes(int mt, int ng) { return mt >= 16 ?
 // that brought them is released before the epilogue needs them): 32 floats for each of the
 // two super-blocks in flight, per warp.
 constexpr int kSigBytes = kMaxGroups * kGroupWarps * 64 * 4;
-// Stages: 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7 for 16 tokens, 4
-// for 32 with three groups' running sums in shared memory).
+// Stages: 9 for 8 tokens, 8 at Mpad 16 and 5 at Mpad 32, or as many as fit beside the rest (7
+// for 16 tokens, 4 for 32 with three groups' running sums in shared memory).
+__host__ __device__ constexpr int zero_bytes(int mt) { return mt == 8 ? kZeroExtBytes + kZeroMainBytes : 0; }
 __host__ __device__ constexpr int stages_fit(int mpad, int f, int mt, int ng) {
-  return (kSmemLimit - ytot_bytes(mt, ng) - kSigBytes - kNumBars * 8 - 32) / stage_bytes(mpad, f);
+  return (kSmemLimit - zero_bytes(mt) - ytot_bytes(mt, ng) - kSigBytes - kNumBars * 8 - 32) /
+         stage_bytes(token_width(mpad, mt), f);
 }
+__host__ __device__ constexpr int stage_cap(int mpad, int mt) { return mt == 8 ? 9 : (mpad <= 16 ? 8 : 5); }
 __host__ __device__ constexpr int stages(int mpad, int f, int mt, int ng) {
-  return stages_fit(mpad, f, mt, ng) < (mpad <= 16 ? 8 : 5) ? stages_fit(mpad, f, mt, ng) : (mpad <= 16 ? 8 : 5);
+  return stages_fit(mpad, f, mt, ng) < stage_cap(mpad, mt) ? stages_fit(mpad, f, mt, ng) : stage_cap(mpad, mt);
 }
 
 template <int MPAD, int FMT, int MT, int NG>
 struct TcSmem {
-  static constexpr int kW = 0;
-  static constexpr int kYtot = kW + stages(MPAD, FMT, MT, NG) * stage_bytes(MPAD, FMT);
+  static constexpr int kZeroExt = 0;                                   // 8 tokens only
+  static constexpr int kW = MT == 8 ? kZeroExtBytes : 0;
+  static constexpr int kZeroMain = kW + stages(MPAD, FMT, MT, NG) * stage_bytes(token_width(MPAD, MT), FMT);
+  static constexpr int kYtot = kZeroMain + (MT == 8 ? kZeroMainBytes : 0);
   static constexpr int kSig = kYtot + ytot_bytes(MT, NG);
   static constexpr int kBars = kSig + kSigBytes;
   static constexpr int kMisc = kBars + kNumBars * 8;
@@ -255,14 +271,15 @@ constexpr bool smem_fits() {
 }
 static_assert(smem_fits<kFmtQ4K>() && smem_fits<kFmtQ5K>() && smem_fits<kFmtNVFP4>() && smem_fits<kFmtINT4>() &&
               smem_fits<kFmtQ6K>(), "shared memory");
-static_assert(stages(16, kFmtQ4K, 8, 3) == 8 && stages(16, kFmtQ4K, 16, 3) == 7 && stages(32, kFmtQ4K, 32, 3) == 4 &&
+static_assert(stages(16, kFmtQ4K, 8, 3) == 9 && stages(16, kFmtQ4K, 16, 3) == 7 && stages(32, kFmtQ4K, 32, 3) == 4 &&
               stages(32, kFmtQ4K, 32, 2) == 5 && stages(16, kFmtQ5K, 16, 3) >= 4 && stages(32, kFmtQ5K, 32, 3) >= 3 &&
               stages(32, kFmtINT4, 32, 2) >= 3 && stages(16, kFmtQ6K, 16, 3) >= 4 && stages(32, kFmtQ6K, 32, 3) >= 3,
               "stage counts");
 static_assert(groups(16) <= kMaxGroups && groups(32) <= kMaxGroups, "group barriers");
 static_assert(stage_bytes(16, kFmtQ4K) % 128 == 0 && stage_bytes(32, kFmtQ5K) % 128 == 0 &&
               stage_bytes(16, kFmtINT4) % 1024 == 0 && w_stage_bytes(kFmtQ5K) % 128 == 0 &&
-              bblock_bytes(16) % 16 == 0 && bblock_bytes(32) % 16 == 0, "stage alignment");
+              bblock_bytes(8) % 16 == 0 && bblock_bytes(16) % 16 == 0 && bblock_bytes(32) % 16 == 0 &&
+              stage_bytes(8, kFmtQ4K) % 128 == 0 && stage_bytes(8, kFmtINT4) % 1024 == 0, "stage alignment");
 
 struct TcEntry {
   float* Y;
@@ -310,7 +327,6 @@ struct PrepParams {
   int M;
   int blocks_total;
   int zero_words;      // split counters of the main launches of this call, zeroed here
-  int shift_ext;       // B_ext token columns moved up by 8 (the 8-token product kernels, M <= 8)
   unsigned* zero;
   PrepEntry e[NX];
 };
@@ -425,12 +441,7 @@ __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_consta
   const uint2 ev = hard ? make_uint2(0u, 0u) : make_uint2(hb * 0x10001u, lb * 0x10001u);
   uint8_t* ext = out + bext_off(MPAD);
   auto ext_at = [&](int c) { return reinterpret_cast<uint2*>(ext + (c >> 3) * 512 + (j >> 1) * 128 + (c & 7) * 16 + (j & 1) * 8); };
-  if (!P.shift_ext) {
-    *ext_at(i) = ev;
-  } else if (i < 8) {   // MPAD 16 and M <= 8: token i's rows in column i + 8, zeros in column i
-    *ext_at(i + 8) = ev;
-    *ext_at(i) = make_uint2(0u, 0u);
-  }
+  *ext_at(i) = ev;
   float* sig = reinterpret_cast<float*>(out + sig_off(MPAD));
   if (j == 0) sig[i] = __uint_as_float((uint32_t)(127 + 14 + s) << 23);   // 2^(s+14)
   const unsigned bits = __reduce_or_sync(0xffffffffu, (hard && j == 0) ? (1u << i) : 0u);
@@ -942,9 +953,10 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
   constexpr int kMmaWarp = kProdWarp + 1;       // (first) MMA issue warp; owns TMEM
   constexpr int kMmaWarps = NG;                 // one MMA warp per group
-  constexpr int kBB = bblock_bytes(MPAD);
+  constexpr int kTW = token_width(MPAD, MT);      // token columns of a prepared block
+  constexpr int kBB = bblock_bytes(kTW);
   constexpr int kS = stages(MPAD, FMT, MT, NG);
-  constexpr int kSB = stage_bytes(MPAD, FMT);
+  constexpr int kSB = stage_bytes(kTW, FMT);
   constexpr int kBlk = blk_bytes(FMT);
   constexpr int kWSB = w_stage_bytes(FMT);
   constexpr bool kExtInA = ext_in_a(FMT, MT, NG);
@@ -973,6 +985,13 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
     for (int m = 0; m < kMmaWarps; ++m) mbar_init(bar(kBarDrain + m), 1);
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if constexpr (MT == 8) {   // the zero regions the 8-token MMAs read as token columns
+    uint4* z0 = reinterpret_cast<uint4*>(smem + L::kZeroExt);
+    uint4* z1 = reinterpret_cast<uint4*>(smem + L::kZeroMain);
+    for (int k = threadIdx.x; k < kZeroExtBytes / 16; k += blockDim.x) z0[k] = make_uint4(0u, 0u, 0u, 0u);
+    for (int k = threadIdx.x; k < kZeroMainBytes / 16; k += blockDim.x) z1[k] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();   // visible to the tensor cores (async proxy) after the barrier below
   }
   if (warp == 0 && lane < NG) {   // super-blocks of each group
     GroupCursor<TcParams<MAXE, naux(FMT, MAXE)>, NG> cur;
@@ -1078,6 +1097,7 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
 #pragma unroll
       for (int h = 0; h < NG; ++h) if (h == g) ngl = n[h];
       const uint32_t abase = tmem + a_col(g, FMT, MT, NG);
+      const uint32_t zext = smem_addr(smem + L::kZeroExt), zmain = smem_addr(smem + L::kZeroMain);
       const uint32_t d1 = tmem + acc1_col(MPAD, g, FMT, MT, NG);
       const uint32_t d2 = tmem + acc2_col(MPAD, g, FMT, MT, NG);
       uint32_t gbits = 0;   // parity of this group's full barrier of each stage
@@ -1087,7 +1107,8 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
         gbits ^= 1u << ws;
         tc::fence_after_sync();
         const uint32_t bslot = sW + ws * kSB + kWSB;
-        const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, 4096);   // + 16 per MMA: 256 bytes
+        // token columns 8..15 (the second group of 8): 4096 bytes further, or the zero region
+        const uint64_t bdesc = tc::smem_desc_kmajor(bslot, 128, MT == 8 ? zmain - bslot : 4096u);   // + 16 per MMA: 256 bytes
         tc::mma_f16_ts_x8(d1, abase, bdesc, 16, idesc, 0);
         if constexpr (kAccInA) tc::commit(bar(kBarH0Done + g));   // the group may reuse these A columns
         if (!wait(bar(kBarAFull + 2 * g + 1), (uint32_t)i & 1u)) break;
@@ -1102,7 +1123,9 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
           // the min term: A_ext (16 columns, K = 32) against B_ext, into the product's
           // accumulator (8 token columns: B_ext fills columns 8..15) or its own
           constexpr bool kShiftExt = MT == 8;   // the min term in columns 8..15 of d1
-          const uint64_t edesc = tc::smem_desc_kmajor(bslot + bext_off(MPAD), 128, 512);
+          // 8 tokens: columns 0..7 from the zero region, the tokens' rows as columns 8..15
+          const uint64_t edesc = MT == 8 ? tc::smem_desc_kmajor(zext, 128, bslot + bext_off(kTW) - zext)
+                                         : tc::smem_desc_kmajor(bslot + bext_off(kTW), 128, 512);
           const uint32_t ea = abase + (kExtInA ? 0u : 128u);
           if constexpr (kAccInA && !kExtInA) {
             if (!wait(bar(kBarH0Done + g), (uint32_t)i & 1u)) break;   // no MMA still reads d2's columns
@@ -1172,8 +1195,8 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
       const uint32_t xblk = sW + A.ws * kSB + kWSB;
       A.hd = FMT == kFmtINT4 ? make_uint4(0, 0, 0, 0) : lds128(rb);
       float* sg = sigw + 32 * (i & 1);
-      if (lane < MT / 4) *reinterpret_cast<uint4*>(sg + 4 * lane) = lds128(xblk + sig_off(MPAD) + 16 * lane);
-      A.hmask = lds_u32(xblk + mask_off(MPAD)) & (MT == 32 ? 0xFFFFFFFFu : ((1u << MT) - 1u));
+      if (lane < MT / 4) *reinterpret_cast<uint4*>(sg + 4 * lane) = lds128(xblk + sig_off(kTW) + 16 * lane);
+      A.hmask = lds_u32(xblk + mask_off(kTW)) & (MT == 32 ? 0xFFFFFFFFu : ((1u << MT) - 1u));
       return true;
     };
 
@@ -1339,7 +1362,7 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
           // hard tokens: this row's part of their outputs on CUDA cores (added after the
           // accumulator in the epilogue of this super-block)
           if (A.hmask != 0u)   // uniform over the CTA: the mask belongs to the super-block of X
-            hard_dot<FMT, MPAD, MT>(rb, xblk, P.aux[nx.e], P.e[nx.e].N, nx.tile * kTileRows + r, nx.sb, hd, A.hmask,
+            hard_dot<FMT, kTW, MT>(rb, xblk, P.aux[nx.e], P.e[nx.e].N, nx.tile * kTileRows + r, nx.sb, hd, A.hmask,
                                     hard_sum);
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
@@ -1694,7 +1717,6 @@ cudaError_t launch_prep_n(const std::vector<std::pair<const uint16_t*, int64_t>>
   prep.M = M;
   prep.zero = zero;
   prep.zero_words = (int)zero_words;
-  prep.shift_ext = (MPAD == 16 && M <= 8) ? 1 : 0;   // the 8-token kernels read the min term from columns 8..15
   int blocks = 0;
   for (size_t u = 0; u < xs.size(); ++u) {
     prep.e[u] = PrepEntry{xs[u].first, outs[u], (int)xs[u].second, blocks};
@@ -1737,7 +1759,10 @@ cudaError_t run_tc(const Job* jobs, int count, int M, cudaStream_t stream,
   }
   static std::mutex mu;
   std::lock_guard<std::mutex> g(mu);
-  cudaError_t err = launch_prep<MPAD, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream);
+  // the blocks hold 8 token columns for the 8-token kernels (M <= 8), else MPAD
+  cudaError_t err = (MPAD == 16 && M <= 8)
+                        ? launch_prep<8, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream)
+                        : launch_prep<MPAD, FMT == kFmtNVFP4>(xs, outs, counters, zero_words, M, stream);
   if (err != cudaSuccess) return err;
   if (count == 1)
     return launch_main<FMT, MPAD, 1>(jobs, bsrc.data(), sp.data(), part.data(), ctr.data(), 1, M,
@@ -1774,7 +1799,7 @@ template <int FMT, int MPAD>
 cudaError_t launch_tc_t(const Job* jobs, int count, int M, cudaStream_t stream) {
   static_assert(sizeof(TcParams<kMaxEBatch, 1>) < 32000 && sizeof(PrepParams<kMaxPrep>) < 32000 &&
                 sizeof(TcParams<kMaxEBatch, kMaxEBatch>) <= 32764, "kernel parameters too large");   // the launch limit
-  constexpr int kBB = bblock_bytes(MPAD);
+  const int kBB = bblock_bytes(MPAD == 16 && M <= 8 ? 8 : MPAD);   // one prepared block
   // distinct activations (an X pointer with its K) get one prepared block run each
   std::vector<std::pair<const uint16_t*, int64_t>> xs;
   std::vector<int> xidx(count);
@@ -1876,7 +1901,7 @@ bool tc_supports(int M, int64_t N, int64_t K) {
 size_t noalloc_scratch_bytes() { return kNoallocScratchBytes; }
 
 size_t noalloc_scratch_needed(int M, int64_t K) {
-  return (size_t)(K / 256) * (size_t)bblock_bytes(M <= 16 ? 16 : 32);
+  return (size_t)(K / 256) * (size_t)bblock_bytes(M <= 8 ? 8 : (M <= 16 ? 16 : 32));
 }
 
 cudaError_t launch_tc_noalloc(const Job& job, int M, cudaStream_t stream) {

@@ -191,9 +191,9 @@ int qmm_select_variant_batched(const qmm_entry* entries_host, int count, int M);
  * never does: it computes the same product with the tensor-core kernel and keeps the prepared
  * activations in a fixed buffer of QMM_NOALLOC_SCRATCH_BYTES (4 MiB) that is part of the
  * library's device image, held by every GPU that loads the library until the process exits.
- *   - Limit: (K/256) * (Mpad*580 + 16) bytes must fit, Mpad = 16 for M <= 16 and 32 above:
- *     K <= 57600 for M > 16, K <= 115456 for M <= 16.  Larger problems return QMM_ERR_SCRATCH
- *     before anything is enqueued.
+ *   - Limit: (K/256) * (T*580 + 16) bytes must fit, T = 8 for M <= 8, 16 for M <= 16 and 32
+ *     above: K <= 230400 for M <= 8, K <= 115456 for M <= 16, K <= 57600 for M > 16.  Larger
+ *     problems return QMM_ERR_SCRATCH before anything is enqueued.
  *   - The first call on each device looks up the buffer's device address (cudaGetSymbolAddress)
  *     with that device current; make that first call before any stream capture.
  *   - Every call shares the one buffer and leaves its contents behind; each call writes every

@@ -64,9 +64,10 @@ def test_noalloc_matches_qmm_run_on_two_calls_in_a_row(qmm, oracle_lib):
         assert np.all(np.abs(y_new - Yref) <= TOL * S)
 
 
-def _limit_k(mpad):
-    """Largest K the fixed buffer takes: (K/256) prepared blocks of Mpad * 580 + 16 bytes."""
-    return (4 << 20) // (mpad * 580 + 16) * 256
+def _limit_k(tw):
+    """Largest K the fixed buffer takes: (K/256) prepared blocks of tw * 580 + 16 bytes (tw: the
+    token columns a block stores, 8 for M <= 8, 16 for M <= 16, 32 above)."""
+    return (4 << 20) // (tw * 580 + 16) * 256
 
 
 def test_noalloc_rejects_problems_larger_than_its_buffer(qmm):
@@ -74,15 +75,16 @@ def test_noalloc_rejects_problems_larger_than_its_buffer(qmm):
     p = ctypes.c_void_p(256)   # never dereferenced: the size check comes before any GPU work
     assert lib.qmm_run_noalloc(p, 8, _limit_k(32) + 256, p, p, 32, None) == 10   # one super-block too many, Mpad 32
     assert lib.qmm_run_noalloc(p, 8, _limit_k(16) + 256, p, p, 16, None) == 10   # and at Mpad 16
+    assert lib.qmm_run_noalloc(p, 8, _limit_k(8) + 256, p, p, 8, None) == 10     # and with 8 token columns
     assert lib.qmm_strerror(10).startswith(b"qmm_run_noalloc")
 
 
-@pytest.mark.parametrize("M", [32, 16])
+@pytest.mark.parametrize("M", [32, 16, 8])
 def test_noalloc_accepts_the_largest_problem_its_buffer_holds(qmm, oracle_lib, M):
     """At exactly the limit the call runs, and agrees with qmm_run within the tolerance."""
     lib = qmm.load()
     stream = torch.cuda.current_stream().cuda_stream
-    N, K = 40, _limit_k(32 if M > 16 else 16)
+    N, K = 40, _limit_k(32 if M > 16 else (16 if M > 8 else 8))
     Wq = oracle_lib.pack(inputs.weights_f32(N, K, 71))
     X = inputs.activations_bf16_bits(M, K, 72)
     Wd, Xd = _dev(Wq), _dev_x(X)
