@@ -87,6 +87,11 @@ q4k_fma_kernel(const __grid_constant__ FmaParams<MAXE> P) {
     fence_barrier_init();
   }
   __syncwarp();
+  // programmatic dependent launch: the next launch in the stream may be scheduled from now on
+  // (it waits for this grid before it touches memory); this grid may have started before the
+  // kernel ahead of it finished, so it reads and writes nothing before that one is complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const uint64_t pol = policy_evict_first();
   uint32_t boxes_done = 0;    // boxes consumed by this warp so far (ring position)
@@ -351,8 +356,17 @@ cudaError_t launch_fma_t(const Job* jobs, int count, int M, cudaStream_t stream)
     }
   }
   const int grid = std::min(tasks, slots);
-  kern<<<grid, kThreads, smem, stream>>>(P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace

@@ -352,7 +352,9 @@ __device__ __forceinline__ __half2 bits2h(uint32_t v) { return *reinterpret_cast
 template <int MPAD, int NX, bool NAT>
 __global__ void __launch_bounds__(8 * MPAD) q4k_xprep_kernel(const __grid_constant__ PrepParams<NX> P) {
   // the product kernel that follows may start its prologue now (programmatic dependent launch);
-  // it waits for this grid's completion before it reads what this grid writes
+  // it waits for this grid's completion before it reads what this grid writes.  This grid itself
+  // is launched in plain stream order: everything before it is complete, so the product's early
+  // weight copies read finished data.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ unsigned s_hard[8 * MPAD / 32];
   const int b = blockIdx.x;
@@ -949,6 +951,12 @@ __global__ void __launch_bounds__(cta_threads(NG), 1)
     q4k_tc_kernel(const __grid_constant__ TcParams<MAXE, naux(FMT, MAXE)> P) {
   static_assert(MT == 8 || MT == MPAD, "token columns");
   extern __shared__ __align__(1024) uint8_t smem[];
+  // programmatic dependent launch: the next launch in the stream may be scheduled from now on,
+  // onto SMs this grid leaves.  That is another product launch of the same call (it issues
+  // weight copies, which no launch of the call writes, then waits for this grid's completion)
+  // or a CUDA-core product (it waits before it touches memory); the other kernels, the
+  // preparation among them, start in plain stream order.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using L = TcSmem<MPAD, FMT, MT, NG>;
   constexpr int kProdWarp = NG * kGroupWarps;   // copies
   constexpr int kMmaWarp = kProdWarp + 1;       // (first) MMA issue warp; owns TMEM
@@ -1723,6 +1731,8 @@ cudaError_t launch_prep_n(const std::vector<std::pair<const uint16_t*, int64_t>>
     blocks += (int)(xs[u].second / 256);
   }
   prep.blocks_total = blocks;
+  // plain stream order (launched early after a product kernel, this grid's CTAs waited on the
+  // SMs that product left: single products at M >= 8 took 3-9 us longer on GB300)
   q4k_xprep_kernel<MPAD, NX, NAT><<<blocks, 8 * MPAD, 0, stream>>>(prep);
   return cudaGetLastError();
 }

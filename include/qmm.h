@@ -71,6 +71,11 @@
  *     workspace.  Every other buffer is the caller's.  qmm_run_noalloc allocates nothing.
  *   - Calls on different streams may run concurrently; the mutable global state (the workspace
  *     pool, a per-device cache of launch attributes and of tensor maps) is guarded by locks.
+ *   - Stream order: the product kernels use programmatic dependent launch (each allows the next
+ *     launch in the stream to be scheduled early; the library's own kernels wait for their
+ *     predecessor before they depend on it).  A caller's kernel enqueued after a call sees
+ *     every write of it as usual; one launched with programmatic stream serialization itself
+ *     must wait for its prerequisite grid (cudaGridDependencySynchronize) before it reads Y.
  */
 #ifndef QMM_H
 #define QMM_H
