@@ -4,7 +4,7 @@ roofline and ms per 15.8 GB weight pass, per M.
 
 Workload of a step (default): one full 64-layer weight pass of the 27B hybrid model's Q4K
 matrices (per layer q 5120x5120, k and v 1024x5120, o 5120x5120, gate_up 34816x5120,
-down 5120x17408: 384 matrices, 11.89 GB of packed weights) through ONE qmm_run_batched launch
+down 5120x17408: 384 matrices, 11.89 GB of packed weights) through ONE qmm_run_batched call
 with M activation rows (M = 8 by default: the pages' 8-row verify pass).  The weights are far
 larger than L2 (129 MB), so no flush is needed between steps.
 
@@ -609,7 +609,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, dist_ok: bool):
         "config": {
             "workload": "64-layer Q4K weight pass: per layer q 5120x5120, k 1024x5120, v 1024x5120, "
                         "o 5120x5120, gate_up 34816x5120, down 5120x17408 (384 matrices), "
-                        f"M={M} bf16 rows, one qmm_run_batched launch per pass",
+                        f"M={M} bf16 rows, one qmm_run_batched call per pass",
             "M": M, "matrices": info_items, "weight_bytes_per_step": wb,
             "ms_per_15.8GB_pass": round(ms_per_pass(per_gpu_gbps), 4),
             "frac_of_spec_8TBps": round(per_gpu_gbps / SPEC_HBM_GBS, 4),

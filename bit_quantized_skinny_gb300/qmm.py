@@ -220,7 +220,8 @@ def make_entries(items):
 
 
 def run_batched(entries, M: int, stream=None):
-    """One launch over independent products sharing M.  `entries` from make_entries()."""
+    """One call over independent products sharing M (one product launch per 160 products).
+    `entries` from make_entries()."""
     st = load().qmm_run_batched(entries, len(entries), M, _stream_handle(stream))
     _check(st, "qmm_run_batched")
 
@@ -317,7 +318,8 @@ def make_fmt_entries(items):
 
 
 def fmt_run_batched(entries, M: int, stream=None):
-    """Independent products sharing M, weights in any formats: one launch per format present."""
+    """Independent products sharing M, weights in any formats: each format's entries run as one
+    batched call."""
     _check(load().qmm_fmt_run_batched(entries, len(entries), M, _stream_handle(stream)), "qmm_fmt_run_batched")
 
 

@@ -148,12 +148,14 @@ typedef struct {
   int64_t K;
 } qmm_entry;
 
-/* Run `count` independent products that share one M, in ONE kernel launch on `stream`.
+/* Run `count` independent products that share one M in one call on `stream`: one activation
+ * preparation launch, then one product launch per 160 products (their tensor maps ride in the
+ * launch parameters), equal in size, each allowed to start while the one before it finishes.
  * This is one pass over a model's layer matrices when every stream shares the pass
  * ("sixi-asi 0.11", section "Why sixteen streams were the ceiling"): many matrices, each
  * weight read once.  Entries may share X; the Y buffers must not overlap each other, any X
  * or any Wq.  entries_host is read during the call only (the work list travels in the
- * kernel's parameters; nothing is allocated).  Every entry is validated as in qmm_run; the
+ * kernels' parameters; nothing is allocated besides the per-stream workspace).  Every entry is validated as in qmm_run; the
  * first invalid entry's error is returned and nothing is launched. */
 qmm_status qmm_run_batched(const qmm_entry* entries_host, int count, int M, cudaStream_t stream);
 
@@ -348,7 +350,7 @@ typedef struct {
 
 /* Run `count` independent products sharing one M whose weights may be in different formats (a
  * model file mixes k-quant widths, "sixi-asi 0.9", section "Numbers"): the entries are grouped
- * by format and each group runs as qmm_run_batched does (one launch per format present, in
+ * by format and each group runs as qmm_run_batched does (its own launches, the groups in
  * order of format code, on `stream`).  Entries are validated as in qmm_fmt_run; the first
  * invalid entry's error is returned and nothing is launched.  Each result equals the one of a
  * single qmm_fmt_run call bit for bit. */
